@@ -1,0 +1,338 @@
+/*
+ * Plain fp64 CPU oracle for the Kimi Delta Attention (KDA) serving hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link,
+ * load or call this file: only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * What it computes, and where each definition comes from:
+ *
+ *   oracle_gather   "vllm-ascend KDA state copy" page, section "Numeric
+ *                   contract / Gather side": packed row s is cache row idx[s]
+ *                   when 0 <= idx[s] < N and the row's flag is true (or no
+ *                   flags are given); otherwise it is all zeros.  Duplicate
+ *                   indices are legal.  Gap elements between stride(0) and
+ *                   the payload are never read.
+ *   oracle_scatter  same page, "Numeric contract / Scatter side" and "Memory
+ *                   and addressing": every packed row whose index is valid is
+ *                   converted to the cache dtype and written over the
+ *                   payload of that row; invalid indices are skipped, flags
+ *                   play no part, gap elements are never written.
+ *   oracle_prefill  the recurrence of the "KDA's challenges for AI infra"
+ *                   page, section 1.1 (S_t = M_t S_{t-1} + b_t), with
+ *                   M_t = (I - beta_t k_t k_t^T) Diag(exp g_t),
+ *                   b_t = beta_t k_t v_t^T and o_t = scale * S_t^T q_t, run
+ *                   token by token per (sequence, head) over a cu_seqlens
+ *                   varlen batch.  q and k are L2-normalised per (token,
+ *                   head) first, as the "Support Kimi-K3 on NPU" report's
+ *                   extend listing does before its chunk math.
+ *   oracle_decode   one token of the same recurrence per request, reading
+ *                   the state from a cache row by index and writing it back
+ *                   in the cache dtype (the decode route named on the state
+ *                   copy page, "Background").  An invalid index starts from
+ *                   a zero state and writes nothing back.
+ *
+ * Readings where the pages are silent:
+ *   - the state S is K x V; a cache row [H, V, K] holds element (v, k) of
+ *     head h at ((h * V) + v) * K + k, i.e. S stored transposed;
+ *   - L2 normalisation is x / sqrt(sum(x^2) + eps);
+ *   - decay is applied before the delta-rule erase (M_t's factor order);
+ *   - an empty sequence leaves its state unchanged and emits no output;
+ *   - fp32 -> bf16 conversion rounds to nearest, ties to even.
+ *
+ * All floating-point work is fp64.  Inputs arrive already upcast to fp64 by
+ * the caller, so the oracle sees exactly the values the GPU sees.
+ * Parity status: pinned (see tests/test_oracle_pins.py for each pin).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1 };
+
+/* ---- bf16 conversion: round to nearest, ties to even, on the fp32 bits ---- */
+static uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays a quiet NaN */
+    /* add half an ulp of the kept part, plus one more when the kept part is odd */
+    uint32_t keep_lsb = (u >> 16) & 1u;
+    u += 0x7fffu + keep_lsb;
+    return (uint16_t)(u >> 16);
+}
+
+static float orc_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Exported for the bf16 rounding pins. */
+void oracle_f32_to_bf16(const float *x, uint16_t *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = orc_f32_to_bf16(x[i]);
+}
+
+static double orc_load(const void *base, int dtype, int64_t e)
+{
+    if (dtype == ORC_F32) return (double)((const float *)base)[e];
+    return (double)orc_bf16_to_f32(((const uint16_t *)base)[e]);
+}
+
+/* fp64 -> cache dtype: first to fp32 (round to nearest), then to bf16 (RNE). */
+static void orc_store(void *base, int dtype, int64_t e, double x)
+{
+    float f = (float)x;
+    if (dtype == ORC_F32) ((float *)base)[e] = f;
+    else ((uint16_t *)base)[e] = orc_f32_to_bf16(f);
+}
+
+static int orc_esize(int dtype) { return dtype == ORC_F32 ? 4 : 2; }
+
+/* ------------------------------- state copy ------------------------------- */
+
+/* packed[s, :] = cache[idx[s], :payload] if valid, else zeros.  Element by
+ * element, bitwise.  Returns 0, or -1 on a bad argument. */
+int oracle_gather(const void *cache, int dtype, int64_t n_rows, int64_t payload,
+                  int64_t row_stride, const int64_t *idx, const uint8_t *flags,
+                  int64_t selected, void *packed)
+{
+    if (dtype != ORC_F32 && dtype != ORC_BF16) return -1;
+    if (n_rows <= 0 || payload <= 0 || row_stride < payload || selected < 0) return -1;
+    const int es = orc_esize(dtype);
+    for (int64_t s = 0; s < selected; ++s) {
+        const int64_t r = idx[s];
+        const int valid = r >= 0 && r < n_rows && (flags == NULL || flags[s] != 0);
+        char *dst = (char *)packed + s * payload * es;
+        for (int64_t e = 0; e < payload; ++e) {
+            if (valid)
+                memcpy(dst + e * es, (const char *)cache + (r * row_stride + e) * es, (size_t)es);
+            else
+                memset(dst + e * es, 0, (size_t)es);
+        }
+    }
+    return 0;
+}
+
+/* cache[idx[s], :payload] = to_cache_dtype(packed[s, :]) for valid idx[s]. */
+int oracle_scatter(void *cache, int cache_dtype, int64_t n_rows, int64_t payload,
+                   int64_t row_stride, const int64_t *idx, int64_t selected,
+                   const void *packed, int packed_dtype)
+{
+    if ((cache_dtype != ORC_F32 && cache_dtype != ORC_BF16) ||
+        (packed_dtype != ORC_F32 && packed_dtype != ORC_BF16))
+        return -1;
+    if (n_rows <= 0 || payload <= 0 || row_stride < payload || selected < 0) return -1;
+    for (int64_t s = 0; s < selected; ++s) {
+        const int64_t r = idx[s];
+        if (r < 0 || r >= n_rows) continue;
+        for (int64_t e = 0; e < payload; ++e) {
+            const int64_t src = s * payload + e;
+            const int64_t dst = r * row_stride + e;
+            if (packed_dtype == cache_dtype) {
+                const int es = orc_esize(cache_dtype);
+                memcpy((char *)cache + dst * es, (const char *)packed + src * es, (size_t)es);
+            } else if (cache_dtype == ORC_F32) {
+                ((float *)cache)[dst] = orc_bf16_to_f32(((const uint16_t *)packed)[src]);
+            } else {
+                ((uint16_t *)cache)[dst] = orc_f32_to_bf16(((const float *)packed)[src]);
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------- recurrence ------------------------------- */
+
+/* One token of S_t = (I - beta k k^T) Diag(exp g) S_{t-1} + beta k v^T and
+ * o_t = scale * S_t^T q, on S (K x V, row-major S[k * V + v]).
+ * qn, kn: K-long scratch; p: V-long scratch. */
+static void orc_token_step(double *S, int64_t K, int64_t V, const double *q, const double *k,
+                           const double *v, const double *g, double beta, double scale,
+                           int l2norm, double eps, double *o, double *qn, double *kn, double *p)
+{
+    if (l2norm) {
+        double sq = 0.0, sk = 0.0;
+        for (int64_t c = 0; c < K; ++c) {
+            sq += q[c] * q[c];
+            sk += k[c] * k[c];
+        }
+        const double rq = 1.0 / sqrt(sq + eps), rk = 1.0 / sqrt(sk + eps);
+        for (int64_t c = 0; c < K; ++c) {
+            qn[c] = q[c] * rq;
+            kn[c] = k[c] * rk;
+        }
+    } else {
+        for (int64_t c = 0; c < K; ++c) {
+            qn[c] = q[c];
+            kn[c] = k[c];
+        }
+    }
+    /* Diag(exp g) S */
+    for (int64_t c = 0; c < K; ++c) {
+        const double d = exp(g[c]);
+        for (int64_t j = 0; j < V; ++j) S[c * V + j] *= d;
+    }
+    /* (I - beta k k^T) applied to the decayed state: S -= beta k (k^T S) */
+    for (int64_t j = 0; j < V; ++j) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < K; ++c) acc += kn[c] * S[c * V + j];
+        p[j] = acc;
+    }
+    for (int64_t c = 0; c < K; ++c)
+        for (int64_t j = 0; j < V; ++j) S[c * V + j] -= beta * kn[c] * p[j];
+    /* + b_t = beta k v^T */
+    for (int64_t c = 0; c < K; ++c)
+        for (int64_t j = 0; j < V; ++j) S[c * V + j] += beta * kn[c] * v[j];
+    /* o_t = scale * S_t^T q */
+    for (int64_t j = 0; j < V; ++j) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < K; ++c) acc += qn[c] * S[c * V + j];
+        o[j] = scale * acc;
+    }
+}
+
+typedef struct {
+    const double *q, *k, *v, *g, *beta;
+    const int64_t *cu_seqlens;
+    const double *init; /* [B, H, V, K] or NULL */
+    double *out;        /* [T, H, V] */
+    double *final_state;/* [B, H, V, K] */
+    int64_t B, H, K, V;
+    double scale, eps;
+    int l2norm;
+    int64_t n_items;
+    int64_t next; /* work counter, atomically advanced */
+} orc_prefill_job;
+
+static void orc_prefill_item(orc_prefill_job *a, int64_t item, double *S, double *qn, double *kn,
+                             double *p)
+{
+    const int64_t H = a->H, K = a->K, V = a->V;
+    const int64_t b = item / H, h = item % H;
+    for (int64_t j = 0; j < V; ++j)
+        for (int64_t c = 0; c < K; ++c)
+            S[c * V + j] = a->init ? a->init[((b * H + h) * V + j) * K + c] : 0.0;
+    for (int64_t t = a->cu_seqlens[b]; t < a->cu_seqlens[b + 1]; ++t) {
+        orc_token_step(S, K, V, a->q + (t * H + h) * K, a->k + (t * H + h) * K,
+                       a->v + (t * H + h) * V, a->g + (t * H + h) * K, a->beta[t * H + h],
+                       a->scale, a->l2norm, a->eps, a->out + (t * H + h) * V, qn, kn, p);
+    }
+    for (int64_t j = 0; j < V; ++j)
+        for (int64_t c = 0; c < K; ++c)
+            a->final_state[((b * H + h) * V + j) * K + c] = S[c * V + j];
+}
+
+static void *orc_prefill_worker(void *arg)
+{
+    orc_prefill_job *a = (orc_prefill_job *)arg;
+    double *S = (double *)malloc(sizeof(double) * (size_t)(a->K * a->V + 2 * a->K + a->V));
+    if (!S) return (void *)1;
+    double *qn = S + a->K * a->V, *kn = qn + a->K, *p = kn + a->K;
+    for (;;) {
+        const int64_t item = __atomic_fetch_add(&a->next, 1, __ATOMIC_RELAXED);
+        if (item >= a->n_items) break;
+        orc_prefill_item(a, item, S, qn, kn, p);
+    }
+    free(S);
+    return NULL;
+}
+
+static int orc_run_threads(void *(*fn)(void *), void *job, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    int started = 0, rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, fn, job) != 0) break;
+        ++started;
+    }
+    if (started == 0) return fn(job) == NULL ? 0 : -2;
+    for (int i = 0; i < started; ++i) {
+        void *ret = NULL;
+        pthread_join(th[i], &ret);
+        if (ret != NULL) rc = -2;
+    }
+    return rc;
+}
+
+/* Token-by-token prefill over a varlen batch.  q, k, g: [T, H, K]; v: [T, H, V];
+ * beta: [T, H]; cu_seqlens: [B + 1]; init: [B, H, V, K] or NULL (zeros);
+ * out: [T, H, V]; final_state: [B, H, V, K].  Returns 0 or a negative code. */
+int oracle_prefill(const double *q, const double *k, const double *v, const double *g,
+                   const double *beta, const int64_t *cu_seqlens, int64_t B, int64_t H,
+                   int64_t K, int64_t V, const double *init, double scale, int l2norm,
+                   double eps, double *out, double *final_state, int nthreads)
+{
+    if (B < 0 || H <= 0 || K <= 0 || V <= 0) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        if (cu_seqlens[b + 1] < cu_seqlens[b]) return -1;
+    orc_prefill_job a = {q, k, v, g, beta, cu_seqlens, init, out, final_state,
+                         B, H, K, V, scale, eps, l2norm, B * H, 0};
+    return orc_run_threads(orc_prefill_worker, &a, nthreads);
+}
+
+typedef struct {
+    const double *q, *k, *v, *g, *beta;
+    int64_t R, H, K, V;
+    double scale, eps;
+    int l2norm;
+    void *cache;
+    int cache_dtype;
+    int64_t n_rows, row_stride;
+    const int64_t *idx;
+    double *out;
+    int64_t n_items, next;
+} orc_decode_job;
+
+static void *orc_decode_worker(void *arg)
+{
+    orc_decode_job *a = (orc_decode_job *)arg;
+    const int64_t H = a->H, K = a->K, V = a->V;
+    double *S = (double *)malloc(sizeof(double) * (size_t)(K * V + 2 * K + V));
+    if (!S) return (void *)1;
+    double *qn = S + K * V, *kn = qn + K, *p = kn + K;
+    for (;;) {
+        const int64_t item = __atomic_fetch_add(&a->next, 1, __ATOMIC_RELAXED);
+        if (item >= a->n_items) break;
+        const int64_t r = item / H, h = item % H;
+        const int64_t row = a->idx[r];
+        const int valid = row >= 0 && row < a->n_rows;
+        const int64_t base = row * a->row_stride + h * V * K; /* used only when valid */
+        for (int64_t j = 0; j < V; ++j)
+            for (int64_t c = 0; c < K; ++c)
+                S[c * V + j] = valid ? orc_load(a->cache, a->cache_dtype, base + j * K + c) : 0.0;
+        orc_token_step(S, K, V, a->q + (r * H + h) * K, a->k + (r * H + h) * K,
+                       a->v + (r * H + h) * V, a->g + (r * H + h) * K, a->beta[r * H + h],
+                       a->scale, a->l2norm, a->eps, a->out + (r * H + h) * V, qn, kn, p);
+        if (valid)
+            for (int64_t j = 0; j < V; ++j)
+                for (int64_t c = 0; c < K; ++c)
+                    orc_store(a->cache, a->cache_dtype, base + j * K + c, S[c * V + j]);
+    }
+    free(S);
+    return NULL;
+}
+
+/* One decode token per request on cache rows, in place.  q, k, g: [R, H, K];
+ * v: [R, H, V]; beta: [R, H]; cache: n_rows rows of row_stride elements, each
+ * holding [H, V, K]; idx: [R]; out: [R, H, V].  Valid indices must be unique. */
+int oracle_decode(const double *q, const double *k, const double *v, const double *g,
+                  const double *beta, int64_t R, int64_t H, int64_t K, int64_t V, double scale,
+                  int l2norm, double eps, void *cache, int cache_dtype, int64_t n_rows,
+                  int64_t row_stride, const int64_t *idx, double *out, int nthreads)
+{
+    if (R < 0 || H <= 0 || K <= 0 || V <= 0 || n_rows <= 0 || row_stride < H * V * K) return -1;
+    if (cache_dtype != ORC_F32 && cache_dtype != ORC_BF16) return -1;
+    orc_decode_job a = {q, k, v, g, beta, R, H, K, V, scale, eps, l2norm, cache, cache_dtype,
+                        n_rows, row_stride, idx, out, R * H, 0};
+    return orc_run_threads(orc_decode_worker, &a, nthreads);
+}

@@ -1,0 +1,15 @@
+"""Test configuration: the `gpu` marker and import paths.
+
+Tests marked `gpu` need a CUDA device (a GB300) and call the CUDA library
+through its C ABI; everything else runs on the CPU.
+"""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU and the built CUDA library")
