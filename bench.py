@@ -1,0 +1,509 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA serving hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  state gather (16 rows of an fp32 cache [1024,32,128,128], 20% flags false)
+  -> chunked prefill of the varlen batch (16 sequences, lengths U[512,8192],
+     H=32, K=V=128, bf16 q/k/v, fp32 g/beta, chunk 64)
+  -> state scatter of the 16 final states back to their rows
+  -> one decode step (512 requests, bf16 cache [2048,32,128,128], 5% invalid).
+value = prefill tokens per second of the whole step (decode time included).
+The state-copy bandwidth of the copy workload (fp32 cache [4096,32,128,128]
+with 64 KiB page gaps, 256 rows) is measured in the same run and reported
+next to it, as the metric names both.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+With --gpus N > 1 the script runs under torchrun, one replica per GPU (the
+path has no exchange step), and reports the aggregate.  --impl reference runs
+the fp64 CPU oracle on the host cores, a bounded sample of the workload per
+step.  Prints ONE JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (H=32,K=V=128) + state gather/scatter GB/s vs HBM peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- ranks --
+
+class Ranks:
+    def __init__(self, want: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = False
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = True
+        self.want = want
+
+    def barrier(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "max")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "sum")
+
+    def _reduce(self, x: float, op: str) -> float:
+        if not self.pg:
+            return x
+        import torch.distributed as dist
+        dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+def aggregate(units_per_rank: float, seconds_per_rank: float, ranks: Ranks) -> tuple:
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    total_units = ranks.sum(units_per_rank)
+    slowest = ranks.max(seconds_per_rank)
+    return total_units / slowest, slowest
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.tmp.read())) if len(r) >= 9]
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- peaks --
+
+def peaks() -> tuple:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, only while the kernel
+    source it was taken from is unchanged (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["bytes_per_launch"] if h == rec["source_sha256_16"] else None
+
+
+# ------------------------------------------------------------- workloads --
+
+def build_inputs(dev, seed=0):
+    import kimi_delta_attention_varlen_gb300 as kda
+    from kimi_delta_attention_varlen_gb300 import workloads as wl
+    w = wl.varlen(seed)
+    H, D = w.H, w.K
+    cu = [0]
+    for n in w.lengths:
+        cu.append(cu[-1] + n)
+    T = cu[-1]
+    P = {}
+    P["w"] = w
+    P["cu_list"] = cu
+    P["cache3"] = wl.paged_cache(w.cache_rows, H, D, D, w.cache_dtype, w.cache_stride, seed=seed + 1, device=dev)
+    P["inp"] = wl.token_inputs(T, H, D, D, w.io_dtype, seed=seed, device=dev)
+    P["cu"] = torch.tensor(cu, dtype=torch.int32, device=dev)
+    P["gidx"] = w.gather_idx.to(dev)
+    P["gflags"] = w.gather_flags.to(dev)
+    P["sidx"] = w.scatter_idx.to(dev)
+    P["packed"] = torch.empty(w.B, H, D, D, dtype=torch.float32, device=dev)
+    P["final"] = torch.empty(w.B, H, D, D, dtype=torch.float32, device=dev)
+    P["out"] = torch.empty(T, H, D, dtype=w.io_dtype, device=dev)
+    P["ws"] = torch.empty(kda.kda_prefill_workspace_size(T, w.B, H, D, D), dtype=torch.uint8, device=dev)
+    dw = wl.decode(seed)
+    P["dw"] = dw
+    P["cache5"] = wl.paged_cache(dw.cache_rows, dw.H, dw.V, dw.K, dw.cache_dtype, None, seed=seed + 2, device=dev)
+    P["dinp"] = wl.token_inputs(dw.R, dw.H, dw.K, dw.V, dw.io_dtype, seed=seed + 3, device=dev)
+    P["didx"] = dw.idx.to(dev)
+    P["dout"] = torch.empty(dw.R, dw.H, dw.V, dtype=dw.io_dtype, device=dev)
+    return P
+
+
+def run_step(P, ev=None):
+    """gather -> prefill -> scatter -> decode on the current stream.  `ev`: dict of
+    events recorded at the boundaries (for the per-kernel breakdown)."""
+    import kimi_delta_attention_varlen_gb300 as kda
+    inp, d = P["inp"], P["dinp"]
+    if ev:
+        ev["g0"].record()
+    kda.kda_state_gather(P["cache3"].view, P["gidx"], P["packed"], P["gflags"])
+    kda.kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], P["cu"], P["out"], P["ws"],
+                           init_state=P["packed"], final_state=P["final"],
+                           events=None if not ev else [ev["p0"], ev["p1"], ev["p2"], ev["p3"]])
+    kda.kda_state_scatter(P["cache3"].view, P["sidx"], P["final"])
+    if ev:
+        ev["s1"].record()
+    kda.kda_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], P["cache5"].view, P["didx"], P["dout"])
+    if ev:
+        ev["d1"].record()
+
+
+LAUNCHES_PER_STEP = 6  # gather, chunk table, chunk prep, state pass, scatter, decode
+
+
+def prefill_bytes(P) -> dict:
+    """Algorithmic bytes of the step's kernels (each kernel's compulsory reads and writes)."""
+    w, T, H, D = P["w"], P["cu_list"][-1], P["w"].H, P["w"].K
+    io = 2  # bf16
+    B = w.B
+    n_chunks = sum((n + 63) // 64 for n in w.lengths)
+    rec = (3 * 64 * D * 2) + 64 * 64 * 2 + D * 4 + D * 64 * 2
+    token_in = T * H * (3 * D * io + D * 4 + 4)
+    state = B * H * D * D * 4
+    method = token_in + T * H * D * io + 2 * state  # q,k,v,g,beta in; o out; init in, final out
+    return {"method": method, "prep": token_in + n_chunks * H * rec, "pass": n_chunks * H * rec + T * H * D * io
+            + 2 * state, "n_chunks": n_chunks}
+
+
+def prefill_flops(P) -> float:
+    """Dense 64-tile FLOPs of the chunked form: per chunk and head, the two gated
+    Gram products, W and U (2 * 64*64*D each), and the state pass (W S, Q S,
+    K^T V_new: 2 * 64*D*D each, plus A_qk V_new: 2 * 64*64*D)."""
+    w, D, H = P["w"], P["w"].K, P["w"].H
+    n_chunks = sum((n + 63) // 64 for n in w.lengths)
+    per = 4 * (2 * 64 * 64 * D) + 3 * (2 * 64 * D * D) + 2 * 64 * 64 * D
+    return float(n_chunks * H * per)
+
+
+def copy_measure(dev, steps: int, warmup: int) -> dict:
+    import kimi_delta_attention_varlen_gb300 as kda
+    from kimi_delta_attention_varlen_gb300 import workloads as wl
+    w = wl.copy_fp32()
+    pc = wl.paged_cache(w.N, w.H, w.V, w.K, w.dtype, w.row_stride, seed=w.seed, device=dev)
+    gidx = wl.gather_indices(w.S, w.N, w.p_invalid, seed=w.seed + 1).to(dev)
+    flags = wl.bernoulli_flags(w.S, w.p_flag, seed=w.seed + 2).to(dev)
+    sidx = wl.scatter_indices(w.S, w.N, w.p_invalid, seed=w.seed + 3).to(dev)
+    packed = torch.empty(w.S, w.H, w.V, w.K, dtype=w.dtype, device=dev)
+    P = w.H * w.V * w.K
+    g_cpu, s_cpu = gidx.cpu(), sidx.cpu()
+    n_g = int(((g_cpu >= 0) & (g_cpu < w.N) & flags.cpu()).sum())
+    n_s = int(((s_cpu >= 0) & (s_cpu < w.N)).sum())
+    g_bytes = (n_g + w.S) * P * 4          # read valid rows, write every packed row
+    s_bytes = 2 * n_s * P * 4              # read + write each valid row
+    res = {}
+    for name, fn, nbytes in (("gather", lambda: kda.kda_state_gather(pc.view, gidx, packed, flags), g_bytes),
+                             ("scatter", lambda: kda.kda_state_scatter(pc.view, sidx, packed), s_bytes)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        res[name] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes}
+    del pc, packed
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "index_dtype": "int32", **res}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def cpu_baseline(P, target_s: float = 12.0, steps: int | None = None) -> dict:
+    """The oracle as it stands, timed on the host cores on a bounded sample of the
+    prefill workload: the shortest sequences, all heads, from their gathered
+    initial states."""
+    import numpy as np
+
+    import oracle
+    w, cu = P["w"], P["cu_list"]
+    order = sorted(range(w.B), key=lambda b: w.lengths[b])
+    nthreads = os.cpu_count() or 1
+
+    def host(b):
+        t0, t1 = cu[b], cu[b + 1]
+        inp = P["inp"]
+        sl = [inp[k][t0:t1].detach().cpu().double().numpy() for k in ("q", "k", "v", "g", "beta")]
+        return sl, P["packed"][b:b + 1].cpu().double().numpy()
+
+    # calibrate on the shortest sequence, then size the sample to ~target_s
+    sl, ini = host(order[0])
+    t = time.perf_counter()
+    oracle.prefill(*sl, [0, sl[0].shape[0]], init=ini, scale=w.K ** -0.5, nthreads=nthreads)
+    dt = time.perf_counter() - t
+    rate = sl[0].shape[0] / max(dt, 1e-9)
+    budget = rate * target_s
+    chosen, tok = [], 0
+    for b in order:
+        if tok + w.lengths[b] > budget and chosen:
+            break
+        chosen.append(b)
+        tok += w.lengths[b]
+    parts = [host(b) for b in chosen]
+    q, k, v, g, beta = (np.concatenate([p[0][i] for p in parts]) for i in range(5))
+    ini = np.concatenate([p[1] for p in parts])
+    cu_s = [0]
+    for b in chosen:
+        cu_s.append(cu_s[-1] + w.lengths[b])
+    t = time.perf_counter()
+    oracle.prefill(q, k, v, g, beta, cu_s, init=ini, scale=w.K ** -0.5, nthreads=nthreads)
+    dt = time.perf_counter() - t
+    return {"value": tok / dt, "unit": UNIT, "cores": min(nthreads, len(chosen) * w.H), "kind": "oracle",
+            "sample": f"{len(chosen)} shortest sequences ({tok} tokens) x {w.H} heads of the varlen workload, "
+                      f"fp64 token-by-token recurrence, {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ main --
+
+def native(args, ranks: Ranks) -> dict | None:
+    import kimi_delta_attention_varlen_gb300 as kda  # noqa: F401  (fails loudly if libkda.so is missing)
+    dev = torch.device("cuda", ranks.local)
+    torch.cuda.set_device(dev)
+    P = build_inputs(dev)
+    T = P["cu_list"][-1]
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        run_step(P)
+    torch.cuda.synchronize()
+
+    names = ["g0", "p0", "p1", "p2", "p3", "s1", "d1"]
+    evs = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(args.steps)]
+    for e in evs:  # create the events outside the timed region
+        for x in e.values():
+            x.record()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(ranks.local)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record(stream)
+    for i in range(args.steps):
+        run_step(P, evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    sec = start.elapsed_time(stop) * 1e-3
+    value, slowest = aggregate(T * args.steps, sec, ranks)
+
+    def med(a, b):
+        return statistics.median(e[a].elapsed_time(e[b]) for e in evs)
+
+    br = {"gather": med("g0", "p0"), "chunk_table": med("p0", "p1"), "chunk_prep": med("p1", "p2"),
+          "state_pass": med("p2", "p3"), "scatter": med("p3", "s1"), "decode": med("s1", "d1")}
+
+    # end to end through the public API: pinned host inputs -> device, step, results -> host
+    inp = P["inp"]
+    host_in = {k: inp[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    host_d = {k: P["dinp"][k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    small = {k: P[k].cpu().pin_memory() for k in ("cu", "gidx", "gflags", "sidx", "didx")}
+    host_out = torch.empty(P["out"].shape, dtype=P["out"].dtype).pin_memory()
+    host_dout = torch.empty(P["dout"].shape, dtype=P["dout"].dtype).pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in (*host_in.values(), *host_d.values(), *small.values()))
+    bo = host_out.numel() * host_out.element_size() + host_dout.numel() * host_dout.element_size()
+
+    def e2e_step():
+        for k2, t in host_in.items():
+            inp[k2].copy_(t, non_blocking=True)
+        for k2, t in host_d.items():
+            P["dinp"][k2].copy_(t, non_blocking=True)
+        for k2, t in small.items():
+            P[k2].copy_(t, non_blocking=True)
+        run_step(P)
+        host_out.copy_(P["out"], non_blocking=True)
+        host_dout.copy_(P["dout"], non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(min(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    ranks.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_value, _ = aggregate(T * e2e_steps, a.elapsed_time(b) * 1e-3, ranks)
+
+    copy = copy_measure(dev, max(5, args.steps), max(3, args.warmup))
+    pk, pk_kind = peaks()
+    nb = prefill_bytes(P)
+    flops = prefill_flops(P)
+    prefill_ms = br["chunk_table"] + br["chunk_prep"] + br["state_pass"]
+    # dominant kernel of the step, by measured time
+    kern = {"chunk_prep": (br["chunk_prep"], nb["prep"]), "state_pass": (br["state_pass"], nb["pass"]),
+            "state_gather": (br["gather"], None), "decode_step": (br["decode"], None)}
+    dom = max(kern, key=lambda k2: kern[k2][0])
+    dom_ms, dom_bytes = kern[dom]
+    if dom_bytes is None:
+        dw = P["dw"]
+        dom_bytes = 2 * int((dw.idx >= 0).sum()) * dw.H * dw.K * dw.V * 2
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = traffic_record(dom)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": slowest * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": P["w"].name + " + gather/scatter fp32 cache [1024,32,128,128] + decode R=512",
+                   "tokens_per_step": T, "lengths": P["w"].lengths, "heads": 32, "head_dim": 128, "chunk": 64,
+                   "step": "state gather -> chunked prefill -> state scatter -> decode step",
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ranks.world}"},
+        "breakdown_ms": br,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "peak_source": pk_kind, "bytes_per_launch": dom_bytes},
+        "prefill_roofline": {
+            "ms": prefill_ms, "algorithmic_bytes": nb["method"],
+            "achieved_gbs": nb["method"] / (prefill_ms * 1e-3) / 1e9,
+            "frac_hbm": nb["method"] / (prefill_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "dense_tile_tflops": flops / (prefill_ms * 1e-3) / 1e12,
+            "frac_bf16": flops / (prefill_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+            "attainable_frac": (nb["method"] / (prefill_ms * 1e-3)) /
+                               min(pk["bf16_tflops"] * 1e12 * nb["method"] / flops, pk["hbm_gbs"] * 1e9),
+            "flop_convention": "dense 64x64 tiles", "peak_source": pk_kind},
+        "state_copy": {**copy, "hbm_peak_gbs": pk["hbm_gbs"],
+                       "gather_frac": copy["gather"]["gbs"] / pk["hbm_gbs"],
+                       "scatter_frac": copy["scatter"]["gbs"] / pk["hbm_gbs"]},
+        "decode": {"ms": br["decode"], "requests_per_s": P["dw"].R / (br["decode"] * 1e-3)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    if ranks.rank == 0 and ranks.world == 1:
+        result["cpu_baseline"] = cpu_baseline(P)
+    return result if ranks.rank == 0 else None
+
+
+def reference(args, ranks: Ranks) -> dict | None:
+    """The oracle arm: each step runs the fp64 CPU oracle on a bounded sample of
+    the same workload (rank 0 only)."""
+    if ranks.rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    from kimi_delta_attention_varlen_gb300 import workloads as wl
+    w = wl.varlen()
+    cu = [0]
+    for n in w.lengths:
+        cu.append(cu[-1] + n)
+    b = min(range(w.B), key=lambda i: w.lengths[i])  # the shortest sequence, all heads
+    L = w.lengths[b]
+    inp = wl.token_inputs(L, w.H, w.K, w.V, w.io_dtype, seed=0, device="cpu")  # same shapes and draws
+    sl = [inp[k].double().numpy() for k in ("q", "k", "v", "g", "beta")]
+    init = np.zeros((1, w.H, w.V, w.K))
+    nthreads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.prefill(*sl, [0, L], init=init, scale=w.K ** -0.5, nthreads=nthreads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.prefill(*sl, [0, L], init=init, scale=w.K ** -0.5, nthreads=nthreads)
+    sec = time.perf_counter() - t
+    value = L * args.steps / sec
+    sample = (f"1 sequence of {L} tokens (the workload's shortest length) x {w.H} heads per step, same "
+              f"distributions, fp64 oracle")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(nthreads, w.H), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ranks = Ranks(args.gpus)
+    try:
+        res = reference(args, ranks) if args.impl == "reference" else native(args, ranks)
+    finally:
+        ranks.close()
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

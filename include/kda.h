@@ -1,0 +1,242 @@
+/*
+ * kda.h - C ABI of the GB300 (sm_103a) Kimi Delta Attention (KDA) hot path.
+ *
+ * Four operations, each an asynchronous launch on a caller-given CUDA stream:
+ *
+ *   kda_state_gather    per-request recurrent state gather from a paged cache
+ *   kda_prefill_varlen  chunkwise (C = 64) gated delta-rule prefill over a
+ *                       cu_seqlens varlen batch
+ *   kda_state_scatter   final-state scatter back to cache rows
+ *   kda_decode_step     one-token recurrent decode step on cache rows
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer unless stated otherwise; the
+ *     caller owns every buffer.  The library keeps no pointer, stream or
+ *     buffer after a call returns, allocates no memory and never
+ *     synchronises the host with the device.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued on it and nothing else.
+ *   - All argument checks run on the host, on metadata only, before anything
+ *     is launched.  A failed check returns a negative kda_status and launches
+ *     nothing.  KDA_ERR_CUDA means the launch itself failed (for example no
+ *     device, or an unsupported architecture); its message is available from
+ *     kda_last_cuda_error_string().
+ *   - Device-side index VALUES are never checked on the host (that would need
+ *     a device-to-host copy); the kernels treat out-of-range indices as the
+ *     contract below says.
+ *   - Floating point: states and gates are fp32; q/k/v/o are bf16 or fp32.
+ *     bf16 results are rounded to nearest, ties to even.
+ *
+ * State layout.  A recurrent state S of one head is a K x V matrix.  Cache
+ * rows and packed states store it transposed, as [V][K] (element (v, k) is
+ * S[k][v]), with the heads outermost: one row is [H][V][K], H*V*K elements
+ * ("payload").  Consecutive cache rows are `row_stride` elements apart,
+ * row_stride >= payload; the gap between a row's payload and the next row is
+ * never read or written.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = -1,        /* a required pointer is NULL                       */
+    KDA_ERR_DTYPE = -2,       /* unknown or unsupported element / index type      */
+    KDA_ERR_LAYOUT = -3,      /* cache layout: n_rows <= 0, row_stride < payload  */
+    KDA_ERR_SHAPE = -4,       /* a size is negative / zero where it must not be   */
+    KDA_ERR_RANGE = -5,       /* a size is beyond what the kernels address        */
+    KDA_ERR_WORKSPACE = -6,   /* workspace missing, too small or misaligned       */
+    KDA_ERR_CUDA = -7,        /* the CUDA launch failed                           */
+    KDA_ERR_UNSUPPORTED = -8, /* head size / combination not built                */
+    KDA_ERR_ALIGN = -9        /* a pointer is not aligned to its element size     */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+typedef enum { KDA_I32 = 0, KDA_I64 = 1 } kda_itype;
+
+/* A paged recurrent-state cache [n_rows, h, v, k] with a row stride.
+ * `data` points at element 0 of row 0 (any storage offset already applied).
+ * Layout rule of the "vllm-ascend KDA state copy" page, section "Automatic
+ * dispatch": dtype fp32 or bf16, four dimensions, n_rows > 0, the inner
+ * [h, v, k] block dense, stride(0) >= payload (pages do not overlap). */
+typedef struct {
+    void *data;
+    int32_t dtype;      /* kda_dtype */
+    int32_t reserved;   /* must be 0 */
+    int64_t n_rows;
+    int64_t h, v, k;
+    int64_t row_stride; /* in elements */
+} kda_cache;
+
+/* ------------------------------------------------------------------------
+ * kda_state_gather
+ *
+ * packed[s] = cache[idx[s]]   when 0 <= idx[s] < n_rows and
+ *                             (flags == NULL or flags[s] != 0)
+ * packed[s] = 0               otherwise.
+ * Defined by the "vllm-ascend KDA state copy" page, section "Numeric
+ * contract / Gather side": invalid or negative indices and flag=false rows
+ * yield zeros, flags=None gathers every valid row, duplicate indices are
+ * legal, and the packed output is written completely.
+ *
+ *   cache     cache descriptor (host pointer to the struct; data on device)
+ *   idx       [selected] device indices, int32 or int64 (`idx_type`); int32
+ *             indices are read as int32 (no conversion) and every address is
+ *             formed in 64-bit arithmetic, so rows more than 4 GiB apart
+ *             resolve ("Memory and addressing").
+ *   selected  number of rows; 0 returns KDA_OK and launches nothing.
+ *   flags     [selected] device bytes (bool), or NULL.
+ *   packed    [selected, h, v, k] device, contiguous, cache dtype.  Must not
+ *             overlap the cache.
+ * ---------------------------------------------------------------------- */
+int kda_state_gather(const kda_cache *cache, const void *idx, int32_t idx_type,
+                     int64_t selected, const uint8_t *flags, void *packed, void *stream);
+
+/* ------------------------------------------------------------------------
+ * kda_state_scatter
+ *
+ * cache[idx[s]] = convert(packed[s]) for every s with 0 <= idx[s] < n_rows;
+ * other s are skipped.  Defined by the same page, "Numeric contract /
+ * Scatter side": invalid targets are skipped, initial-state flags play no
+ * part, and the final state is converted to the cache dtype before it is
+ * written ("Memory and addressing").  Gap elements and rows not selected
+ * are never touched.
+ *
+ *   packed        [selected, h, v, k] device, contiguous, `packed_dtype`
+ *                 (fp32 or bf16; fp32 -> bf16 rounds to nearest even,
+ *                 bf16 -> fp32 is exact).
+ *   Preconditions (not checked, no host sync): valid targets are unique;
+ *   packed does not overlap the cache; no concurrent writer.
+ * ---------------------------------------------------------------------- */
+int kda_state_scatter(const kda_cache *cache, const void *idx, int32_t idx_type,
+                      int64_t selected, const void *packed, int32_t packed_dtype, void *stream);
+
+/* ------------------------------------------------------------------------
+ * kda_prefill_workspace_size
+ *
+ * Bytes of device workspace kda_prefill_varlen needs for a batch of
+ * `num_seqs` sequences totalling `total_tokens` tokens, `h` heads and head
+ * sizes dk, dv.  The size depends only on these numbers (an upper bound on
+ * the chunk count is used), never on device data.  Returns 0 for an
+ * unsupported combination.
+ * ---------------------------------------------------------------------- */
+size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t dk,
+                                  int32_t dv);
+
+/* ------------------------------------------------------------------------
+ * kda_prefill_varlen
+ *
+ * For every sequence b (tokens cu_seqlens[b] .. cu_seqlens[b+1]-1) and head:
+ *   S <- init_state[b] (zeros when init_state == NULL)
+ *   for each token t in order:
+ *     q_t, k_t <- L2-normalised (x / sqrt(sum x^2 + 1e-6)) when qk_l2norm
+ *     S   <- (I - beta_t k_t k_t^T) Diag(exp g_t) S + beta_t k_t v_t^T
+ *     o_t <- scale * S^T q_t
+ *   final_state[b] <- S
+ * The recurrence is the one of the "KDA's challenges for AI infra" page,
+ * section 1.1; the kernels evaluate it chunkwise, 64 tokens at a time, in
+ * the order of the "Support Kimi-K3 on NPU" report's extend listing
+ * (l2norm -> chunk table -> in-chunk gate cumsum -> gated K K^T and Q K^T ->
+ * triangular solve -> W, U -> inter-chunk state pass -> output).  Chunks
+ * restart at every sequence start.
+ *
+ *   q, k        [total_tokens, h, dk] device, `io_dtype` (bf16 or fp32)
+ *   v           [total_tokens, h, dv] device, `io_dtype`
+ *   g           [total_tokens, h, dk] device fp32, per-channel log-decay.
+ *               The kernels evaluate exp of partial sums of g inside 16-token
+ *               blocks; results are exact to rounding while every channel's
+ *               decay over any 8 consecutive tokens stays above -80
+ *               (sum of g > -80); the pages' gate -softplus(N(0,1)) stays
+ *               above -30.  g > 0 (growth) is accepted within the same bound.
+ *   beta        [total_tokens, h] device fp32
+ *   cu_seqlens  [num_seqs + 1] device int32, cu_seqlens[0] = 0, non-
+ *               decreasing, cu_seqlens[num_seqs] = total_tokens (precondition,
+ *               not checked).  Empty sequences are allowed: their final state
+ *               equals their initial state.
+ *   num_seqs    >= 1;  total_tokens >= 0 (0: final = init, no output).
+ *   h, dk, dv   heads and head sizes; built: dk == dv in {32, 64, 128}.
+ *   scale       output scale (the report's listing uses dk^-0.5).
+ *   qk_l2norm   1: normalise q and k; 0: use them as given.
+ *   init_state  [num_seqs, h, dv, dk] device, `init_dtype` (fp32 / bf16),
+ *               or NULL for zero initial states.
+ *   final_state [num_seqs, h, dv, dk] device fp32, or NULL (not written).
+ *   out         [total_tokens, h, dv] device, `io_dtype`; must not overlap
+ *               any input (unlike the report's listing, which reuses v's
+ *               buffer, the output is a separate buffer here).
+ *   workspace   device scratch of at least kda_prefill_workspace_size(...)
+ *               bytes, 256-byte aligned; its contents on entry do not matter.
+ *   Calls on one workspace must not overlap in time.
+ * ---------------------------------------------------------------------- */
+int kda_prefill_varlen(const void *q, const void *k, const void *v, int32_t io_dtype,
+                       const float *g, const float *beta, const int32_t *cu_seqlens,
+                       int64_t num_seqs, int64_t total_tokens, int32_t h, int32_t dk, int32_t dv,
+                       float scale, int32_t qk_l2norm, const void *init_state, int32_t init_dtype,
+                       float *final_state, void *out, void *workspace, size_t ws_bytes,
+                       void *stream);
+
+/* ------------------------------------------------------------------------
+ * kda_prefill_varlen_timed
+ *
+ * kda_prefill_varlen, launching the same kernels, that also records four
+ * caller-created CUDA events (cudaEvent_t passed as void*, host array
+ * `events`) on `stream`: events[0] before the chunk-table kernel, events[1]
+ * before the chunk-preparation kernel, events[2] before the state-pass
+ * kernel, events[3] after it.  For measuring each kernel's device time.
+ * events == NULL or any NULL entry returns KDA_ERR_NULL.
+ * ---------------------------------------------------------------------- */
+int kda_prefill_varlen_timed(const void *q, const void *k, const void *v, int32_t io_dtype,
+                             const float *g, const float *beta, const int32_t *cu_seqlens,
+                             int64_t num_seqs, int64_t total_tokens, int32_t h, int32_t dk,
+                             int32_t dv, float scale, int32_t qk_l2norm, const void *init_state,
+                             int32_t init_dtype, float *final_state, void *out, void *workspace,
+                             size_t ws_bytes, void *stream, void *const *events);
+
+/* ------------------------------------------------------------------------
+ * kda_decode_step
+ *
+ * For each request r and head: with row = idx[r],
+ *   S   <- cache[row] (upcast to fp32) when 0 <= row < n_rows, else zeros
+ *   q, k <- L2-normalised when qk_l2norm
+ *   S   <- (I - beta k k^T) Diag(exp g) S + beta k v^T
+ *   o   <- scale * S^T q
+ *   cache[row] <- S converted to the cache dtype, only when row is valid.
+ * One token of the same recurrence (infra page, section 1.1), on cache rows
+ * in place - the decode route named on the state-copy page, "Background".
+ * An invalid index behaves as gather (zeros) -> step -> scatter (skipped).
+ *
+ *   q, k, v     [batch, h, dk] / [batch, h, dv] device, `io_dtype`
+ *   g           [batch, h, dk] device fp32;  beta [batch, h] device fp32
+ *   cache       state cache with cache->h == h, ->k == dk, ->v == dv
+ *   idx         [batch] device int32 / int64
+ *   out         [batch, h, dv] device, `io_dtype`
+ *   Preconditions (not checked): valid indices are unique.
+ *   Built: dk == dv in {32, 64, 128}.  batch == 0 launches nothing.
+ * ---------------------------------------------------------------------- */
+int kda_decode_step(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,
+                    const float *beta, int64_t batch, int32_t h, int32_t dk, int32_t dv,
+                    float scale, int32_t qk_l2norm, const kda_cache *cache, const void *idx,
+                    int32_t idx_type, void *out, void *stream);
+
+/* Human-readable name of a kda_status value (static string, never NULL). */
+const char *kda_status_string(int32_t status);
+
+/* Text of the CUDA error behind the last KDA_ERR_CUDA returned on this host
+ * thread (static storage; "no error" if none). */
+const char *kda_last_cuda_error_string(void);
+
+/* Reads the device-side status word a prefill call leaves in its workspace:
+ * 0 when every internal wait completed, otherwise a non-zero code.  This is
+ * the one call that synchronises: it copies 4 bytes on `stream` and waits. */
+int kda_prefill_workspace_status(const void *workspace, int32_t *status_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

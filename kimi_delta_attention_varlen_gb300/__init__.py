@@ -1,0 +1,194 @@
+"""Kimi Delta Attention (KDA) serving hot path on GB300 (sm_103a).
+
+Thin Python binding of the C ABI in include/kda.h (libkda.so).  The functions
+keep the C names; they take torch tensors (device memory) and only marshal
+arguments - every step of the computation runs in the library's CUDA kernels.
+
+    kda_state_gather(cache, idx, packed, flags=None)
+    kda_state_scatter(cache, idx, packed)
+    kda_prefill_workspace_size(total_tokens, num_seqs, h, dk, dv)
+    kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, out, workspace, ...)
+    kda_decode_step(q, k, v, g, beta, cache, idx, out, ...)
+
+`cache` is a 4-D tensor view [N, H, V, K] whose inner [H, V, K] block is dense
+and whose stride(0) >= H*V*K (page gaps allowed); its data_ptr() already
+includes any storage offset.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._abi import (EXPORTED, KDA_BF16, KDA_F32, KDA_I32, KDA_I64, LIB_PATH, KdaCache, KdaError,
+                   _check, lib)
+
+__all__ = [
+    "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
+    "kda_decode_step", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
+    "KdaError", "EXPORTED", "LIB_PATH",
+]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return KDA_F32
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError(f"expected float32 or bfloat16, got {t.dtype}")
+
+
+def _itype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.int32:
+        return KDA_I32
+    if t.dtype == torch.int64:
+        return KDA_I64
+    raise TypeError(f"indices must be int32 or int64, got {t.dtype}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _need(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def cache_descriptor(cache: torch.Tensor) -> KdaCache:
+    """kda_cache for a [N, H, V, K] view with a dense inner block."""
+    _need(cache.dim() == 4, "cache must be a 4-D view [N, H, V, K]")
+    N, H, V, K = cache.shape
+    for d, want in ((1, V * K), (2, K), (3, 1)):
+        _need(cache.size(d) == 1 or cache.stride(d) == want,
+              "cache rows must hold a dense [H, V, K] block")
+    return KdaCache(cache.data_ptr(), _dtype_code(cache), 0, N, H, V, K, cache.stride(0))
+
+
+def _index_vector(idx: torch.Tensor) -> None:
+    _need(idx.dim() == 1 and idx.is_contiguous(), "indices must be a contiguous 1-D tensor")
+
+
+def kda_state_gather(cache: torch.Tensor, idx: torch.Tensor, packed: torch.Tensor,
+                     flags: torch.Tensor | None = None, stream=None) -> None:
+    """packed[s] = cache[idx[s]] for valid indices with a true flag, else zeros."""
+    d = cache_descriptor(cache)
+    _index_vector(idx)
+    S = idx.numel()
+    _need(packed.is_contiguous() and packed.dtype == cache.dtype and
+          tuple(packed.shape) == (S, *cache.shape[1:]), "packed must be contiguous [S, H, V, K], cache dtype")
+    if flags is not None:
+        _need(flags.dtype in (torch.bool, torch.uint8) and flags.is_contiguous() and flags.numel() == S,
+              "flags must be a contiguous bool tensor of length S")
+    rc = lib().kda_state_gather(ctypes.byref(d), _ptr(idx), _itype_code(idx), S, _ptr(flags), _ptr(packed),
+                                _stream(stream))
+    _check(rc, "kda_state_gather")
+
+
+def kda_state_scatter(cache: torch.Tensor, idx: torch.Tensor, packed: torch.Tensor, stream=None) -> None:
+    """cache[idx[s]] = packed[s] converted to the cache dtype, for valid indices."""
+    d = cache_descriptor(cache)
+    _index_vector(idx)
+    S = idx.numel()
+    _need(packed.is_contiguous() and tuple(packed.shape) == (S, *cache.shape[1:]),
+          "packed must be contiguous [S, H, V, K]")
+    rc = lib().kda_state_scatter(ctypes.byref(d), _ptr(idx), _itype_code(idx), S, _ptr(packed),
+                                 _dtype_code(packed), _stream(stream))
+    _check(rc, "kda_state_scatter")
+
+
+def kda_prefill_workspace_size(total_tokens: int, num_seqs: int, h: int, dk: int, dv: int) -> int:
+    return int(lib().kda_prefill_workspace_size(total_tokens, num_seqs, h, dk, dv))
+
+
+def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, out, workspace, *, scale: float | None = None,
+                       qk_l2norm: bool = True, init_state=None, final_state=None, stream=None,
+                       events=None) -> None:
+    """Chunkwise gated delta-rule prefill over a cu_seqlens varlen batch.
+
+    q, k: [T, H, K]; v, out: [T, H, V] (bf16 or fp32, one dtype); g: [T, H, K] fp32;
+    beta: [T, H] fp32; cu_seqlens: [B + 1] int32; init_state: [B, H, V, K] fp32/bf16 or
+    None; final_state: [B, H, V, K] fp32 or None; workspace: uint8 device tensor of at
+    least kda_prefill_workspace_size(T, B, H, K, V) bytes.  events: optional list of four
+    torch.cuda.Event (timing enabled) recorded at the boundaries of the three kernels
+    (kda_prefill_varlen_timed)."""
+    T, H, K = q.shape
+    V = v.shape[2]
+    B = cu_seqlens.numel() - 1
+    for name, t, shape in (("q", q, (T, H, K)), ("k", k, (T, H, K)), ("v", v, (T, H, V)),
+                           ("out", out, (T, H, V)), ("g", g, (T, H, K)), ("beta", beta, (T, H))):
+        _need(tuple(t.shape) == shape and t.is_contiguous(), f"{name} must be contiguous {shape}")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype and out.dtype == q.dtype, "q, k, v, out share a dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g and beta must be float32")
+    _need(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous() and B >= 1,
+          "cu_seqlens must be a contiguous int32 tensor of B + 1 >= 2 offsets")
+    init_code = 0
+    if init_state is not None:
+        _need(tuple(init_state.shape) == (B, H, V, K) and init_state.is_contiguous(),
+              "init_state must be contiguous [B, H, V, K]")
+        init_code = _dtype_code(init_state)
+    if final_state is not None:
+        _need(tuple(final_state.shape) == (B, H, V, K) and final_state.is_contiguous() and
+              final_state.dtype == torch.float32, "final_state must be contiguous float32 [B, H, V, K]")
+    _need(workspace.dtype == torch.uint8 and workspace.is_contiguous(), "workspace must be a uint8 tensor")
+    if scale is None:
+        scale = K ** -0.5
+    args = (_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g), _ptr(beta), _ptr(cu_seqlens), B, T, H, K, V,
+            float(scale), 1 if qk_l2norm else 0, _ptr(init_state), init_code, _ptr(final_state), _ptr(out),
+            _ptr(workspace), workspace.numel(), _stream(stream))
+    if events is None:
+        _check(lib().kda_prefill_varlen(*args), "kda_prefill_varlen")
+        return
+    _need(len(events) == 4, "events: four torch.cuda.Event")
+    handles = []
+    for ev in events:
+        if not ev.cuda_event:  # torch creates the event lazily at its first record
+            ev.record()
+        handles.append(ev.cuda_event)
+    arr = (ctypes.c_void_p * 4)(*handles)
+    _check(lib().kda_prefill_varlen_timed(*args, arr), "kda_prefill_varlen_timed")
+
+
+def kda_decode_step(q, k, v, g, beta, cache, idx, out, *, scale: float | None = None,
+                    qk_l2norm: bool = True, stream=None) -> None:
+    """One recurrent token per request on cache rows, in place.
+
+    q, k: [R, H, K]; v, out: [R, H, V] (bf16 or fp32); g: [R, H, K] fp32; beta: [R, H] fp32;
+    cache: [N, H, V, K] view; idx: [R] int32/int64."""
+    R, H, K = q.shape
+    V = v.shape[2]
+    for name, t, shape in (("q", q, (R, H, K)), ("k", k, (R, H, K)), ("v", v, (R, H, V)),
+                           ("out", out, (R, H, V)), ("g", g, (R, H, K)), ("beta", beta, (R, H))):
+        _need(tuple(t.shape) == shape and t.is_contiguous(), f"{name} must be contiguous {shape}")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype and out.dtype == q.dtype, "q, k, v, out share a dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g and beta must be float32")
+    _index_vector(idx)
+    _need(idx.numel() == R, "idx must hold one index per request")
+    d = cache_descriptor(cache)
+    if scale is None:
+        scale = K ** -0.5
+    rc = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g), _ptr(beta), R, H, K, V,
+                               float(scale), 1 if qk_l2norm else 0, ctypes.byref(d), _ptr(idx),
+                               _itype_code(idx), _ptr(out), _stream(stream))
+    _check(rc, "kda_decode_step")
+
+
+def kda_status_string(status: int) -> str:
+    return lib().kda_status_string(status).decode()
+
+
+def kda_prefill_workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    """Device status word of the last prefill on this workspace (0 = all waits completed).
+    Synchronises the stream."""
+    out = ctypes.c_int32(-1)
+    _check(lib().kda_prefill_workspace_status(_ptr(workspace), ctypes.byref(out), _stream(stream)),
+           "kda_prefill_workspace_status")
+    return int(out.value)

@@ -1,0 +1,219 @@
+// C ABI of the KDA hot path: argument validation on the host (metadata only,
+// before any launch) and dispatch to the kernel launchers.
+//
+// Fail-closed, as the "vllm-ascend KDA state copy" page requires ("Startup
+// preparation": bad layouts and metadata are rejected before compile or
+// launch; "Numeric contract": an empty selection validates metadata and
+// launches nothing).  No call allocates, synchronises or keeps a pointer.
+#include <cuda_runtime.h>
+
+#include "kda_internal.h"
+
+namespace {
+
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return KDA_OK;
+    t_last_cuda = e;
+    return KDA_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int64_t esize(int32_t dtype) { return dtype == KDA_F32 ? 4 : 2; }
+
+bool valid_dtype(int32_t d) { return d == KDA_F32 || d == KDA_BF16; }
+
+bool valid_itype(int32_t t) { return t == KDA_I32 || t == KDA_I64; }
+
+bool built_head_size(int32_t dk, int32_t dv) { return dk == dv && (dk == 32 || dk == 64 || dk == 128); }
+
+// Layout predicate of the state-copy page ("Automatic dispatch"): fp32/bf16,
+// n_rows > 0, positive inner sizes, rows that do not overlap.
+int check_cache(const kda_cache *c, kda::CacheDesc *out)
+{
+    if (c == nullptr || c->data == nullptr) return KDA_ERR_NULL;
+    if (!valid_dtype(c->dtype)) return KDA_ERR_DTYPE;
+    if (c->reserved != 0) return KDA_ERR_LAYOUT;
+    if (c->n_rows <= 0 || c->h <= 0 || c->v <= 0 || c->k <= 0) return KDA_ERR_LAYOUT;
+    const int64_t lim = INT64_C(1) << 40;
+    if (c->h > lim || c->v > lim || c->k > lim) return KDA_ERR_RANGE;
+    const __int128 payload = static_cast<__int128>(c->h) * c->v * c->k;
+    if (payload > (INT64_C(1) << 40)) return KDA_ERR_RANGE;
+    if (c->row_stride < static_cast<int64_t>(payload)) return KDA_ERR_LAYOUT;
+    const __int128 bytes = static_cast<__int128>(c->n_rows) * c->row_stride * esize(c->dtype);
+    if (bytes > (static_cast<__int128>(1) << 62)) return KDA_ERR_RANGE;
+    if (!aligned(c->data, static_cast<uintptr_t>(esize(c->dtype)))) return KDA_ERR_ALIGN;
+    *out = kda::CacheDesc{c->data, c->dtype, c->n_rows, c->h, c->v, c->k, c->row_stride};
+    return KDA_OK;
+}
+
+int check_index_array(const void *idx, int32_t idx_type)
+{
+    if (idx == nullptr) return KDA_ERR_NULL;
+    if (!aligned(idx, idx_type == KDA_I32 ? 4 : 8)) return KDA_ERR_ALIGN;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_state_gather(const kda_cache *cache, const void *idx, int32_t idx_type, int64_t selected,
+                     const uint8_t *flags, void *packed, void *stream)
+{
+    kda::CacheDesc c{};
+    int rc = check_cache(cache, &c);
+    if (rc != KDA_OK) return rc;
+    if (!valid_itype(idx_type)) return KDA_ERR_DTYPE;
+    if (selected < 0) return KDA_ERR_SHAPE;
+    if (selected == 0) return KDA_OK;
+    if ((rc = check_index_array(idx, idx_type)) != KDA_OK) return rc;
+    if (packed == nullptr) return KDA_ERR_NULL;
+    if (!aligned(packed, static_cast<uintptr_t>(esize(c.dtype)))) return KDA_ERR_ALIGN;
+    if (static_cast<__int128>(selected) * c.h * c.v * c.k * esize(c.dtype) > (static_cast<__int128>(1) << 62))
+        return KDA_ERR_RANGE;
+    return cuda_status(kda::launch_state_gather(c, idx, idx_type, selected, flags, packed,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int kda_state_scatter(const kda_cache *cache, const void *idx, int32_t idx_type, int64_t selected,
+                      const void *packed, int32_t packed_dtype, void *stream)
+{
+    kda::CacheDesc c{};
+    int rc = check_cache(cache, &c);
+    if (rc != KDA_OK) return rc;
+    if (!valid_itype(idx_type) || !valid_dtype(packed_dtype)) return KDA_ERR_DTYPE;
+    if (selected < 0) return KDA_ERR_SHAPE;
+    if (selected == 0) return KDA_OK;
+    if ((rc = check_index_array(idx, idx_type)) != KDA_OK) return rc;
+    if (packed == nullptr) return KDA_ERR_NULL;
+    if (!aligned(packed, static_cast<uintptr_t>(esize(packed_dtype)))) return KDA_ERR_ALIGN;
+    if (static_cast<__int128>(selected) * c.h * c.v * c.k * 4 > (static_cast<__int128>(1) << 62))
+        return KDA_ERR_RANGE;
+    return cuda_status(kda::launch_state_scatter(c, idx, idx_type, selected, packed, packed_dtype,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t dk, int32_t dv)
+{
+    if (!built_head_size(dk, dv)) return 0;
+    kda::PrefillLayout L{};
+    if (!kda::prefill_layout(total_tokens, num_seqs, h, dk, &L)) return 0;
+    return L.total;
+}
+
+namespace {
+int prefill_impl(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g, const float *beta,
+                 const int32_t *cu_seqlens, int64_t num_seqs, int64_t total_tokens, int32_t h, int32_t dk,
+                 int32_t dv, float scale, int32_t qk_l2norm, const void *init_state, int32_t init_dtype,
+                 float *final_state, void *out, void *workspace, size_t ws_bytes, void *stream,
+                 void *const *events)
+{
+    if (!valid_dtype(io_dtype)) return KDA_ERR_DTYPE;
+    if (init_state != nullptr && !valid_dtype(init_dtype)) return KDA_ERR_DTYPE;
+    if (num_seqs < 1 || total_tokens < 0 || h < 1 || dk < 1 || dv < 1) return KDA_ERR_SHAPE;
+    if (!built_head_size(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens >= (INT64_C(1) << 31) || num_seqs >= (INT64_C(1) << 30) || h > 65535)
+        return KDA_ERR_RANGE;
+    if (static_cast<__int128>(total_tokens) * h * dk >= (static_cast<__int128>(1) << 62)) return KDA_ERR_RANGE;
+    if (cu_seqlens == nullptr || workspace == nullptr) return KDA_ERR_NULL;
+    if (total_tokens > 0 && (q == nullptr || k == nullptr || v == nullptr || g == nullptr || beta == nullptr ||
+                             out == nullptr))
+        return KDA_ERR_NULL;
+    const void *vec16[] = {q, k, v, g, out, init_state, final_state};
+    for (const void *p : vec16)
+        if (p != nullptr && !aligned(p, 16)) return KDA_ERR_ALIGN;
+    if (!aligned(beta, 4) || !aligned(cu_seqlens, 4)) return KDA_ERR_ALIGN;
+    kda::PrefillLayout L{};
+    if (!kda::prefill_layout(total_tokens, num_seqs, h, dk, &L)) return KDA_ERR_SHAPE;
+    if (L.n_chunk_max >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
+    if (!aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+    if (ws_bytes < L.total) return KDA_ERR_WORKSPACE;
+    kda::PrefillArgs a{q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, scale,
+                       qk_l2norm ? 1 : 0, init_state, init_dtype, final_state, out, workspace, events};
+    return cuda_status(kda::launch_prefill(a, L, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+int kda_prefill_varlen(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,
+                       const float *beta, const int32_t *cu_seqlens, int64_t num_seqs, int64_t total_tokens,
+                       int32_t h, int32_t dk, int32_t dv, float scale, int32_t qk_l2norm, const void *init_state,
+                       int32_t init_dtype, float *final_state, void *out, void *workspace, size_t ws_bytes,
+                       void *stream)
+{
+    return prefill_impl(q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, dv, scale,
+                        qk_l2norm, init_state, init_dtype, final_state, out, workspace, ws_bytes, stream,
+                        nullptr);
+}
+
+int kda_prefill_varlen_timed(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,
+                             const float *beta, const int32_t *cu_seqlens, int64_t num_seqs,
+                             int64_t total_tokens, int32_t h, int32_t dk, int32_t dv, float scale,
+                             int32_t qk_l2norm, const void *init_state, int32_t init_dtype, float *final_state,
+                             void *out, void *workspace, size_t ws_bytes, void *stream, void *const *events)
+{
+    if (events == nullptr) return KDA_ERR_NULL;
+    for (int i = 0; i < 4; ++i)
+        if (events[i] == nullptr) return KDA_ERR_NULL;
+    return prefill_impl(q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, dv, scale,
+                        qk_l2norm, init_state, init_dtype, final_state, out, workspace, ws_bytes, stream, events);
+}
+
+int kda_decode_step(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,
+                    const float *beta, int64_t batch, int32_t h, int32_t dk, int32_t dv, float scale,
+                    int32_t qk_l2norm, const kda_cache *cache, const void *idx, int32_t idx_type, void *out,
+                    void *stream)
+{
+    kda::CacheDesc c{};
+    int rc = check_cache(cache, &c);
+    if (rc != KDA_OK) return rc;
+    if (!valid_dtype(io_dtype) || !valid_itype(idx_type)) return KDA_ERR_DTYPE;
+    if (batch < 0 || h < 1 || dk < 1 || dv < 1) return KDA_ERR_SHAPE;
+    if (!built_head_size(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    if (c.h != h || c.k != dk || c.v != dv) return KDA_ERR_SHAPE;
+    if (batch == 0) return KDA_OK;
+    if (batch * static_cast<int64_t>(h) >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
+    if ((rc = check_index_array(idx, idx_type)) != KDA_OK) return rc;
+    if (q == nullptr || k == nullptr || v == nullptr || g == nullptr || beta == nullptr || out == nullptr)
+        return KDA_ERR_NULL;
+    const void *vec16[] = {q, k, v, g, out, c.data};
+    for (const void *p : vec16)
+        if (!aligned(p, 16)) return KDA_ERR_ALIGN;
+    if (!aligned(beta, 4)) return KDA_ERR_ALIGN;
+    if ((c.row_stride * esize(c.dtype)) % 16 != 0) return KDA_ERR_ALIGN;
+    kda::DecodeArgs a{q, k, v, io_dtype, g, beta, batch, h, dk, scale, qk_l2norm ? 1 : 0, c, idx, idx_type, out};
+    return cuda_status(kda::launch_decode_step(a, static_cast<cudaStream_t>(stream)));
+}
+
+const char *kda_status_string(int32_t status)
+{
+    switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_NULL: return "KDA_ERR_NULL: a required pointer is NULL";
+    case KDA_ERR_DTYPE: return "KDA_ERR_DTYPE: unknown or unsupported element or index type";
+    case KDA_ERR_LAYOUT: return "KDA_ERR_LAYOUT: invalid cache layout (n_rows, sizes or row stride)";
+    case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE: invalid size or shape";
+    case KDA_ERR_RANGE: return "KDA_ERR_RANGE: size beyond the supported range";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA launch failed";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: head size combination not built";
+    case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN: pointer or stride misaligned";
+    default: return "unknown kda_status";
+    }
+}
+
+const char *kda_last_cuda_error_string(void) { return cudaGetErrorString(t_last_cuda); }
+
+int kda_prefill_workspace_status(const void *workspace, int32_t *status_out, void *stream)
+{
+    if (workspace == nullptr || status_out == nullptr) return KDA_ERR_NULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(status_out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return cuda_status(e);
+}
+
+}  // extern "C"

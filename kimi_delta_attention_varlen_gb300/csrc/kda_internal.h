@@ -1,0 +1,67 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+// Launchers assume their arguments were validated by the ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+struct CacheDesc {
+    void *data;
+    int32_t dtype;
+    int64_t n_rows, h, v, k, row_stride;
+};
+
+constexpr int kChunk = 64;  // tokens per chunk (the report's extend listing fixes 64)
+
+cudaError_t launch_state_gather(const CacheDesc &c, const void *idx, int32_t idx_type, int64_t selected,
+                                const uint8_t *flags, void *packed, cudaStream_t st);
+cudaError_t launch_state_scatter(const CacheDesc &c, const void *idx, int32_t idx_type, int64_t selected,
+                                 const void *packed, int32_t packed_dtype, cudaStream_t st);
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    int32_t io_dtype;
+    const float *g, *beta;
+    int64_t batch;
+    int32_t h, d;
+    float scale;
+    int32_t l2norm;
+    CacheDesc cache;
+    const void *idx;
+    int32_t idx_type;
+    void *out;
+};
+cudaError_t launch_decode_step(const DecodeArgs &a, cudaStream_t st);
+
+// Prefill workspace: a header (status word), the chunk table, and one record
+// per (chunk, head) holding the chunk's W, Q~, K~, A_qk, gamma and U^T.
+struct PrefillLayout {
+    int64_t n_chunk_max;
+    size_t off_chunk_off, off_seq_order, off_records, rec_bytes, total;
+};
+bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d, PrefillLayout *out);
+
+struct PrefillArgs {
+    const void *q, *k, *v;
+    int32_t io_dtype;
+    const float *g, *beta;
+    const int32_t *cu_seqlens;
+    int64_t num_seqs, total_tokens;
+    int32_t h, d;
+    float scale;
+    int32_t l2norm;
+    const void *init_state;
+    int32_t init_dtype;
+    float *final_state;
+    void *out;
+    void *workspace;
+    void *const *events;  // NULL, or 4 cudaEvent_t recorded at the kernel boundaries
+};
+cudaError_t launch_prefill(const PrefillArgs &a, const PrefillLayout &L, cudaStream_t st);
+
+}  // namespace kda

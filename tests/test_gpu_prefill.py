@@ -1,0 +1,176 @@
+"""GPU parity of kda_prefill_varlen (and the gather -> prefill -> scatter
+composition) against the token-by-token fp64 oracle.
+
+Tolerances (the method's target): outputs max|d| <= 2e-2 max|ref|, final
+states ||dS||_F <= 1e-2 ||S_ref||_F; state copies bit-exact.  Cases span
+several chunks with ragged tails, empty and single-token sequences, every
+built head size, both io dtypes, mild decay (long-range state propagation)
+and the degenerate gates; the full-size workloads are checked on sampled
+(sequence, head) pairs the oracle evaluates one by one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kimi_delta_attention_varlen_gb300 import (kda_prefill_varlen, kda_prefill_workspace_size,
+                                               kda_prefill_workspace_status, kda_state_gather,
+                                               kda_state_scatter)
+from kimi_delta_attention_varlen_gb300 import workloads as wl
+from tests.helpers import (assert_out_close, assert_state_close, bytes_of, f64, oracle_prefill_from_device,
+                           raw)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_prefill(inp, cu, H, D, init=None, scale=None, final=True, l2norm=True):
+    T = inp["q"].shape[0]
+    B = len(cu) - 1
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    out = torch.full((T, H, D), float("nan"), dtype=inp["q"].dtype, device=DEV)
+    fin = torch.full((B, H, D, D), float("nan"), dtype=torch.float32, device=DEV) if final else None
+    ws = torch.empty(kda_prefill_workspace_size(T, B, H, D, D), dtype=torch.uint8, device=DEV)
+    kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, out, ws,
+                       scale=scale, init_state=init, final_state=fin, qk_l2norm=l2norm)
+    torch.cuda.synchronize()
+    assert kda_prefill_workspace_status(ws) == 0
+    return out, fin
+
+
+def check_against_oracle(inp, cu, H, D, init, out, fin, scale, l2norm=True, heads=None, seqs=None):
+    o_ref, f_ref, toks = oracle_prefill_from_device(inp, cu, init, scale, l2norm, heads, seqs)
+    hs = slice(None) if heads is None else list(heads)
+    sq = list(range(len(cu) - 1)) if seqs is None else list(seqs)
+    got_o = f64(out[torch.tensor(toks, dtype=torch.long, device=DEV)][:, hs]) if toks else np.zeros((0,))
+    if toks:
+        assert_out_close(got_o, o_ref)
+    if fin is not None:
+        assert_state_close(f64(fin[sq][:, hs]), f_ref)
+
+
+@pytest.mark.parametrize("D,io", [(128, torch.bfloat16), (64, torch.bfloat16), (32, torch.float32),
+                                  (128, torch.float32)])
+@pytest.mark.parametrize("decay", [1.0, 0.01])
+def test_prefill_ragged_varlen(D, io, decay):
+    lengths = [1, 63, 64, 65, 0, 200, 333]
+    H = 3
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    inp = wl.token_inputs(cu[-1], H, D, D, io, seed=D + int(decay * 10), device=DEV, decay_scale=decay)
+    init = torch.randn(len(lengths), H, D, D, generator=wl.generator(3, DEV), device=DEV) * 0.5
+    scale = D ** -0.5
+    out, fin = run_prefill(inp, cu, H, D, init=init, scale=scale)
+    check_against_oracle(inp, cu, H, D, init, out, fin, scale)
+    assert torch.equal(fin[4], init[4])  # the empty sequence keeps its state bit for bit
+
+
+def test_prefill_bf16_init_and_no_final():
+    lengths, H, D = [130, 7], 2, 128
+    cu = [0, 130, 137]
+    inp = wl.token_inputs(137, H, D, D, torch.bfloat16, seed=5, device=DEV)
+    init = torch.randn(2, H, D, D, generator=wl.generator(6, DEV), device=DEV).to(torch.bfloat16)
+    out, _ = run_prefill(inp, cu, H, D, init=init, scale=0.1, final=False)
+    check_against_oracle(inp, cu, H, D, init.float(), out, None, 0.1)
+
+
+def test_prefill_zero_tokens_keeps_init():
+    H, D = 2, 64
+    inp = wl.token_inputs(0, H, D, D, torch.bfloat16, seed=1, device=DEV)
+    init = torch.randn(3, H, D, D, generator=wl.generator(2, DEV), device=DEV)
+    out, fin = run_prefill(inp, [0, 0, 0, 0], H, D, init=init)
+    assert torch.equal(fin, init)
+
+
+def test_prefill_without_l2norm_and_unit_scale():
+    lengths, H, D = [100, 29], 2, 64
+    cu = [0, 100, 129]
+    inp = wl.token_inputs(129, H, D, D, torch.bfloat16, seed=8, device=DEV)
+    out, fin = run_prefill(inp, cu, H, D, scale=1.0, l2norm=False)
+    check_against_oracle(inp, cu, H, D, None, out, fin, 1.0, l2norm=False)
+
+
+def test_degenerate_beta0_g0_keeps_state():
+    H, D, T = 2, 128, 150
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=9, device=DEV)
+    inp["g"].zero_()
+    inp["beta"].zero_()
+    init = torch.randn(1, H, D, D, generator=wl.generator(10, DEV), device=DEV)
+    out, fin = run_prefill(inp, [0, T], H, D, init=init, scale=D ** -0.5)
+    assert_state_close(f64(fin), f64(init))
+    check_against_oracle(inp, [0, T], H, D, init, out, fin, D ** -0.5)
+
+
+def test_degenerate_strong_decay():
+    """g = -8 per token (inside the documented gate range): the state keeps almost
+    nothing beyond the last token; outputs follow beta_t (k.q) v_t."""
+    H, D, T = 2, 128, 140
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=11, device=DEV)
+    inp["g"].fill_(-8.0)
+    init = torch.randn(1, H, D, D, generator=wl.generator(12, DEV), device=DEV)
+    out, fin = run_prefill(inp, [0, T], H, D, init=init, scale=D ** -0.5)
+    check_against_oracle(inp, [0, T], H, D, init, out, fin, D ** -0.5)
+
+
+def test_tiny_workload_gather_prefill_scatter():
+    """The tiny workload end to end: gather initial states by index and flag,
+    prefill, scatter final states - each step against its oracle."""
+    w = wl.tiny()
+    H, D = w.H, w.K
+    cu = [0]
+    for n in w.lengths:
+        cu.append(cu[-1] + n)
+    pc = wl.paged_cache(w.cache_rows, H, D, D, w.cache_dtype, w.cache_stride, seed=w.seed, device=DEV)
+    inp = wl.token_inputs(w.T, H, D, D, w.io_dtype, seed=w.seed, device=DEV)
+    packed = torch.empty(w.B, H, D, D, dtype=pc.view.dtype, device=DEV)
+    kda_state_gather(pc.view, w.gather_idx.to(DEV), packed, w.gather_flags.to(DEV))
+    out, fin = run_prefill(inp, cu, H, D, init=packed, scale=D ** -0.5)
+    host_before = raw(pc.backing)
+    kda_state_scatter(pc.view, w.scatter_idx.to(DEV), fin)
+    torch.cuda.synchronize()
+    # gather: bit-exact
+    N, P = w.cache_rows, H * D * D
+    body = host_before[pc.front:pc.front + N * pc.row_stride]
+    want_packed = oracle.gather(body, N, P, pc.row_stride, w.gather_idx.numpy(), w.gather_flags.numpy())
+    assert np.array_equal(raw(packed).reshape(w.B, -1), want_packed)
+    assert not torch.any(packed[1] != 0) and not torch.any(packed[2] != 0)  # idx -1, flag false
+    # prefill: tolerance
+    check_against_oracle(inp, cu, H, D, packed, out, fin, D ** -0.5)
+    # scatter: bit-exact given the GPU's final states
+    oracle.scatter(body, N, P, pc.row_stride, w.scatter_idx.numpy(), raw(fin).reshape(w.B, -1))
+    host_before[pc.front:pc.front + N * pc.row_stride] = body
+    assert np.array_equal(bytes_of(pc.backing), host_before.view(np.uint8))
+
+
+def _full_workload(w, sample_pairs):
+    H, D = w.H, w.K
+    cu = [0]
+    for n in w.lengths:
+        cu.append(cu[-1] + n)
+    pc = wl.paged_cache(w.cache_rows, H, D, D, w.cache_dtype, w.cache_stride, seed=w.seed, device=DEV)
+    inp = wl.token_inputs(w.T, H, D, D, w.io_dtype, seed=w.seed, device=DEV)
+    packed = torch.empty(w.B, H, D, D, dtype=pc.view.dtype, device=DEV)
+    kda_state_gather(pc.view, w.gather_idx.to(DEV), packed, w.gather_flags.to(DEV))
+    out, fin = run_prefill(inp, cu, H, D, init=packed, scale=D ** -0.5)
+    kda_state_scatter(pc.view, w.scatter_idx.to(DEV), fin)
+    torch.cuda.synchronize()
+    for b, h in sample_pairs:
+        check_against_oracle(inp, cu, H, D, packed, out, fin, D ** -0.5, heads=[h], seqs=[b])
+        r = int(w.scatter_idx[b])
+        if 0 <= r < w.cache_rows:  # the scattered row holds exactly the GPU's final state
+            assert torch.equal(pc.view[r, h], fin[b, h].to(pc.view.dtype))
+    return pc, inp, out, fin
+
+
+def test_full_varlen_workload_sampled():
+    w = wl.varlen()
+    order = sorted(range(w.B), key=lambda b: -w.lengths[b])
+    pairs = [(order[0], 0), (order[0], 31), (order[-1], 7), (order[w.B // 2], 19)]
+    _full_workload(w, pairs)
+    torch.cuda.empty_cache()
+
+
+def test_full_long_sequence_sampled():
+    w = wl.long_seq()
+    _full_workload(w, [(0, 5)])
+    torch.cuda.empty_cache()
