@@ -87,7 +87,8 @@ def test_bad_layout_is_rejected_before_launch():
     packed = torch.zeros(2, 2, 8, 8, device=DEV)
     with pytest.raises(KdaError):
         kda_state_gather(overlapping, idx, packed)
-    inner_strided = pc.backing.as_strided((4, 2, 8, 8), (256, 128, 8, 1), pc.front)
+    roomy = torch.zeros(4096, device=DEV)
+    inner_strided = roomy.as_strided((4, 2, 8, 8), (256, 128, 8, 1), 0)  # heads 128 apart, not 64
     with pytest.raises(ValueError):
         kda_state_gather(inner_strided, idx, packed)
 
