@@ -198,6 +198,39 @@ int kda_prefill_varlen_timed(const void *q, const void *k, const void *v, int32_
                              size_t ws_bytes, void *stream, void *const *events);
 
 /* ------------------------------------------------------------------------
+ * kda_prefill_varlen_noalloc
+ *
+ * The reference pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory - a host program that links
+ * only this library and has no device allocator, or a serving runtime that
+ * fixes its device memory at start-up and allows no allocation (cudaMalloc
+ * may synchronise the device and fail under fragmentation) on the request
+ * path.
+ *
+ * Same computation, arguments and results as kda_prefill_varlen, without the
+ * workspace: the kernels use a fixed array of KDA_NOALLOC_SCRATCH_BYTES bytes
+ * of device memory owned by the library (held by every GPU that loads the
+ * library until the process exits).  The call allocates nothing.
+ *   - A batch whose kda_prefill_workspace_size(...) exceeds
+ *     KDA_NOALLOC_SCRATCH_BYTES is rejected with KDA_ERR_WORKSPACE and
+ *     nothing is launched (128 MiB holds, at h = 32, dk = dv = 128, about
+ *     53 chunks of 64 tokens: e.g. one 3,300-token sequence).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *     KDA_ERR_CUDA if the lookup fails.
+ *   - Every call shares the one array: calls that overlap on the GPU (other
+ *     streams, or other threads without ordering) race and corrupt each
+ *     other's results.  Its contents left by the previous call do not matter.
+ * ---------------------------------------------------------------------- */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
+
+int kda_prefill_varlen_noalloc(const void *q, const void *k, const void *v, int32_t io_dtype,
+                               const float *g, const float *beta, const int32_t *cu_seqlens,
+                               int64_t num_seqs, int64_t total_tokens, int32_t h, int32_t dk,
+                               int32_t dv, float scale, int32_t qk_l2norm, const void *init_state,
+                               int32_t init_dtype, float *final_state, void *out, void *stream);
+
+/* ------------------------------------------------------------------------
  * kda_decode_step
  *
  * For each request r and head: with row = idx[r],

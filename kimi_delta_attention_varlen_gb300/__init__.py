@@ -192,3 +192,39 @@ def kda_prefill_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     _check(lib().kda_prefill_workspace_status(_ptr(workspace), ctypes.byref(out), _stream(stream)),
            "kda_prefill_workspace_status")
     return int(out.value)
+
+
+def kda_prefill_varlen_noalloc(q, k, v, g, beta, cu_seqlens, out, *, scale: float | None = None,
+                               qk_l2norm: bool = True, init_state=None, final_state=None, stream=None) -> None:
+    """kda_prefill_varlen without a workspace argument, for callers that cannot
+    allocate device memory (a host program with no device allocator, or a runtime
+    whose device memory is fixed at start-up and allows no allocation while
+    serving).  The kernels use a fixed scratch array of the library
+    (KDA_NOALLOC_SCRATCH_BYTES); batches that need more raise KdaError
+    (KDA_ERR_WORKSPACE).  The first call on a device looks up the scratch address
+    (make it before any stream capture); calls that overlap on the GPU race."""
+    T, H, K = q.shape
+    V = v.shape[2]
+    B = cu_seqlens.numel() - 1
+    for name, t, shape in (("q", q, (T, H, K)), ("k", k, (T, H, K)), ("v", v, (T, H, V)),
+                           ("out", out, (T, H, V)), ("g", g, (T, H, K)), ("beta", beta, (T, H))):
+        _need(tuple(t.shape) == shape and t.is_contiguous(), f"{name} must be contiguous {shape}")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype and out.dtype == q.dtype, "q, k, v, out share a dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g and beta must be float32")
+    _need(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous() and B >= 1,
+          "cu_seqlens must be a contiguous int32 tensor of B + 1 >= 2 offsets")
+    init_code = 0
+    if init_state is not None:
+        _need(tuple(init_state.shape) == (B, H, V, K) and init_state.is_contiguous(),
+              "init_state must be contiguous [B, H, V, K]")
+        init_code = _dtype_code(init_state)
+    if final_state is not None:
+        _need(tuple(final_state.shape) == (B, H, V, K) and final_state.is_contiguous() and
+              final_state.dtype == torch.float32, "final_state must be contiguous float32 [B, H, V, K]")
+    if scale is None:
+        scale = K ** -0.5
+    rc = lib().kda_prefill_varlen_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g), _ptr(beta),
+                                          _ptr(cu_seqlens), B, T, H, K, V, float(scale), 1 if qk_l2norm else 0,
+                                          _ptr(init_state), init_code, _ptr(final_state), _ptr(out),
+                                          _stream(stream))
+    _check(rc, "kda_prefill_varlen_noalloc")

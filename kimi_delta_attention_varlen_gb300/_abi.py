@@ -19,6 +19,7 @@ KDA_F32 = 0
 KDA_BF16 = 1
 KDA_I32 = 0
 KDA_I64 = 1
+KDA_NOALLOC_SCRATCH_BYTES = 128 << 20  # include/kda.h
 
 # Every symbol include/kda.h declares.
 EXPORTED = (
@@ -27,6 +28,7 @@ EXPORTED = (
     "kda_prefill_workspace_size",
     "kda_prefill_varlen",
     "kda_prefill_varlen_timed",
+    "kda_prefill_varlen_noalloc",
     "kda_decode_step",
     "kda_status_string",
     "kda_last_cuda_error_string",
@@ -85,6 +87,8 @@ def lib():
         L.kda_prefill_varlen.restype = ctypes.c_int
         L.kda_prefill_varlen_timed.argtypes = L.kda_prefill_varlen.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
         L.kda_prefill_varlen_timed.restype = ctypes.c_int
+        L.kda_prefill_varlen_noalloc.argtypes = L.kda_prefill_varlen.argtypes[:18] + [vp]
+        L.kda_prefill_varlen_noalloc.restype = ctypes.c_int
         L.kda_decode_step.argtypes = [vp, vp, vp, i32, vp, vp, i64, i32, i32, i32, f32, i32, cache_p, vp, i32,
                                       vp, vp]
         L.kda_decode_step.restype = ctypes.c_int

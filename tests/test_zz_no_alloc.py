@@ -1,0 +1,72 @@
+"""kda_prefill_varlen_noalloc: the prefill entry point for callers that cannot
+allocate device memory (a host program linking only this library, with no
+device allocator; a runtime whose device memory is fixed at start-up and that
+allows no allocation on the request path).  It must give the same results as
+kda_prefill_varlen with a caller workspace - checked here through the C ABI on
+two calls in a row, since every call reuses the library's one fixed scratch
+array.  The file is named to be collected last."""
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_varlen_gb300 as kda
+from kimi_delta_attention_varlen_gb300 import _abi
+from kimi_delta_attention_varlen_gb300 import workloads as wl
+from tests.helpers import assert_out_close, assert_state_close, f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _batch(lengths, seed, H=32, D=128):
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    inp = wl.token_inputs(cu[-1], H, D, D, torch.bfloat16, seed=seed, device=DEV)
+    init = torch.randn(len(lengths), H, D, D, generator=wl.generator(seed + 100, DEV), device=DEV)
+    return inp, torch.tensor(cu, dtype=torch.int32, device=DEV), init
+
+
+def _with_workspace(inp, cu, init):
+    T, H, D = inp["q"].shape
+    B = cu.numel() - 1
+    out = torch.empty(T, H, D, dtype=inp["q"].dtype, device=DEV)
+    fin = torch.empty(B, H, D, D, device=DEV)
+    ws = torch.empty(kda.kda_prefill_workspace_size(T, B, H, D, D), dtype=torch.uint8, device=DEV)
+    kda.kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu, out, ws,
+                           init_state=init, final_state=fin)
+    return out, fin
+
+
+def _noalloc(inp, cu, init):
+    T, H, D = inp["q"].shape
+    B = cu.numel() - 1
+    out = torch.full((T, H, D), float("nan"), dtype=inp["q"].dtype, device=DEV)
+    fin = torch.full((B, H, D, D), float("nan"), device=DEV)
+    kda.kda_prefill_varlen_noalloc(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu, out,
+                                   init_state=init, final_state=fin)
+    return out, fin
+
+
+def test_noalloc_matches_workspace_entry_point_on_two_calls():
+    # two different batches back to back: the second call reuses the scratch the first one left
+    for lengths, seed in (([700, 1, 130, 64], 1), ([65, 1000, 300], 2)):
+        inp, cu, init = _batch(lengths, seed)
+        want_out, want_fin = _with_workspace(inp, cu, init)
+        got_out, got_fin = _noalloc(inp, cu, init)
+        torch.cuda.synchronize()
+        assert_out_close(f64(got_out), f64(want_out))
+        assert_state_close(f64(got_fin), f64(want_fin))
+
+
+def test_noalloc_rejects_a_batch_beyond_its_scratch():
+    H, D = 32, 128
+    T = 64 * 64  # 64 chunks of 32 heads: more than the fixed scratch holds
+    assert kda.kda_prefill_workspace_size(T, 1, H, D, D) > _abi.KDA_NOALLOC_SCRATCH_BYTES
+    inp, cu, _ = _batch([T], 3)
+    out = torch.zeros(T, H, D, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_prefill_varlen_noalloc(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu, out)
+    assert e.value.status == -6  # KDA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert not torch.any(out != 0)  # nothing was launched
