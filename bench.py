@@ -148,9 +148,11 @@ def peaks() -> tuple:
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_record(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, only while the kernel
-    source it was taken from is unchanged (else None)."""
+def traffic_record(kernel: str, units: int):
+    """DRAM bytes per launch from a committed ncu capture (bytes per unit x the
+    units this launch processes; the capture ran a smaller case of the same
+    kernel, whose traffic grows in proportion to its chunk-heads), only while
+    the kernel source it was taken from is unchanged (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -162,15 +164,15 @@ def traffic_record(kernel: str):
     if not os.path.exists(src):
         return None
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec["bytes_per_launch"] if h == rec["source_sha256_16"] else None
+    return rec["bytes_per_unit"] * units if h == rec["source_sha256_16"] else None
 
 
 # ------------------------------------------------------------- workloads --
 
-def build_inputs(dev, seed=0):
+def build_inputs(dev, seed=0, small=False):
     import kimi_delta_attention_varlen_gb300 as kda
     from kimi_delta_attention_varlen_gb300 import workloads as wl
-    w = wl.varlen(seed)
+    w = wl.varlen(seed, B=4) if small else wl.varlen(seed)
     H, D = w.H, w.K
     cu = [0]
     for n in w.lengths:
@@ -330,7 +332,7 @@ def native(args, ranks: Ranks) -> dict | None:
     import kimi_delta_attention_varlen_gb300 as kda  # noqa: F401  (fails loudly if libkda.so is missing)
     dev = torch.device("cuda", ranks.local)
     torch.cuda.set_device(dev)
-    P = build_inputs(dev)
+    P = build_inputs(dev, small=args.workload == "small")
     T = P["cu_list"][-1]
     stream = torch.cuda.current_stream()
 
@@ -365,6 +367,9 @@ def native(args, ranks: Ranks) -> dict | None:
 
     br = {"gather": med("g0", "p0"), "chunk_table": med("p0", "p1"), "chunk_prep": med("p1", "p2"),
           "state_pass": med("p2", "p3"), "scatter": med("p3", "s1"), "decode": med("s1", "d1")}
+    if args.workload == "small":  # reduced batch for profiler captures: the step only
+        return {"metric": METRIC, "value": value, "unit": UNIT, "workload": P["w"].name, "tokens": T,
+                "breakdown_ms": br} if ranks.rank == 0 else None
 
     # end to end through the public API: pinned host inputs -> device, step, results -> host
     inp = P["inp"]
@@ -414,7 +419,7 @@ def native(args, ranks: Ranks) -> dict | None:
         dw = P["dw"]
         dom_bytes = 2 * int((dw.idx >= 0).sum()) * dw.H * dw.K * dw.V * 2
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = traffic_record(dom)
+    traffic = traffic_record(dom, nb["n_chunks"] * P["w"].H)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
@@ -493,6 +498,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=["full", "small"], default="full",
+                    help="small: 4-sequence varlen batch, step timing only (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
