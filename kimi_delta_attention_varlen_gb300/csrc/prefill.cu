@@ -33,31 +33,14 @@
 // R_j = e^{G_mJ - G_j}; each of P and R spans at most 8 tokens of decay, so
 // the products stay in fp32/bf16 range while that decay is above -80.  All
 // inter-chunk factors (e^G, e^{G_last - G}, e^{G_last}) are <= 1 for g <= 0.
-#include "kda_common.cuh"
-#include "kda_internal.h"
+#include "prefill_common.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int C = kChunk;
+using prefill::C;
+using prefill::Rec;
 constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier polls
-constexpr int kPrepThreads = 256;
-
-// ------------------------------------------------------------ record ------
-// One record per (chunk, head).  bf16 tiles are swizzled (see swz_off) so the
-// state pass can bulk-copy a record verbatim into shared memory.
-template <int D> struct Rec {
-    static constexpr int RB = 2 * D;                  // row bytes of [64][D] tiles
-    static constexpr int TILE = C * D * 2;            // bf16 [64][D]
-    static constexpr int W = 0;                       // W       [64][D]
-    static constexpr int QT = TILE;                   // Q~      [64][D]  (scale q e^G)
-    static constexpr int KT = 2 * TILE;               // K~      [64][D]  (k e^{G_last - G})
-    static constexpr int AQK = 3 * TILE;              // A_qk    [64][64] (scaled, causal)
-    static constexpr int GAMMA = AQK + C * C * 2;     // e^G_last [D] fp32
-    static constexpr int UT = GAMMA + D * 4;          // U^T     [D][64]
-    static constexpr int BYTES = UT + D * C * 2;
-    static_assert(UT % 128 == 0 && BYTES % 128 == 0, "record alignment");
-};
 
 // ---------------------------------------------------------- chunk table ---
 
@@ -118,380 +101,6 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int32_t *__restric
         }
     } else {
         for (int64_t b = tid; b < B; b += 1024) seq_order[b] = static_cast<int32_t>(b);
-    }
-}
-
-// ----------------------------------------------------------- chunk prep ---
-
-template <int D> struct PrepSmem {
-    static constexpr int TILE = C * D * 2;
-    static constexpr int AS = 68;                                    // fp32 row stride of A, T
-    static constexpr int GREG = (C * D * 4 > 2 * C * AS * 4) ? C * D * 4 : 2 * C * AS * 4;
-    static constexpr int G = 0;                                      // fp32 G [64][D]; later A, T fp32
-    static constexpr int KP = ((GREG + 127) / 128) * 128;            // k P      (later W)
-    static constexpr int QP = KP + TILE;                             // q P      (later U^T)
-    static constexpr int KR = QP + TILE;                             // k R
-    static constexpr int KE = KR + TILE;                             // beta k e^G
-    static constexpr int VB = KE + TILE;                             // beta v
-    static constexpr int AQK = VB + TILE;                            // A_qk bf16 [64][64]
-    static constexpr int TB = AQK + C * C * 2;                       // T bf16 [64][64]
-    static constexpr int TAB = TB + C * C * 2;                       // L[4][D] Z[4][D] F[16][D]
-    static constexpr int BETA = TAB + 24 * D * 4;                    // beta [64]
-    static constexpr int XS = BETA + C * 4;                          // solve scratch 8 x [16][16]
-    static constexpr int BYTES = XS + 8 * 16 * 16 * 4;
-};
-
-template <typename IO, int N> __device__ __forceinline__ void load_slice(const IO *p, float x[N]);
-template <> __device__ __forceinline__ void load_slice<float, 4>(const float *p, float x[4])
-{
-    const float4 a = *reinterpret_cast<const float4 *>(p);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-}
-template <> __device__ __forceinline__ void load_slice<float, 2>(const float *p, float x[2])
-{
-    const float2 a = *reinterpret_cast<const float2 *>(p);
-    x[0] = a.x; x[1] = a.y;
-}
-template <> __device__ __forceinline__ void load_slice<float, 1>(const float *p, float x[1]) { x[0] = *p; }
-template <>
-__device__ __forceinline__ void load_slice<__nv_bfloat16, 4>(const __nv_bfloat16 *p, float x[4])
-{
-    const uint2 a = *reinterpret_cast<const uint2 *>(p);
-    x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
-}
-template <>
-__device__ __forceinline__ void load_slice<__nv_bfloat16, 2>(const __nv_bfloat16 *p, float x[2])
-{
-    const uint32_t a = *reinterpret_cast<const uint32_t *>(p);
-    x[0] = bf16_lo(a); x[1] = bf16_hi(a);
-}
-template <>
-__device__ __forceinline__ void load_slice<__nv_bfloat16, 1>(const __nv_bfloat16 *p, float x[1])
-{
-    x[0] = __bfloat162float(*p);
-}
-
-// Store N (1, 2 or 4) consecutive values as bf16 at byte offset `off` of `base`.
-template <int N> __device__ __forceinline__ void store_bf16(char *base, uint32_t off, const float x[N])
-{
-    if constexpr (N == 4) {
-        *reinterpret_cast<uint2 *>(base + off) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
-    } else if constexpr (N == 2) {
-        *reinterpret_cast<uint32_t *>(base + off) = pack_bf16x2(x[0], x[1]);
-    } else {
-        *reinterpret_cast<uint16_t *>(base + off) = f32_to_bf16_bits(x[0]);
-    }
-}
-
-struct PrepParams {
-    const void *q, *k, *v;
-    const float *g, *beta;
-    const int32_t *cu;
-    const int32_t *chunk_off;
-    int64_t B;
-    int32_t H;
-    float scale;
-    int32_t l2norm;
-    char *records;
-};
-
-template <int D, typename IO>
-__global__ void __launch_bounds__(kPrepThreads)
-chunk_prep_kernel(PrepParams p)
-{
-    using SM = PrepSmem<D>;
-    using R = Rec<D>;
-    constexpr int RB = R::RB;
-    constexpr int CPL = D / 32;  // channels per lane in the row pass
-    extern __shared__ __align__(1024) char smem[];
-    __shared__ int32_t s_seq[3];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, ri = lane & 7;
-    const int64_t chunk = blockIdx.x;
-    const int h = blockIdx.y;
-    const int32_t n_chunks = p.chunk_off[p.B];
-    if (chunk >= n_chunks) return;
-
-    if (tid == 0) {  // sequence owning this chunk: chunk_off[b] <= chunk < chunk_off[b + 1]
-        int64_t lo = 0, hi = p.B;  // count of b in [1, B] with chunk_off[b] <= chunk
-        while (lo < hi) {
-            const int64_t mid = (lo + hi + 1) / 2;
-            if (p.chunk_off[mid] <= chunk) lo = mid;
-            else hi = mid - 1;
-        }
-        const int64_t b = lo;
-        const int32_t t0 = p.cu[b] + static_cast<int32_t>(chunk - p.chunk_off[b]) * C;
-        const int32_t left = p.cu[b + 1] - t0;
-        s_seq[0] = t0;
-        s_seq[1] = left < C ? left : C;
-    }
-    __syncthreads();
-    const int64_t t0 = s_seq[0];
-    const int len = s_seq[1];
-    const int64_t H = p.H;
-    char *rec = p.records + (chunk * H + h) * static_cast<int64_t>(R::BYTES);
-
-    float *sG = reinterpret_cast<float *>(smem + SM::G);
-    float *sBeta = reinterpret_cast<float *>(smem + SM::BETA);
-    float *sL = reinterpret_cast<float *>(smem + SM::TAB);
-    float *sZ = sL + 4 * D;
-    float *sF = sZ + 4 * D;  // sF[(I * 4 + J) * D + c]
-
-    // ---- 1. gate rows and beta; in-chunk cumulative sum of g per channel ----
-    for (int e = tid; e < C * (D / 4); e += kPrepThreads) {
-        const int i = e / (D / 4), c4 = e % (D / 4);
-        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < len) val = *reinterpret_cast<const float4 *>(p.g + ((t0 + i) * H + h) * D + c4 * 4);
-        *reinterpret_cast<float4 *>(sG + i * D + c4 * 4) = val;
-    }
-    if (tid < C) sBeta[tid] = tid < len ? p.beta[(t0 + tid) * H + h] : 0.f;
-    __syncthreads();
-    {
-        constexpr int SEG = kPrepThreads / D, RPS = C / SEG;
-        const int c = tid % D, sg = tid / D;
-        float acc = 0.f;
-        for (int i = sg * RPS; i < (sg + 1) * RPS; ++i) {
-            acc += sG[i * D + c];
-            sG[i * D + c] = acc;
-        }
-        __syncthreads();
-        float off = 0.f;
-        for (int s2 = 0; s2 < sg; ++s2) off += sG[((s2 + 1) * RPS - 1) * D + c];
-        __syncthreads();
-        if (sg > 0)
-            for (int i = sg * RPS; i < (sg + 1) * RPS; ++i) sG[i * D + c] += off;
-        __syncthreads();
-    }
-    // per-channel tables at the 16-row block midpoints m_I = 16 I + 8
-    for (int c = tid; c < D; c += kPrepThreads) {
-        const float gl = sG[(C - 1) * D + c];
-        float gm[4];
-#pragma unroll
-        for (int I = 0; I < 4; ++I) gm[I] = sG[(16 * I + 8) * D + c];
-#pragma unroll
-        for (int I = 0; I < 4; ++I) {
-            sL[I * D + c] = expf(gm[I]);       // e^{G_mI}          <= 1
-            sZ[I * D + c] = expf(gl - gm[I]);  // e^{G_last - G_mI} <= 1
-#pragma unroll
-            for (int J = 0; J < 4; ++J) sF[(I * 4 + J) * D + c] = J < I ? expf(gm[I] - gm[J]) : 1.f;
-        }
-        reinterpret_cast<float *>(rec + R::GAMMA)[c] = expf(gl);
-    }
-    __syncthreads();
-
-    // ---- 2. row pass: normalise q, k; build the bf16 operand tiles ----
-    {
-        const int cb = lane * CPL;
-        const IO *qg = static_cast<const IO *>(p.q);
-        const IO *kg = static_cast<const IO *>(p.k);
-        const IO *vg = static_cast<const IO *>(p.v);
-        for (int i = warp; i < C; i += kPrepThreads / 32) {
-            float qv[CPL], kv[CPL], vv[CPL];
-            if (i < len) {
-                const int64_t off = ((t0 + i) * H + h) * D + cb;
-                load_slice<IO, CPL>(qg + off, qv);
-                load_slice<IO, CPL>(kg + off, kv);
-                load_slice<IO, CPL>(vg + off, vv);
-            } else {
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) qv[c] = kv[c] = vv[c] = 0.f;
-            }
-            float sq = 0.f, sk = 0.f;
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                sq += qv[c] * qv[c];
-                sk += kv[c] * kv[c];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            }
-            const float rq = p.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
-            const float rk = p.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
-            const int I = i >> 4, m = 16 * I + 8;
-            const float bt = sBeta[i];
-            float kp[CPL], qp[CPL], kr[CPL], ke[CPL], qt[CPL], kt[CPL], vb[CPL];
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                const int ch = cb + c;
-                const float gi = sG[i * D + ch], gmid = sG[m * D + ch];
-                const float P = __expf(gi - gmid);
-                const float Rr = __expf(gmid - gi);
-                const float qh = qv[c] * rq, kh = kv[c] * rk;
-                kp[c] = kh * P;
-                qp[c] = qh * P;
-                kr[c] = kh * Rr;
-                ke[c] = bt * kh * P * sL[I * D + ch];
-                qt[c] = p.scale * qh * P * sL[I * D + ch];
-                kt[c] = kh * Rr * sZ[I * D + ch];
-                vb[c] = bt * vv[c];
-            }
-            const uint32_t o = swz_off<RB>(i, cb);
-            store_bf16<CPL>(smem + SM::KP, o, kp);
-            store_bf16<CPL>(smem + SM::QP, o, qp);
-            store_bf16<CPL>(smem + SM::KR, o, kr);
-            store_bf16<CPL>(smem + SM::KE, o, ke);
-            store_bf16<CPL>(smem + SM::VB, o, vb);
-            store_bf16<CPL>(rec + R::QT, o, qt);
-            store_bf16<CPL>(rec + R::KT, o, kt);
-        }
-    }
-    __syncthreads();
-
-    // ---- 3. gated Gram products: warps 0-3 A_kk, warps 4-7 A_qk ----
-    float *sA = reinterpret_cast<float *>(smem + SM::G);  // fp32 [64][AS]
-    float *sT = sA + C * SM::AS;                           // fp32 [64][AS]
-    {
-        const int I = warp & 3;
-        const bool is_qk = warp >= 4;
-        const char *src = smem + (is_qk ? SM::QP : SM::KP);
-        for (int J = 0; J < 4; ++J) {
-            float acc[2][4] = {};
-            if (J <= I) {
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    uint32_t a[4], b[4];
-                    ldmatrix_x4(a, smem_u32(src + swz_off<RB>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
-                    if (J < I) {  // a <- a * F_IJ over the fragment's four channels
-                        const float *f = sF + (I * 4 + J) * D + 16 * ks + 2 * tig;
-                        const float f0 = f[0], f1 = f[1], f2 = f[8], f3 = f[9];
-                        a[0] = pack_bf16x2(bf16_lo(a[0]) * f0, bf16_hi(a[0]) * f1);
-                        a[1] = pack_bf16x2(bf16_lo(a[1]) * f0, bf16_hi(a[1]) * f1);
-                        a[2] = pack_bf16x2(bf16_lo(a[2]) * f2, bf16_hi(a[2]) * f3);
-                        a[3] = pack_bf16x2(bf16_lo(a[3]) * f2, bf16_hi(a[3]) * f3);
-                    }
-                    ldmatrix_x4(b, smem_u32(smem + SM::KR +
-                                            swz_off<RB>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
-                    mma_bf16(acc[0], a, b[0], b[1]);
-                    mma_bf16(acc[1], a, b[2], b[3]);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int i = 16 * I + gid + 8 * hr;
-                    const int j = 16 * J + 8 * nt + 2 * tig;
-                    const float x0 = acc[nt][2 * hr], x1 = acc[nt][2 * hr + 1];
-                    if (!is_qk) {
-                        const float bi = sBeta[i];
-                        sA[i * SM::AS + j] = j < i ? x0 * bi : 0.f;
-                        sA[i * SM::AS + j + 1] = j + 1 < i ? x1 * bi : 0.f;
-                    } else {
-                        const float y0 = j <= i ? x0 * p.scale : 0.f;
-                        const float y1 = j + 1 <= i ? x1 * p.scale : 0.f;
-                        *reinterpret_cast<uint32_t *>(smem + SM::AQK + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
-                    }
-                }
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- 4. T = (I + A_kk)^-1, blocked by 16 (fp32) ----
-    if (warp < 4 && lane < 16) {  // diagonal blocks: forward substitution, lane = column
-        const int I = warp, j = lane;
-        const float *A = sA + 16 * I * SM::AS + 16 * I;
-        float tcol[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = i == j ? 1.f : 0.f;
-#pragma unroll
-            for (int kk = 0; kk < i; ++kk) acc -= A[i * SM::AS + kk] * tcol[kk];
-            tcol[i] = acc;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sT[(16 * I + i) * SM::AS + 16 * I + j] = tcol[i];
-    }
-    __syncthreads();
-    for (int d = 1; d < 4; ++d) {  // off-diagonal blocks by sub-diagonal
-        if (warp < 4 - d) {
-            const int J = warp, I = warp + d;
-            const int r = lane >> 1, c0 = (lane & 1) * 8;
-            float *xs = reinterpret_cast<float *>(smem + SM::XS) + warp * 256;
-            float x[8] = {};
-            for (int Kb = J; Kb < I; ++Kb) {
-#pragma unroll 4
-                for (int m = 0; m < 16; ++m) {
-                    const float a = sA[(16 * I + r) * SM::AS + 16 * Kb + m];
-                    const float *t = sT + (16 * Kb + m) * SM::AS + 16 * J + c0;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) x[c] += a * t[c];
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c) xs[r * 16 + c0 + c] = x[c];
-            __syncwarp();
-            float y[8] = {};
-#pragma unroll 4
-            for (int m = 0; m < 16; ++m) {
-                const float t = sT[(16 * I + r) * SM::AS + 16 * I + m];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) y[c] += t * xs[m * 16 + c0 + c];
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c) sT[(16 * I + r) * SM::AS + 16 * J + c0 + c] = -y[c];
-        }
-        __syncthreads();
-    }
-    for (int e = tid; e < C * (C / 2); e += kPrepThreads) {  // T -> bf16, zero above block diagonal
-        const int i = e / (C / 2), j = 2 * (e % (C / 2));
-        const bool keep = (j >> 4) <= (i >> 4);
-        const float t0v = keep ? sT[i * SM::AS + j] : 0.f;
-        const float t1v = keep ? sT[i * SM::AS + j + 1] : 0.f;
-        *reinterpret_cast<uint32_t *>(smem + SM::TB + swz_off<128>(i, j)) = pack_bf16x2(t0v, t1v);
-    }
-    __syncthreads();
-
-    // ---- 5. W = T (beta K e^G) (warps 0-3), U = T (beta V) (warps 4-7) ----
-    {
-        const int I = warp & 3;
-        const bool is_u = warp >= 4;
-        const char *bsrc = smem + (is_u ? SM::VB : SM::KE);
-        float acc[D / 8][4] = {};
-        for (int ks = 0; ks <= I; ++ks) {  // T is lower triangular
-            uint32_t a[4];
-            ldmatrix_x4(a, smem_u32(smem + SM::TB + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
-#pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
-                uint32_t b[4];
-                ldmatrix_x4_trans(b, smem_u32(bsrc + swz_off<RB>(16 * ks + ri + 8 * (mi & 1), 16 * np + 8 * (mi >> 1))));
-                mma_bf16(acc[2 * np], a, b[0], b[1]);
-                mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
-            }
-        }
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int i = 16 * I + gid + 8 * hr;
-                const int c = 8 * n + 2 * tig;
-                if (!is_u) {
-                    *reinterpret_cast<uint32_t *>(smem + SM::KP + swz_off<RB>(i, c)) =
-                        pack_bf16x2(acc[n][2 * hr], acc[n][2 * hr + 1]);
-                } else {  // U^T [D][64]
-                    *reinterpret_cast<uint16_t *>(smem + SM::QP + swz_off<128>(c, i)) = f32_to_bf16_bits(acc[n][2 * hr]);
-                    *reinterpret_cast<uint16_t *>(smem + SM::QP + swz_off<128>(c + 1, i)) =
-                        f32_to_bf16_bits(acc[n][2 * hr + 1]);
-                }
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- 6. copy W, A_qk, U^T out to the record ----
-    {
-        const uint4 *sw = reinterpret_cast<const uint4 *>(smem + SM::KP);
-        const uint4 *sq = reinterpret_cast<const uint4 *>(smem + SM::AQK);
-        const uint4 *su = reinterpret_cast<const uint4 *>(smem + SM::QP);
-        uint4 *gw = reinterpret_cast<uint4 *>(rec + R::W);
-        uint4 *gq = reinterpret_cast<uint4 *>(rec + R::AQK);
-        uint4 *gu = reinterpret_cast<uint4 *>(rec + R::UT);
-        for (int e = tid; e < R::TILE / 16; e += kPrepThreads) gw[e] = sw[e];
-        for (int e = tid; e < C * C * 2 / 16; e += kPrepThreads) gq[e] = sq[e];
-        for (int e = tid; e < D * C * 2 / 16; e += kPrepThreads) gu[e] = su[e];
     }
 }
 
@@ -716,18 +325,6 @@ state_pass_kernel(PassParams p)
     }
 }
 
-template <int D> int rec_bytes() { return Rec<D>::BYTES; }
-
-int rec_bytes_for(int d)
-{
-    switch (d) {
-    case 32: return rec_bytes<32>();
-    case 64: return rec_bytes<64>();
-    case 128: return rec_bytes<128>();
-    default: return 0;
-    }
-}
-
 template <int D, typename IO, int WARPS>
 cudaError_t launch_pass(const PassParams &pp, int64_t items, cudaStream_t st)
 {
@@ -761,13 +358,9 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     if ((e = mark(1)) != cudaSuccess) return e;
 
     if (L.n_chunk_max > 0) {
-        PrepParams pp{a.q, a.k, a.v, a.g, a.beta, a.cu_seqlens, chunk_off, a.num_seqs, a.h, a.scale, a.l2norm, records};
-        auto kern = chunk_prep_kernel<D, IO>;
-        constexpr int smem = PrepSmem<D>::BYTES;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        kern<<<dim3(static_cast<unsigned>(L.n_chunk_max), static_cast<unsigned>(a.h)), kPrepThreads, smem, st>>>(pp);
-        e = cudaGetLastError();
+        const prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, a.cu_seqlens, chunk_off, a.num_seqs,
+                                     a.h, a.scale, a.l2norm, records};
+        e = prefill::launch_chunk_prep(D, a.io_dtype, pp, L.n_chunk_max, a.h, st);
         if (e != cudaSuccess) return e;
     }
 
@@ -800,7 +393,7 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
 
 bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d, PrefillLayout *out)
 {
-    const int rb = rec_bytes_for(d);
+    const int rb = prefill::rec_bytes_for(d);
     if (rb == 0 || total_tokens < 0 || num_seqs < 1 || h < 1) return false;
     auto up = [](size_t x, size_t a) { return (x + a - 1) / a * a; };
     PrefillLayout L{};
