@@ -14,7 +14,8 @@
 // per warp, g columns per cumsum thread), so one memory latency covers the
 // whole chunk and the co-resident CTA's compute hides it.  The gated Gram
 // products and W, U run on the tensor cores (bf16 operands, fp32 accumulate);
-// the triangular solve is blocked by 16 and stays in fp32.
+// W and U come from block forward substitution on (I + A_kk): only the four
+// 16x16 diagonal inverses are formed (fp32), every product is an MMA.
 //
 // Exponents: e^{G_i - G_j} = P_i F_IJ R_j with P_i = e^{G_i - G_mI},
 // R_j = e^{G_mJ - G_j} (m = midpoint of the 16-row block) and F_IJ =
@@ -35,19 +36,25 @@ constexpr int kWarps = kThreads / 32;
 
 template <int D> struct PrepSmem {
     static constexpr int TILE = C * D * 2;                 // bf16 [64][D]
-    static constexpr int AS = 68;                          // fp32 row stride of A and T
-    static constexpr int GREG0 = C * D * 4 > 2 * C * AS * 4 ? C * D * 4 : 2 * C * AS * 4;
+    static constexpr int XT = 16 * D * 2;                  // bf16 [16][D]
+    // G region: G fp32 [64][D] during the row pass; afterwards A_kk bf16, T_diag bf16,
+    // the diagonal blocks of A_kk in fp32 and the two substitution tiles X_W, X_U.
+    static constexpr int AB = 0;                           // A_kk bf16 [64][64]
+    static constexpr int TD = AB + C * C * 2;              // diag(T_00..T_33) bf16 [64][64]
+    static constexpr int AD = TD + C * C * 2;              // A_II fp32 [4][16][17]
+    static constexpr int XW = (AD + 4 * 16 * 17 * 4 + 127) / 128 * 128;
+    static constexpr int XU = XW + XT;
+    static constexpr int GREG0 = C * D * 4 > XU + XT ? C * D * 4 : XU + XT;
     static constexpr int GREG = (GREG0 + 127) / 128 * 128;
-    static constexpr int G = 0;          // G fp32 [64][D] -> A, T fp32 [64][AS] -> T' bf16 [64][64]
-    static constexpr int KP = GREG;      // k P: Gram A operand, W's B operand
-    static constexpr int QP = KP + TILE; // q P: Gram A operand -> U^T staging [D][64]
-    static constexpr int KR = QP + TILE; // k R: Gram B operand -> solve scratch -> W staging
-    static constexpr int VS = KR + TILE; // v (bf16): U's B operand
-    static constexpr int TAB = VS + TILE;                  // L[4][D], Z[4][D], F[6][D] fp32
-    static constexpr int BETA = TAB + 14 * D * 4;          // beta [64]
+    static constexpr int G = 0;
+    static constexpr int KP = GREG;      // k P: Gram A operand, W base
+    static constexpr int QP = KP + TILE; // q P: Gram A operand -> U tile
+    static constexpr int KR = QP + TILE; // k R: Gram B operand -> W tile
+    static constexpr int VS = KR + TILE; // v (bf16): U base
+    static constexpr int TAB = VS + TILE;                  // L[4][D], Z[4][D], F[6][D], L*scale[4][D]
+    static constexpr int BETA = TAB + 18 * D * 4;          // beta [64]
     static constexpr int TOT = BETA + C * 4;               // cumsum segment totals
     static constexpr int BYTES = TOT + kThreads * 4;
-    static_assert(C * C * 2 <= GREG, "T' fits the G region");
 };
 
 // CPL io elements of one row, kept packed in registers until used.
@@ -90,6 +97,30 @@ template <typename IO, int N> struct Slice {
         }
     }
 };
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// N consecutive fp32 values from shared memory (N = 1, 2, 4; aligned to N floats).
+template <int N> __device__ __forceinline__ void load_f32(const float *p, float x[N])
+{
+    if constexpr (N == 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(p);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    } else if constexpr (N == 2) {
+        const float2 a = *reinterpret_cast<const float2 *>(p);
+        x[0] = a.x; x[1] = a.y;
+    } else {
+        x[0] = *p;
+    }
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a);
+    const __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162 *>(&b);
+    x = __hmul2(x, y);
+    return *reinterpret_cast<uint32_t *>(&x);
+}
 
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float f0, float f1)
 {
@@ -140,7 +171,8 @@ chunk_prep_kernel(PrepParams p)
     float *sG = reinterpret_cast<float *>(smem + SM::G);
     float *sL = reinterpret_cast<float *>(smem + SM::TAB);
     float *sZ = sL + 4 * D;
-    float *sF = sZ + 4 * D;
+    float *sLs = sZ + 4 * D;
+    uint16_t *sFb = reinterpret_cast<uint16_t *>(sLs + 4 * D);  // F_IJ as bf16 [6][D]
     float *sBeta = reinterpret_cast<float *>(smem + SM::BETA);
     float *sTot = reinterpret_cast<float *>(smem + SM::TOT);
 
@@ -149,7 +181,8 @@ chunk_prep_kernel(PrepParams p)
     const IO *kg = static_cast<const IO *>(p.k);
     const IO *vg = static_cast<const IO *>(p.v);
     const int cb = lane * CPL;
-    Slice<IO, CPL> rq[PRE], rk[PRE], rv[PRE];
+    constexpr bool kStage = sizeof(IO) == 2;  // bf16 rows are staged into their swizzled tiles
+    Slice<IO, CPL> rq[kStage ? 1 : PRE], rk[kStage ? 1 : PRE], rv[kStage ? 1 : PRE];
     auto load_rows = [&](int j0) {
 #pragma unroll
         for (int j = 0; j < PRE; ++j) {
@@ -166,18 +199,38 @@ chunk_prep_kernel(PrepParams p)
             }
         }
     };
-    load_rows(0);
-    const int gc = tid % D, gs = tid / D;
-    float gr[RPS];
+    // g rows -> shared memory asynchronously (rows past the sequence end read as zeros)
 #pragma unroll
-    for (int r = 0; r < RPS; ++r) {
-        const int i = gs * RPS + r;
-        gr[r] = i < len ? p.g[((t0 + i) * H + h) * D + gc] : 0.f;
+    for (int e = tid; e < C * (D / 4); e += kThreads) {
+        const int i = e / (D / 4), c4 = e % (D / 4);
+        const int ii = i < len ? i : 0;
+        cp_async16(smem_u32(sG + i * D + 4 * c4), p.g + ((t0 + ii) * H + h) * D + 4 * c4, i < len ? 16u : 0u);
+    }
+    if constexpr (kStage) {  // q -> QP, k -> KP, v -> VS tiles, 16-byte chunks, zeros past the end
+        constexpr int CH = RB / 16;  // chunks per row
+#pragma unroll
+        for (int e = tid; e < C * CH; e += kThreads) {
+            const int i = e / CH, ch = e % CH;
+            const int ii = i < len ? i : 0;
+            const int64_t off = ((t0 + ii) * H + h) * D + 8 * ch;
+            const uint32_t so = swz_off<RB>(i, 8 * ch);
+            const uint32_t nb = i < len ? 16u : 0u;
+            cp_async16(smem_u32(smem + SM::QP + so), qg + off, nb);
+            cp_async16(smem_u32(smem + SM::KP + so), kg + off, nb);
+            cp_async16(smem_u32(smem + SM::VS + so), vg + off, nb);
+        }
+    } else {
+        load_rows(0);
     }
     if (tid < C) sBeta[tid] = tid < len ? p.beta[(t0 + tid) * H + h] : 0.f;
-    // in-chunk cumulative sum of g, per channel: registers, then segment offsets
+    cp_async_wait_all();
+    __syncthreads();
+    // in-chunk cumulative sum of g per channel, in log2 units: registers, then segment offsets
+    const int gc = tid % D, gs = tid / D;
+    float gr[RPS];
+    gr[0] = sG[(gs * RPS) * D + gc] * kLog2e;
 #pragma unroll
-    for (int r = 1; r < RPS; ++r) gr[r] += gr[r - 1];
+    for (int r = 1; r < RPS; ++r) gr[r] = fmaf(sG[(gs * RPS + r) * D + gc], kLog2e, gr[r - 1]);
     sTot[gs * D + gc] = gr[RPS - 1];
     __syncthreads();
     {
@@ -187,7 +240,7 @@ chunk_prep_kernel(PrepParams p)
         for (int r = 0; r < RPS; ++r) sG[(gs * RPS + r) * D + gc] = gr[r] + off;
     }
     __syncthreads();
-    // per-channel factors at the block midpoints m_I = 16 I + 8
+    // per-channel factors at the block midpoints m_I = 16 I + 8 (G is in log2 units)
     if (tid < D) {
         const int c = tid;
         const float gl = sG[(C - 1) * D + c];
@@ -196,26 +249,34 @@ chunk_prep_kernel(PrepParams p)
         for (int I = 0; I < 4; ++I) gm[I] = sG[(16 * I + 8) * D + c];
 #pragma unroll
         for (int I = 0; I < 4; ++I) {
-            sL[I * D + c] = expf(gm[I]);       // e^{G_mI}          <= 1
-            sZ[I * D + c] = expf(gl - gm[I]);  // e^{G_last - G_mI} <= 1
+            const float l = exp2f(gm[I]);
+            sL[I * D + c] = l;                  // e^{G_mI}          <= 1
+            sLs[I * D + c] = l * p.scale;       // scale e^{G_mI}
+            sZ[I * D + c] = exp2f(gl - gm[I]);  // e^{G_last - G_mI} <= 1
 #pragma unroll
-            for (int J = 0; J < I; ++J) sF[fslot(I, J) * D + c] = expf(gm[I] - gm[J]);
+            for (int J = 0; J < I; ++J) sFb[fslot(I, J) * D + c] = f32_to_bf16_bits(exp2f(gm[I] - gm[J]));
         }
-        reinterpret_cast<float *>(rec + R::GAMMA)[c] = expf(gl);
+        reinterpret_cast<float *>(rec + R::GAMMA)[c] = exp2f(gl);
     }
     __syncthreads();
 
     // ---- 2. row pass: normalise q, k; operand tiles in shared memory; Q~, K~ to the record ----
 #pragma unroll 1
     for (int j0 = 0; j0 < ROWS; j0 += PRE) {
-        if (j0 > 0) load_rows(j0);
+        if (!kStage && j0 > 0) load_rows(j0);
 #pragma unroll
         for (int j = 0; j < PRE; ++j) {
             const int i = warp + kWarps * (j0 + j);
+            const uint32_t o = swz_off<RB>(i, cb);
             float qv[CPL], kv[CPL], vv[CPL];
-            rq[j].get(qv);
-            rk[j].get(kv);
-            rv[j].get(vv);
+            if constexpr (kStage) {
+                load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::QP + o), qv);
+                load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::KP + o), kv);
+            } else {
+                rq[j].get(qv);
+                rk[j].get(kv);
+                rv[j].get(vv);
+            }
             float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
@@ -230,25 +291,28 @@ chunk_prep_kernel(PrepParams p)
             const float nq = p.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
             const float nk = p.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
             const int I = i >> 4, m = 16 * I + 8;
+            float gi[CPL], gmid[CPL], ls[CPL], zz[CPL];
+            load_f32<CPL>(sG + i * D + cb, gi);
+            load_f32<CPL>(sG + m * D + cb, gmid);
+            load_f32<CPL>(sLs + I * D + cb, ls);
+            load_f32<CPL>(sZ + I * D + cb, zz);
             float kp[CPL], qp[CPL], kr[CPL], qt[CPL], kt[CPL];
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
-                const int ch = cb + c;
-                const float gi = sG[i * D + ch], gmid = sG[m * D + ch];
-                const float P = __expf(gi - gmid);
-                const float Rr = __expf(gmid - gi);
+                const float P = ex2_approx(gi[c] - gmid[c]);   // e^{G_i - G_m}
+                const float Rr = ex2_approx(gmid[c] - gi[c]);  // e^{G_m - G_i}
                 const float qh = qv[c] * nq, kh = kv[c] * nk;
                 kp[c] = kh * P;
                 qp[c] = qh * P;
                 kr[c] = kh * Rr;
-                qt[c] = p.scale * qh * P * sL[I * D + ch];
-                kt[c] = kh * Rr * sZ[I * D + ch];
+                qt[c] = qp[c] * ls[c];
+                kt[c] = kr[c] * zz[c];
             }
-            const uint32_t o = swz_off<RB>(i, cb);
+            __syncwarp();  // every lane has read its q, k slice before the tiles are overwritten
             store_bf16<CPL>(smem + SM::KP, o, kp);
             store_bf16<CPL>(smem + SM::QP, o, qp);
             store_bf16<CPL>(smem + SM::KR, o, kr);
-            store_bf16<CPL>(smem + SM::VS, o, vv);
+            if constexpr (!kStage) store_bf16<CPL>(smem + SM::VS, o, vv);
             store_bf16<CPL>(rec + R::QT, o, qt);
             store_bf16<CPL>(rec + R::KT, o, kt);
         }
@@ -256,157 +320,182 @@ chunk_prep_kernel(PrepParams p)
     __syncthreads();
 
     // ---- 3. gated Gram products, 20 (matrix, I, J) block pairs over 8 warps ----
-    float *sA = reinterpret_cast<float *>(smem + SM::G);  // A_kk fp32 [64][AS]
-    float *sT = sA + C * SM::AS;                           // T fp32 [64][AS]
-    for (int pr = warp; pr < 20; pr += kWarps) {
-        const bool is_qk = pr >= 10;
-        const int li = pr % 10;                            // lower-triangle block index
-        const int I = li >= 6 ? 3 : li >= 3 ? 2 : li >= 1 ? 1 : 0;
-        const int J = li - I * (I + 1) / 2;
-        const char *src = smem + (is_qk ? SM::QP : SM::KP);
-        float acc[2][4] = {};
+    // A_kk (x beta_i, strictly lower) -> bf16 tile for the substitution products, and its
+    // diagonal blocks in fp32 for their inverses; A_qk (x scale, causal) -> the record.
+    float *sAd = reinterpret_cast<float *>(smem + SM::AD);  // [4][16][17] fp32
+    {
+        constexpr int MAXP = (20 + kWarps - 1) / kWarps;  // pairs per warp (3)
+        const int npairs = (20 - warp + kWarps - 1) / kWarps;
+        int pI[MAXP], pJ[MAXP];
+        bool pqk[MAXP];
+#pragma unroll
+        for (int u = 0; u < MAXP; ++u) {
+            const int pr = warp + kWarps * u;
+            const int li = pr % 10;                        // lower-triangle block index
+            pqk[u] = pr >= 10;
+            pI[u] = li >= 6 ? 3 : li >= 3 ? 2 : li >= 1 ? 1 : 0;
+            pJ[u] = li - pI[u] * (pI[u] + 1) / 2;
+        }
+        float acc[MAXP][2][4] = {};
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            uint32_t a[4], b[4];
-            ldmatrix_x4(a, smem_u32(src + swz_off<RB>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
-            if (J < I) {  // a <- a * F_IJ on the fragment's four channels
-                const float *f = sF + fslot(I, J) * D + 16 * ks + 2 * tig;
-                const float f0 = f[0], f1 = f[1], f2 = f[8], f3 = f[9];
-                a[0] = scale_bf16x2(a[0], f0, f1);
-                a[1] = scale_bf16x2(a[1], f0, f1);
-                a[2] = scale_bf16x2(a[2], f2, f3);
-                a[3] = scale_bf16x2(a[3], f2, f3);
+#pragma unroll
+            for (int u = 0; u < MAXP; ++u) {  // independent accumulation chains
+                if (u < npairs) {
+                    const int I = pI[u], J = pJ[u];
+                    uint32_t a[4], b[4];
+                    ldmatrix_x4(a, smem_u32(smem + (pqk[u] ? SM::QP : SM::KP) +
+                                            swz_off<RB>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
+                    if (J < I) {  // a <- a * F_IJ on the fragment's four channels (bf16x2 products)
+                        const uint16_t *f = sFb + fslot(I, J) * D + 16 * ks + 2 * tig;
+                        const uint32_t f01 = *reinterpret_cast<const uint32_t *>(f);
+                        const uint32_t f23 = *reinterpret_cast<const uint32_t *>(f + 8);
+                        a[0] = mul_bf16x2(a[0], f01);
+                        a[1] = mul_bf16x2(a[1], f01);
+                        a[2] = mul_bf16x2(a[2], f23);
+                        a[3] = mul_bf16x2(a[3], f23);
+                    }
+                    ldmatrix_x4(b, smem_u32(smem + SM::KR + swz_off<RB>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
+                    mma_bf16(acc[u][0], a, b[0], b[1]);
+                    mma_bf16(acc[u][1], a, b[2], b[3]);
+                }
             }
-            ldmatrix_x4(b, smem_u32(smem + SM::KR + swz_off<RB>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
-            mma_bf16(acc[0], a, b[0], b[1]);
-            mma_bf16(acc[1], a, b[2], b[3]);
         }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int u = 0; u < MAXP; ++u) {
+            if (u >= npairs) continue;
+            const int I = pI[u], J = pJ[u];
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int i = 16 * I + gid + 8 * hr;
-                const int j = 16 * J + 8 * nt + 2 * tig;
-                const float x0 = acc[nt][2 * hr], x1 = acc[nt][2 * hr + 1];
-                if (!is_qk) {
-                    const float bi = sBeta[i];
-                    sA[i * SM::AS + j] = j < i ? x0 * bi : 0.f;
-                    sA[i * SM::AS + j + 1] = j + 1 < i ? x1 * bi : 0.f;
-                } else {
-                    const float y0 = j <= i ? x0 * p.scale : 0.f;
-                    const float y1 = j + 1 <= i ? x1 * p.scale : 0.f;
-                    *reinterpret_cast<uint32_t *>(rec + R::AQK + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int i = 16 * I + gid + 8 * hr;
+                    const int j = 16 * J + 8 * nt + 2 * tig;
+                    const float x0 = acc[u][nt][2 * hr], x1 = acc[u][nt][2 * hr + 1];
+                    if (!pqk[u]) {
+                        const float bi = sBeta[i];
+                        const float y0 = j < i ? x0 * bi : 0.f, y1 = j + 1 < i ? x1 * bi : 0.f;
+                        *reinterpret_cast<uint32_t *>(smem + SM::AB + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
+                        if (I == J) {
+                            float *d = sAd + I * 16 * 17 + (i - 16 * I) * 17 + (j - 16 * J);
+                            d[0] = y0;
+                            d[1] = y1;
+                        }
+                    } else {
+                        const float y0 = j <= i ? x0 * p.scale : 0.f;
+                        const float y1 = j + 1 <= i ? x1 * p.scale : 0.f;
+                        *reinterpret_cast<uint32_t *>(rec + R::AQK + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
+                    }
                 }
             }
         }
     }
     __syncthreads();
 
-    // ---- 4. T = (I + A_kk)^-1, blocked by 16, fp32 ----
-    if (warp < 4 && lane < 16) {  // diagonal blocks: forward substitution, one column per lane
+    // ---- 4. inverses of the diagonal blocks, T_II = (I + A_II)^-1, fp32 forward substitution ----
+    if (warp < 4 && lane < 16) {  // one column per lane
         const int I = warp, j = lane;
-        const float *A = sA + 16 * I * SM::AS + 16 * I;
+        const float *A = sAd + I * 16 * 17;
         float tcol[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float acc = i == j ? 1.f : 0.f;
 #pragma unroll
-            for (int kk = 0; kk < i; ++kk) acc -= A[i * SM::AS + kk] * tcol[kk];
+            for (int kk = 0; kk < i; ++kk) acc -= A[i * 17 + kk] * tcol[kk];
             tcol[i] = acc;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sT[(16 * I + i) * SM::AS + 16 * I + j] = tcol[i];
-    }
-    __syncthreads();
-    float *sX = reinterpret_cast<float *>(smem + SM::KR);  // [3][16][16] scratch
-    for (int d = 1; d < 4; ++d) {  // blocks (J + d, J), all threads: X = sum_K A_IK T_KJ, then T_IJ = -T_II X
-        const int nb = 4 - d;
-        for (int o = tid; o < nb * 256; o += kThreads) {
-            const int J = o >> 8, I = J + d, r = (o >> 4) & 15, c = o & 15;
-            float x = 0.f;
-            for (int Kb = J; Kb < I; ++Kb) {
-                const float *a = sA + (16 * I + r) * SM::AS + 16 * Kb;
-                const float *t = sT + (16 * Kb) * SM::AS + 16 * J + c;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) x += a[m] * t[m * SM::AS];
-            }
-            sX[o] = x;
-        }
-        __syncthreads();
-        for (int o = tid; o < nb * 256; o += kThreads) {
-            const int J = o >> 8, I = J + d, r = (o >> 4) & 15, c = o & 15;
-            const float *t = sT + (16 * I + r) * SM::AS + 16 * I;
-            const float *x = sX + (J << 8) + c;
-            float y = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) y += t[m] * x[m * 16];
-            sT[(16 * I + r) * SM::AS + 16 * J + c] = -y;
-        }
-        __syncthreads();
-    }
-    // T' = T diag(beta) as bf16 (the A operand of W and U), zero above the block diagonal
-    for (int e = tid; e < C * (C / 2); e += kThreads) {
-        const int i = e / (C / 2), j = 2 * (e % (C / 2));
-        const bool keep = (j >> 4) <= (i >> 4);
-        const float t0v = keep ? sT[i * SM::AS + j] * sBeta[j] : 0.f;
-        const float t1v = keep ? sT[i * SM::AS + j + 1] * sBeta[j + 1] : 0.f;
-        *reinterpret_cast<uint32_t *>(smem + SM::G + swz_off<128>(i, j)) = pack_bf16x2(t0v, t1v);
+        for (int i = 0; i < 16; ++i)
+            *reinterpret_cast<uint16_t *>(smem + SM::TD + swz_off<128>(16 * I + i, 16 * I + j)) = f32_to_bf16_bits(tcol[i]);
     }
     __syncthreads();
 
-    // ---- 5. W = T' (K e^G) (warps 0-3, e^G = P L on the B fragments), U = T' V (warps 4-7) ----
+    // ---- 5. W = (I + A)^-1 diag(beta) K e^G and U = (I + A)^-1 diag(beta) V, by block
+    //         forward substitution: X_I = base_I - sum_{K<I} A_IK Y_K, Y_I = T_II X_I.
+    //         Warps 0-3: W, warps 4-7: U; each warp owns D / NW columns and, since
+    //         every product keeps columns apart, needs no other warp's results. ----
     {
-        const int I = warp & 3;
+        constexpr int NW = D / 16 < 4 ? D / 16 : 4;  // warps per matrix with work
+        constexpr int COLS = D / NW, NP = COLS / 16;
         const bool is_u = warp >= 4;
-        const char *bsrc = smem + (is_u ? SM::VS : SM::KP);
-        float acc[D / 8][4] = {};
-        for (int ks = 0; ks <= I; ++ks) {  // T' is block lower triangular
-            uint32_t a[4];
-            ldmatrix_x4(a, smem_u32(smem + SM::G + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
+        const int q4 = warp & 3;
+        const int c0 = q4 * COLS;
+        char *ytile = smem + (is_u ? SM::QP : SM::KR);  // Y = U or W, [64][D] bf16
+        char *xtile = smem + (is_u ? SM::XU : SM::XW);  // X_I, [16][D] bf16
+        for (int I = 0; I < 4; ++I) {
+            if (q4 < NW) {
+                float acc[2 * NP][4] = {};
+                for (int K = 0; K < I; ++K) {
+                    uint32_t a[4];
+                    ldmatrix_x4(a, smem_u32(smem + SM::AB + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * K + 8 * (mi >> 1))));
 #pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
-                uint32_t b[4];
-                ldmatrix_x4_trans(b, smem_u32(bsrc + swz_off<RB>(16 * ks + ri + 8 * (mi & 1), 16 * np + 8 * (mi >> 1))));
-                if (!is_u) {  // row block ks of k P times L_ks, per channel
-                    const float f0 = sL[ks * D + 16 * np + gid], f1 = sL[ks * D + 16 * np + 8 + gid];
-                    b[0] = scale_bf16x2(b[0], f0, f0);
-                    b[1] = scale_bf16x2(b[1], f0, f0);
-                    b[2] = scale_bf16x2(b[2], f1, f1);
-                    b[3] = scale_bf16x2(b[3], f1, f1);
+                    for (int np = 0; np < NP; ++np) {
+                        uint32_t b[4];
+                        ldmatrix_x4_trans(b, smem_u32(ytile + swz_off<RB>(16 * K + ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
+                        mma_bf16(acc[2 * np], a, b[0], b[1]);
+                        mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+                    }
                 }
-                mma_bf16(acc[2 * np], a, b[0], b[1]);
-                mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
-            }
-        }
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
+                for (int n = 0; n < 2 * NP; ++n) {
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int i = 16 * I + gid + 8 * hr;
-                const int c = 8 * n + 2 * tig;
-                if (!is_u) {  // W staging [64][D] in the KR region
-                    *reinterpret_cast<uint32_t *>(smem + SM::KR + swz_off<RB>(i, c)) =
-                        pack_bf16x2(acc[n][2 * hr], acc[n][2 * hr + 1]);
-                } else {      // U^T staging [D][64] in the QP region
-                    *reinterpret_cast<uint16_t *>(smem + SM::QP + swz_off<128>(c, i)) = f32_to_bf16_bits(acc[n][2 * hr]);
-                    *reinterpret_cast<uint16_t *>(smem + SM::QP + swz_off<128>(c + 1, i)) =
-                        f32_to_bf16_bits(acc[n][2 * hr + 1]);
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int i = 16 * I + gid + 8 * hr;
+                        const int c = c0 + 8 * n + 2 * tig;
+                        const float bi = sBeta[i];
+                        float b0, b1;
+                        if (!is_u) {  // beta_i k_i e^{G_i} = beta_i (k P)_i L_I
+                            const uint32_t kp = *reinterpret_cast<const uint32_t *>(smem + SM::KP + swz_off<RB>(i, c));
+                            b0 = bi * bf16_lo(kp) * sL[I * D + c];
+                            b1 = bi * bf16_hi(kp) * sL[I * D + c + 1];
+                        } else {      // beta_i v_i
+                            const uint32_t vv = *reinterpret_cast<const uint32_t *>(smem + SM::VS + swz_off<RB>(i, c));
+                            b0 = bi * bf16_lo(vv);
+                            b1 = bi * bf16_hi(vv);
+                        }
+                        *reinterpret_cast<uint32_t *>(xtile + swz_off<RB>(i - 16 * I, c)) =
+                            pack_bf16x2(b0 - acc[n][2 * hr], b1 - acc[n][2 * hr + 1]);
+                    }
                 }
             }
+            __syncwarp();  // X_I columns of this warp are complete (no other warp reads them)
+            if (q4 < NW) {
+                float acc[2 * NP][4] = {};
+                uint32_t a[4];
+                ldmatrix_x4(a, smem_u32(smem + SM::TD + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * I + 8 * (mi >> 1))));
+#pragma unroll
+                for (int np = 0; np < NP; ++np) {
+                    uint32_t b[4];
+                    ldmatrix_x4_trans(b, smem_u32(xtile + swz_off<RB>(ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
+                    mma_bf16(acc[2 * np], a, b[0], b[1]);
+                    mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+                }
+#pragma unroll
+                for (int n = 0; n < 2 * NP; ++n) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int i = 16 * I + gid + 8 * hr;
+                        const int c = c0 + 8 * n + 2 * tig;
+                        const float y0 = acc[n][2 * hr], y1 = acc[n][2 * hr + 1];
+                        *reinterpret_cast<uint32_t *>(ytile + swz_off<RB>(i, c)) = pack_bf16x2(y0, y1);
+                        if (is_u) {  // U^T [D][64] straight into the record
+                            *reinterpret_cast<uint16_t *>(rec + R::UT + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
+                            *reinterpret_cast<uint16_t *>(rec + R::UT + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);
+                        }
+                    }
+                }
+            }
+            __syncwarp();  // Y_I columns of this warp are complete
         }
     }
     __syncthreads();
 
-    // ---- 6. W and U^T out to the record (Q~, K~, A_qk, gamma are already there) ----
+    // ---- 6. W out to the record (Q~, K~, A_qk, gamma and U^T are already there) ----
     {
         const uint4 *sw = reinterpret_cast<const uint4 *>(smem + SM::KR);
-        const uint4 *su = reinterpret_cast<const uint4 *>(smem + SM::QP);
         uint4 *gw = reinterpret_cast<uint4 *>(rec + R::W);
-        uint4 *gu = reinterpret_cast<uint4 *>(rec + R::UT);
 #pragma unroll
         for (int e = tid; e < R::TILE / 16; e += kThreads) gw[e] = sw[e];
-#pragma unroll
-        for (int e = tid; e < D * C * 2 / 16; e += kThreads) gu[e] = su[e];
     }
 }
 

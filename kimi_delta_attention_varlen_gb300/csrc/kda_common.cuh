@@ -29,6 +29,14 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f)
     return *reinterpret_cast<uint16_t *>(&h);
 }
 
+// 2^x with the hardware's approximate exponential (denormal results flush to 0).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Load one element of an io tensor (fp32 or bf16) as fp32.
 template <typename T> __device__ __forceinline__ float load_as_f32(const T *p);
 template <> __device__ __forceinline__ float load_as_f32<float>(const float *p) { return *p; }
@@ -166,6 +174,18 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// 16-byte global -> shared asynchronous copy; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst_smem), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
 
 // ------------------------------------------------------ cache-hinted I/O --

@@ -6,7 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/kda.h"
+#include "kda.h"
 
 namespace kda {
 
