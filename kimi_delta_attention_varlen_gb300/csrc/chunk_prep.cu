@@ -136,7 +136,7 @@ chunk_prep_kernel(PrepParams p)
 {
     using SM = PrepSmem<D>;
     using R = Rec<D>;
-    constexpr int RB = R::RB;
+    constexpr int ROWB = tile_row_bytes<D>();   // bytes per tile row
     constexpr int CPL = D / 32;                 // channels per lane in the row pass
     constexpr int ROWS = C / kWarps;            // rows per warp
     constexpr int PRE = (sizeof(IO) == 2 || CPL < 4) ? ROWS : ROWS / 2;  // rows loaded per batch
@@ -207,13 +207,13 @@ chunk_prep_kernel(PrepParams p)
         cp_async16(smem_u32(sG + i * D + 4 * c4), p.g + ((t0 + ii) * H + h) * D + 4 * c4, i < len ? 16u : 0u);
     }
     if constexpr (kStage) {  // q -> QP, k -> KP, v -> VS tiles, 16-byte chunks, zeros past the end
-        constexpr int CH = RB / 16;  // chunks per row
+        constexpr int CH = D / 8;    // 16-byte chunks per row
 #pragma unroll
         for (int e = tid; e < C * CH; e += kThreads) {
             const int i = e / CH, ch = e % CH;
             const int ii = i < len ? i : 0;
             const int64_t off = ((t0 + ii) * H + h) * D + 8 * ch;
-            const uint32_t so = swz_off<RB>(i, 8 * ch);
+            const uint32_t so = tile_off<D, C>(i, 8 * ch);
             const uint32_t nb = i < len ? 16u : 0u;
             cp_async16(smem_u32(smem + SM::QP + so), qg + off, nb);
             cp_async16(smem_u32(smem + SM::KP + so), kg + off, nb);
@@ -267,7 +267,7 @@ chunk_prep_kernel(PrepParams p)
 #pragma unroll
         for (int j = 0; j < PRE; ++j) {
             const int i = warp + kWarps * (j0 + j);
-            const uint32_t o = swz_off<RB>(i, cb);
+            const uint32_t o = tile_off<D, C>(i, cb);
             float qv[CPL], kv[CPL], vv[CPL];
             if constexpr (kStage) {
                 load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::QP + o), qv);
@@ -319,6 +319,13 @@ chunk_prep_kernel(PrepParams p)
     }
     __syncthreads();
 
+    // A_qk blocks above the diagonal are zero (the record is used as a full 64 x 64 operand)
+    for (int e = tid; e < 6 * 16 * 2; e += kThreads) {
+        const int b = e >> 5, r = (e >> 1) & 15, ch = e & 1;
+        const int I = b < 3 ? 0 : b < 5 ? 1 : 2;        // upper blocks (I, J), J > I
+        const int J = b < 3 ? b + 1 : b < 5 ? b - 1 : 3;
+        *reinterpret_cast<uint4 *>(rec + R::AQK + swz_off<128>(16 * I + r, 16 * J + 8 * ch)) = make_uint4(0u, 0u, 0u, 0u);
+    }
     // ---- 3. gated Gram products, 20 (matrix, I, J) block pairs over 8 warps ----
     // A_kk (x beta_i, strictly lower) -> bf16 tile for the substitution products, and its
     // diagonal blocks in fp32 for their inverses; A_qk (x scale, causal) -> the record.
@@ -345,7 +352,7 @@ chunk_prep_kernel(PrepParams p)
                     const int I = pI[u], J = pJ[u];
                     uint32_t a[4], b[4];
                     ldmatrix_x4(a, smem_u32(smem + (pqk[u] ? SM::QP : SM::KP) +
-                                            swz_off<RB>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
+                                            tile_off<D, C>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
                     if (J < I) {  // a <- a * F_IJ on the fragment's four channels (bf16x2 products)
                         const uint16_t *f = sFb + fslot(I, J) * D + 16 * ks + 2 * tig;
                         const uint32_t f01 = *reinterpret_cast<const uint32_t *>(f);
@@ -355,7 +362,7 @@ chunk_prep_kernel(PrepParams p)
                         a[2] = mul_bf16x2(a[2], f23);
                         a[3] = mul_bf16x2(a[3], f23);
                     }
-                    ldmatrix_x4(b, smem_u32(smem + SM::KR + swz_off<RB>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
+                    ldmatrix_x4(b, smem_u32(smem + SM::KR + tile_off<D, C>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
                     mma_bf16(acc[u][0], a, b[0], b[1]);
                     mma_bf16(acc[u][1], a, b[2], b[3]);
                 }
@@ -422,6 +429,14 @@ chunk_prep_kernel(PrepParams p)
         const int c0 = q4 * COLS;
         char *ytile = smem + (is_u ? SM::QP : SM::KR);  // Y = U or W, [64][D] bf16
         char *xtile = smem + (is_u ? SM::XU : SM::XW);  // X_I, [16][D] bf16
+        // Swizzled byte offset of column c0 + 8n + 2tig within any row r with r % 8 == gid.
+        // (64-row tiles and the 16-row X tile differ only in their slab stride.)
+        uint32_t colo[2 * NP], colx[2 * NP];
+#pragma unroll
+        for (int n = 0; n < 2 * NP; ++n) {
+            colo[n] = tile_off<D, C>(gid, c0 + 8 * n + 2 * tig) - gid * ROWB;
+            colx[n] = tile_off<D, 16>(gid, c0 + 8 * n + 2 * tig) - gid * ROWB;
+        }
         for (int I = 0; I < 4; ++I) {
             if (q4 < NW) {
                 float acc[2 * NP][4] = {};
@@ -431,29 +446,25 @@ chunk_prep_kernel(PrepParams p)
 #pragma unroll
                     for (int np = 0; np < NP; ++np) {
                         uint32_t b[4];
-                        ldmatrix_x4_trans(b, smem_u32(ytile + swz_off<RB>(16 * K + ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
+                        ldmatrix_x4_trans(b, smem_u32(ytile + tile_off<D, C>(16 * K + ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
                         mma_bf16(acc[2 * np], a, b[0], b[1]);
                         mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
                     }
                 }
+                const float bi[2] = {sBeta[16 * I + gid], sBeta[16 * I + gid + 8]};
 #pragma unroll
                 for (int n = 0; n < 2 * NP; ++n) {
+                    const int c = c0 + 8 * n + 2 * tig;
+                    float2 lf = make_float2(1.f, 1.f);
+                    if (!is_u) lf = *reinterpret_cast<const float2 *>(sL + I * D + c);
 #pragma unroll
                     for (int hr = 0; hr < 2; ++hr) {
-                        const int i = 16 * I + gid + 8 * hr;
-                        const int c = c0 + 8 * n + 2 * tig;
-                        const float bi = sBeta[i];
-                        float b0, b1;
-                        if (!is_u) {  // beta_i k_i e^{G_i} = beta_i (k P)_i L_I
-                            const uint32_t kp = *reinterpret_cast<const uint32_t *>(smem + SM::KP + swz_off<RB>(i, c));
-                            b0 = bi * bf16_lo(kp) * sL[I * D + c];
-                            b1 = bi * bf16_hi(kp) * sL[I * D + c + 1];
-                        } else {      // beta_i v_i
-                            const uint32_t vv = *reinterpret_cast<const uint32_t *>(smem + SM::VS + swz_off<RB>(i, c));
-                            b0 = bi * bf16_lo(vv);
-                            b1 = bi * bf16_hi(vv);
-                        }
-                        *reinterpret_cast<uint32_t *>(xtile + swz_off<RB>(i - 16 * I, c)) =
+                        const uint32_t rx = static_cast<uint32_t>(gid + 8 * hr) * ROWB;  // row within block I
+                        const uint32_t base = *reinterpret_cast<const uint32_t *>(
+                            smem + (is_u ? SM::VS : SM::KP) + static_cast<uint32_t>(16 * I) * ROWB + rx + colo[n]);
+                        const float b0 = bi[hr] * bf16_lo(base) * lf.x;  // beta_i k_i e^{G_i} or beta_i v_i
+                        const float b1 = bi[hr] * bf16_hi(base) * lf.y;
+                        *reinterpret_cast<uint32_t *>(xtile + rx + colx[n]) =
                             pack_bf16x2(b0 - acc[n][2 * hr], b1 - acc[n][2 * hr + 1]);
                     }
                 }
@@ -466,7 +477,7 @@ chunk_prep_kernel(PrepParams p)
 #pragma unroll
                 for (int np = 0; np < NP; ++np) {
                     uint32_t b[4];
-                    ldmatrix_x4_trans(b, smem_u32(xtile + swz_off<RB>(ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
+                    ldmatrix_x4_trans(b, smem_u32(xtile + tile_off<D, 16>(ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
                     mma_bf16(acc[2 * np], a, b[0], b[1]);
                     mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
                 }
@@ -477,7 +488,7 @@ chunk_prep_kernel(PrepParams p)
                         const int i = 16 * I + gid + 8 * hr;
                         const int c = c0 + 8 * n + 2 * tig;
                         const float y0 = acc[n][2 * hr], y1 = acc[n][2 * hr + 1];
-                        *reinterpret_cast<uint32_t *>(ytile + swz_off<RB>(i, c)) = pack_bf16x2(y0, y1);
+                        *reinterpret_cast<uint32_t *>(ytile + static_cast<uint32_t>(i) * ROWB + colo[n]) = pack_bf16x2(y0, y1);
                         if (is_u) {  // U^T [D][64] straight into the record
                             *reinterpret_cast<uint16_t *>(rec + R::UT + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
                             *reinterpret_cast<uint16_t *>(rec + R::UT + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);

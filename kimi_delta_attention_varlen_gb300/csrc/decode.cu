@@ -14,17 +14,17 @@
 //   S'[k][v] = e^{g_k} S[k][v] + k_k u_v,   o_v = scale (b_v + (q.k) u_v)
 // so one pass over the state suffices: read row, two dot products, write row.
 //
-// GPU mapping: one CTA (128 threads) per (request, head).  D/8 lanes share a
-// state row, each holding 8 channels (one 16-byte bf16 vector); a CTA covers
-// 128/(D/8) rows per pass and keeps NR rows per thread in flight.  The kernel
-// is bound by HBM: 2 * D * D * sizeof(cache) bytes per (request, head).
+// GPU mapping: one CTA (up to 256 threads) per (request, head).  D/8 lanes
+// share a state row, each holding 8 channels (one 16-byte bf16 vector); every
+// thread issues the loads of all its rows before using any, so a CTA keeps
+// its whole 32 KiB (bf16, D = 128) state block in flight.  The kernel is bound
+// by HBM: 2 * D * D * sizeof(cache) bytes per (request, head).
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
 namespace kda {
 namespace {
 
-constexpr int kDecodeThreads = 128;
 
 __device__ __forceinline__ void load8(const float *p, float x[8])
 {
@@ -62,120 +62,167 @@ template <int LPR> __device__ __forceinline__ float group_sum(float x)
     return x;
 }
 
+// Threads per CTA: one 16-byte state slice (8 channels) per lane, up to 256 lanes.
+template <int D> __host__ __device__ constexpr int decode_threads() { return D * D / 8 < 256 ? D * D / 8 : 256; }
+
+// Per-item inputs of one lane, loaded one item ahead.
+template <int D, typename IO, int ROWS> struct ItemIn {
+    float q[8], k[8], g[8], v[ROWS], beta;
+    int64_t row;
+};
+
 template <int D, typename IO, typename CT, typename IdxT>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(decode_threads<D>())
 decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta, int32_t H, float scale,
               int32_t l2norm, CT *__restrict__ cache, int64_t n_rows, int64_t row_stride,
-              const IdxT *__restrict__ idx, IO *__restrict__ out)
+              const IdxT *__restrict__ idx, IO *__restrict__ out, int64_t items)
 {
-    constexpr int LPR = D / 8;                     // lanes per state row
-    constexpr int RPP = kDecodeThreads / LPR;      // rows per pass
-    constexpr int PASSES = D / RPP;
-    constexpr int NR = PASSES >= 4 ? 4 : PASSES;   // rows in flight per thread
-    static_assert(PASSES % NR == 0, "row batching");
+    constexpr int THREADS = decode_threads<D>();
+    constexpr int LPR = D / 8;              // lanes per state row
+    constexpr int RPP = THREADS / LPR;      // rows per pass
+    constexpr int ROWS = D / RPP;           // rows per thread
+    constexpr int V16 = 8 * static_cast<int>(sizeof(CT)) / 16;  // 16-byte pieces per slice
+    extern __shared__ __align__(16) uint4 slots[];  // [2 stages][ROWS][V16][THREADS]
 
-    __shared__ float s_out[D];
+    const int tid = threadIdx.x;
+    const int lr = tid % LPR, rip = tid / LPR, c0 = lr * 8;
 
-    const int64_t item = blockIdx.x;
-    const int64_t r = item / H;
-    const int h = static_cast<int>(item % H);
-    const int lr = threadIdx.x % LPR;   // lane within the row group
-    const int rip = threadIdx.x / LPR;  // row within the pass
-    const int c0 = lr * 8;
-    const int64_t tok = r * H + h;
-
-    float qv[8], kv[8], gv[8];
-    load8(q + tok * D + c0, qv);
-    load8(k + tok * D + c0, kv);
-    load8(g + tok * D + c0, gv);
-    float sq = 0.f, sk = 0.f;
+    auto fetch_inputs = [&](int64_t it, ItemIn<D, IO, ROWS> &in) {
+        const int64_t r = it / H, tok = it;
+        load8(q + tok * D + c0, in.q);
+        load8(k + tok * D + c0, in.k);
+        load8(g + tok * D + c0, in.g);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        sq += qv[c] * qv[c];
-        sk += kv[c] * kv[c];
-    }
-    sq = group_sum<LPR>(sq);
-    sk = group_sum<LPR>(sk);
-    const float rq = l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
-    const float rk = l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
-    float ke[8], qe[8], eg[8], kh[8];
-    float qk = 0.f;
+        for (int j = 0; j < ROWS; ++j) in.v[j] = load_as_f32(v + tok * D + j * RPP + rip);
+        in.beta = beta[tok];
+        const int64_t row = static_cast<int64_t>(idx[r]);
+        in.row = (row >= 0 && row < n_rows) ? row : -1;
+    };
+    // Copies this thread's slices of item `it` into stage `s` (nothing for an invalid row).
+    auto fetch_state = [&](int64_t it, int64_t row, int s) {
+        if (row >= 0) {
+            const CT *src = cache + row * row_stride + static_cast<int64_t>(it % H) * D * D;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const float qh = qv[c] * rq;
-        kh[c] = kv[c] * rk;
-        eg[c] = expf(gv[c]);
-        ke[c] = kh[c] * eg[c];
-        qe[c] = qh * eg[c];
-        qk += qh * kh[c];
-    }
-    qk = group_sum<LPR>(qk);
-    const float bt = beta[tok];
-
-    const int64_t row = static_cast<int64_t>(idx[r]);
-    const bool valid = row >= 0 && row < n_rows;
-    CT *srow = cache + (valid ? row : 0) * row_stride + static_cast<int64_t>(h) * D * D;
-    const IO *vrow = v + tok * D;
-
-#pragma unroll 1
-    for (int p0 = 0; p0 < PASSES; p0 += NR) {
-        float s[NR][8];
+            for (int j = 0; j < ROWS; ++j)
 #pragma unroll
-        for (int j = 0; j < NR; ++j) {
-            const int vi = (p0 + j) * RPP + rip;
+                for (int w = 0; w < V16; ++w)
+                    cp_async16(smem_u32(&slots[((s * ROWS + j) * V16 + w) * THREADS + tid]),
+                               src + (j * RPP + rip) * D + c0 + w * (16 / sizeof(CT)), 16u);
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+
+    int64_t it = blockIdx.x;
+    if (it >= items) return;
+    ItemIn<D, IO, ROWS> cur, nxt;
+    fetch_inputs(it, cur);
+    fetch_state(it, cur.row, 0);
+    for (int s = 0; it < items; it += gridDim.x, s ^= 1) {
+        const int64_t it2 = it + gridDim.x;
+        if (it2 < items) {
+            fetch_inputs(it2, nxt);
+            fetch_state(it2, nxt.row, s ^ 1);
+        } else {
+            asm volatile("cp.async.commit_group;\n" ::: "memory");
+        }
+        asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // this item's slices have landed
+
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            sq += cur.q[c] * cur.q[c];
+            sk += cur.k[c] * cur.k[c];
+        }
+        sq = group_sum<LPR>(sq);
+        sk = group_sum<LPR>(sk);
+        const float rq = l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
+        const float rk = l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+        float ke[8], qe[8], eg[8], kh[8];
+        float qk = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float qh = cur.q[c] * rq;
+            kh[c] = cur.k[c] * rk;
+            eg[c] = expf(cur.g[c]);
+            ke[c] = kh[c] * eg[c];
+            qe[c] = qh * eg[c];
+            qk += qh * kh[c];
+        }
+        qk = group_sum<LPR>(qk);
+        const bool valid = cur.row >= 0;
+        CT *dst = cache + (valid ? cur.row : 0) * row_stride + static_cast<int64_t>(it % H) * D * D;
+#pragma unroll
+        for (int j = 0; j < ROWS; ++j) {
+            const int vi = j * RPP + rip;
+            float st[8];
             if (valid) {
-                load8(srow + vi * D + c0, s[j]);
+                if constexpr (V16 == 1) {
+                    const uint4 a = slots[((s * ROWS + j) * V16) * THREADS + tid];
+                    st[0] = bf16_lo(a.x); st[1] = bf16_hi(a.x); st[2] = bf16_lo(a.y); st[3] = bf16_hi(a.y);
+                    st[4] = bf16_lo(a.z); st[5] = bf16_hi(a.z); st[6] = bf16_lo(a.w); st[7] = bf16_hi(a.w);
+                } else {
+                    const uint4 a = slots[((s * ROWS + j) * V16) * THREADS + tid];
+                    const uint4 b = slots[((s * ROWS + j) * V16 + 1) * THREADS + tid];
+                    st[0] = __uint_as_float(a.x); st[1] = __uint_as_float(a.y);
+                    st[2] = __uint_as_float(a.z); st[3] = __uint_as_float(a.w);
+                    st[4] = __uint_as_float(b.x); st[5] = __uint_as_float(b.y);
+                    st[6] = __uint_as_float(b.z); st[7] = __uint_as_float(b.w);
+                }
             } else {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) s[j][c] = 0.f;
+                for (int c = 0; c < 8; ++c) st[c] = 0.f;
             }
-        }
-#pragma unroll
-        for (int j = 0; j < NR; ++j) {
-            const int vi = (p0 + j) * RPP + rip;
             float a = 0.f, b = 0.f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                a += ke[c] * s[j][c];
-                b += qe[c] * s[j][c];
+                a += ke[c] * st[c];
+                b += qe[c] * st[c];
             }
             a = group_sum<LPR>(a);
             b = group_sum<LPR>(b);
-            const float vv = load_as_f32(vrow + vi);
-            const float u = bt * (vv - a);
+            const float u = cur.beta * (cur.v[j] - a);
             if (valid) {
                 float sn[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) sn[c] = eg[c] * s[j][c] + kh[c] * u;
-                store8(srow + vi * D + c0, sn);
+                for (int c = 0; c < 8; ++c) sn[c] = eg[c] * st[c] + kh[c] * u;
+                store8(dst + vi * D + c0, sn);
             }
-            if (lr == 0) s_out[vi] = scale * (b + qk * u);
+            if (lr == 0) out[it * D + vi] = from_f32<IO>(scale * (b + qk * u));
         }
+        cur = nxt;
     }
-    __syncthreads();
-    for (int vi = threadIdx.x; vi < D; vi += kDecodeThreads) out[tok * D + vi] = from_f32<IO>(s_out[vi]);
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
+template <int D, typename IO, typename CT, typename IdxT>
+cudaError_t decode_launch_typed(const DecodeArgs &a, cudaStream_t st)
+{
+    constexpr int THREADS = decode_threads<D>();
+    constexpr int ROWS = D / (THREADS / (D / 8));
+    constexpr int smem = 2 * ROWS * 8 * static_cast<int>(sizeof(CT)) * THREADS;
+    const int64_t items = a.batch * a.h;
+    auto kern = decode_kernel<D, IO, CT, IdxT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem)) != cudaSuccess) return e;
+    const int64_t resident = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    const unsigned grid = static_cast<unsigned>(items < resident ? items : resident);
+    kern<<<grid, THREADS, smem, st>>>(static_cast<const IO *>(a.q), static_cast<const IO *>(a.k),
+                                      static_cast<const IO *>(a.v), a.g, a.beta, a.h, a.scale, a.l2norm,
+                                      static_cast<CT *>(a.cache.data), a.cache.n_rows, a.cache.row_stride,
+                                      static_cast<const IdxT *>(a.idx), static_cast<IO *>(a.out), items);
+    return cudaGetLastError();
 }
 
 template <int D, typename IO, typename CT>
 cudaError_t decode_launch_idx(const DecodeArgs &a, cudaStream_t st)
 {
-    const int64_t items = a.batch * a.h;
-    const dim3 grid(static_cast<unsigned>(items));
-    const IO *q = static_cast<const IO *>(a.q);
-    const IO *k = static_cast<const IO *>(a.k);
-    const IO *v = static_cast<const IO *>(a.v);
-    CT *cache = static_cast<CT *>(a.cache.data);
-    IO *out = static_cast<IO *>(a.out);
-    if (a.idx_type == KDA_I32)
-        decode_kernel<D, IO, CT, int32_t><<<grid, kDecodeThreads, 0, st>>>(
-            q, k, v, a.g, a.beta, a.h, a.scale, a.l2norm, cache, a.cache.n_rows, a.cache.row_stride,
-            static_cast<const int32_t *>(a.idx), out);
-    else
-        decode_kernel<D, IO, CT, int64_t><<<grid, kDecodeThreads, 0, st>>>(
-            q, k, v, a.g, a.beta, a.h, a.scale, a.l2norm, cache, a.cache.n_rows, a.cache.row_stride,
-            static_cast<const int64_t *>(a.idx), out);
-    return cudaGetLastError();
+    return a.idx_type == KDA_I32 ? decode_launch_typed<D, IO, CT, int32_t>(a, st)
+                                 : decode_launch_typed<D, IO, CT, int64_t>(a, st);
 }
 
 template <int D>

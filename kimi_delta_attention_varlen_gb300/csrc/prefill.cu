@@ -40,6 +40,8 @@ namespace {
 
 using prefill::C;
 using prefill::Rec;
+using prefill::tile_off;
+using prefill::PassParams;
 constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier polls
 
 // ---------------------------------------------------------- chunk table ---
@@ -106,25 +108,12 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int32_t *__restric
 
 // ----------------------------------------------------------- state pass ---
 
-struct PassParams {
-    const int32_t *cu;
-    const int32_t *chunk_off;
-    const int32_t *seq_order;
-    int32_t *status;
-    const char *records;
-    int32_t H;
-    const void *init;
-    int32_t init_dtype;
-    float *final_state;
-    void *out;
-};
 
 template <int D, typename IO, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 state_pass_kernel(PassParams p)
 {
     using R = Rec<D>;
-    constexpr int RB = R::RB;
     constexpr int VT = 16 * WARPS;          // value columns per CTA
     constexpr int NSPLIT = D / VT;
     constexpr int HEAD = R::UT;             // W, Q~, K~, A_qk, gamma
@@ -219,7 +208,7 @@ state_pass_kernel(PassParams p)
         for (int np = 0; np < 4; ++np) {
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t o = swz_off<RB>(16 * np + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1));
+                const uint32_t o = tile_off<D, C>(16 * np + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1));
                 uint32_t bw[4], bq[4];
                 ldmatrix_x4(bw, smem_u32(sb + R::W + o));
                 ldmatrix_x4(bq, smem_u32(sb + R::QT + o));
@@ -302,7 +291,7 @@ state_pass_kernel(PassParams p)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     uint32_t bk[4];
-                    ldmatrix_x4_trans(bk, smem_u32(sb + R::KT + swz_off<RB>(16 * ks + ri + 8 * (mi & 1), 16 * np + 8 * (mi >> 1))));
+                    ldmatrix_x4_trans(bk, smem_u32(sb + R::KT + tile_off<D, C>(16 * ks + ri + 8 * (mi & 1), 16 * np + 8 * (mi >> 1))));
                     mma_bf16(s[2 * np], va[ks], bk[0], bk[1]);
                     mma_bf16(s[2 * np + 1], va[ks], bk[2], bk[3]);
                 }

@@ -11,11 +11,22 @@ namespace prefill {
 
 constexpr int C = kChunk;  // 64 tokens per chunk
 
-// One record per (chunk, head).  bf16 tiles are swizzled (see swz_off) so the
-// state pass can bulk-copy a record verbatim into shared memory and read it
-// with conflict-free ldmatrix.
+// Byte offset of bf16 element (r, c) of a [ROWS][D] tile.  D >= 64: the
+// canonical 128-byte-swizzle layout of the tensor cores - 64-column slabs of
+// ROWS rows x 128 bytes, 16-byte chunks XOR-permuted by r % 8 - which serves as
+// a K-major operand when the long side is K and as an MN-major one when it is
+// N.  D == 32: 64-byte rows with the 64-byte permutation.
+template <int D, int ROWS> __device__ __forceinline__ uint32_t tile_off(int r, int c)
+{
+    if constexpr (D >= 64) return static_cast<uint32_t>((c >> 6) * (ROWS * 128)) + swz_off<128>(r, c & 63);
+    else return swz_off<64>(r, c);
+}
+template <int D> __host__ __device__ constexpr int tile_row_bytes() { return D >= 64 ? 128 : 64; }
+
+// One record per (chunk, head).  bf16 tiles use tile_off (A_qk and U^T: 128-
+// byte rows) so the state pass can bulk-copy a record verbatim into shared
+// memory and use it directly as tensor-core operands.
 template <int D> struct Rec {
-    static constexpr int RB = 2 * D;                  // row bytes of [64][D] tiles
     static constexpr int TILE = C * D * 2;            // bf16 [64][D]
     static constexpr int W = 0;                       // W       [64][D]
     static constexpr int QT = TILE;                   // Q~      [64][D]  (scale q e^G)
@@ -48,6 +59,23 @@ struct PrepParams {
     int32_t l2norm;
     char *records;
 };
+
+struct PassParams {
+    const int32_t *cu;
+    const int32_t *chunk_off;
+    const int32_t *seq_order;
+    int32_t *status;
+    const char *records;
+    int32_t H;
+    const void *init;
+    int32_t init_dtype;
+    float *final_state;
+    void *out;
+};
+
+// Launches the tensor-memory state pass (D = 128, bf16 output, one CTA per
+// (sequence, head)) over `items` = num_seqs x h CTAs.
+cudaError_t launch_state_pass_tc(const PassParams &p, int64_t items, cudaStream_t st);
 
 // Launches the chunk-preparation kernel over n_chunk_max x h CTAs.
 cudaError_t launch_chunk_prep(int d, int32_t io_dtype, const PrepParams &p, int64_t n_chunk_max, int32_t h,
