@@ -361,6 +361,12 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     const int64_t items = a.num_seqs * a.h;
     int warps = D / 16;
     while (warps > 1 && items * (D / (16 * warps)) < 120) warps /= 2;
+    if constexpr (D == 128 && sizeof(IO) == 2) {  // one CTA per (sequence, head): tensor-memory state pass
+        if (warps == 8) {
+            if ((e = prefill::launch_state_pass_tc(sp, items, st)) != cudaSuccess) return e;
+            return mark(3);
+        }
+    }
     if constexpr (D == 128) {
         if (warps == 8) e = launch_pass<D, IO, 8>(sp, items, st);
         else if (warps == 4) e = launch_pass<D, IO, 4>(sp, items, st);

@@ -1,0 +1,284 @@
+// Inter-chunk state pass on the 5th-generation tensor cores (tcgen05, TMEM),
+// for head size 128 with bf16 output: one CTA of 128 threads per (sequence,
+// head), walking the sequence's chunks in order.
+//
+// Per chunk, with S the K x V state and the chunk's record (W, Q~, K~, A_qk,
+// gamma, U^T) in shared memory:
+//   X^T = S^T W^T,  Y^T = S^T Q~^T                    (M = 128 value rows, N = 64)
+//   V_new^T = U^T - X^T                               (threads, one value row each)
+//   O^T = Y^T + V_new^T A_qk^T,  S^T <- S^T diag(gamma) + V_new^T K~   (N = 64, 128)
+// which is the chunkwise form of S_t = (I - beta k k^T) Diag(e^g) S + beta k v^T,
+// o_t = scale S^T q of the "KDA's challenges for AI infra" page (section 1.1),
+// in the order of the "Support Kimi-K3 on NPU" report's extend listing.
+//
+// Layout: S^T (fp32, 128 lanes x 128 columns), X^T (64 columns) and two
+// Y^T/O^T buffers (64 columns each) live in tensor memory.  Value row v is TMEM
+// lane v; two warps share each 32-lane quadrant and split its columns.  The MMA
+// operands are bf16 in shared memory in the 128-byte-swizzle layout: S^T and
+// V_new^T written by the threads each chunk, W, Q~, A_qk (K-major) and K~
+// (MN-major) straight from the bulk-copied record.  One thread issues the MMAs;
+// an mbarrier signals their completion.  Records are double-buffered (the
+// copy of chunk i + 2 starts when chunk i is done), and the outputs of chunk
+// i - 1 are written while the first MMA group of chunk i runs.  Every wait is bounded; an expired wait sets the
+// workspace status word and the CTA stops waiting (and still frees its TMEM).
+#include "prefill_common.cuh"
+#include "tcgen05.cuh"
+
+namespace kda {
+namespace prefill {
+namespace {
+
+constexpr int kTcThreads = 256;
+constexpr uint32_t kTcWaitLimit = 1u << 22;
+constexpr int kTcD = 128;
+using RT = Rec<kTcD>;
+constexpr int kStage = (RT::BYTES + 1023) / 1024 * 1024;  // one record, padded to 1 KiB
+constexpr int kSA = 2 * kStage;          // S^T bf16 [128][128] (2 slabs); V_new^T [128][64] reuses slab 0
+constexpr int kOS = kSA + 32768;         // output staging bf16 [64 tokens][128 values]
+constexpr int kTcSmem = kOS + 16384 + 1024;  // + slack to align the base to 1 KiB
+constexpr uint32_t kColS = 0, kColX = 128, kColY = 192, kTmemCols = 512;  // Y buffers at 192 and 256
+
+// Byte offset of (row, col) in a [rows][64k] bf16 operand: 64-column slabs of rows x 128 bytes.
+__device__ __forceinline__ uint32_t op_off(int rows, int row, int col)
+{
+    return static_cast<uint32_t>((col >> 6) * rows * 128) + swz_off<128>(row, col & 63);
+}
+
+__device__ __forceinline__ uint4 pack8(const uint32_t *r)
+{
+    return make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                      pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                      pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                      pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+state_pass_tc_kernel(PassParams p)
+{
+    extern __shared__ char smem_raw[];
+    char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bars[3];  // two record stages, MMA completion
+    __shared__ uint32_t tmem_base;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int quad = warp & 3, half = warp >> 2;   // TMEM lane quadrant; which half of the columns
+    const int v = 32 * quad + (tid & 31);          // value row = TMEM lane
+    const int64_t H = p.H;
+    const int64_t item = blockIdx.x;
+    const int h = static_cast<int>(item % H);
+    const int64_t b = p.seq_order[item / H];
+    const int32_t c_begin = p.chunk_off[b], n_chunks = p.chunk_off[b + 1] - c_begin;
+    const int64_t tok_begin = p.cu[b], tok_end = p.cu[b + 1];
+
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
+        fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);  // this warp's lanes
+
+    // initial state: columns [64 half, 64 half + 64) of S^T row v (= cache row [v][k])
+    {
+        const int64_t base = ((b * H + h) * kTcD + v) * kTcD;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c0 = 64 * half + 32 * j;
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.init != nullptr) {
+                    if (p.init_dtype == KDA_F32) {
+                        x = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.init) + base + c0 + e);
+                    } else {
+                        const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.init) + base + c0 + e);
+                        x = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+                    }
+                }
+                r[e] = __float_as_uint(x.x);
+                r[e + 1] = __float_as_uint(x.y);
+                r[e + 2] = __float_as_uint(x.z);
+                r[e + 3] = __float_as_uint(x.w);
+            }
+            tc::st32(tl + kColS + c0, r);
+        }
+        tc::wait_st();
+    }
+
+    auto issue = [&](int32_t i, int st) {  // record of chunk i -> stage st (thread 0)
+        const char *rec = p.records + (static_cast<int64_t>(c_begin + i) * H + h) * RT::BYTES;
+        mbar_arrive_expect_tx(&bars[st], RT::BYTES);
+        bulk_g2s(smem + st * kStage, rec, RT::BYTES, &bars[st]);
+    };
+    if (tid == 0) {
+        if (n_chunks > 0) issue(0, 0);
+        if (n_chunks > 1) issue(1, 1);
+    }
+
+    constexpr uint32_t kIdN64 = tc::idesc_bf16(128, 64, false);
+    constexpr uint32_t kIdN128Mn = tc::idesc_bf16(128, 128, true);
+    const uint32_t sa = smem_u32(smem + kSA);
+    uint32_t mma_phase = 0;
+    bool gave_up = false;
+    auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
+        if (!gave_up && !mbar_wait(bar, parity, kTcWaitLimit)) {
+            gave_up = true;
+            if ((tid & 31) == 0) atomicExch(p.status, 2);
+        }
+    };
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+
+    // Outputs of chunk c (O^T in Y buffer c & 1): staging [t][v], then whole output rows.
+    auto write_outputs = [&](int32_t c) {
+        const int64_t t0 = tok_begin + static_cast<int64_t>(c) * C;
+        const int len = static_cast<int>(tok_end - t0 < C ? tok_end - t0 : C);
+        __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(smem + kOS);
+        uint32_t y[32];
+        tc::ld32(tl + kColY + 64 * (c & 1) + 32 * half, y);
+        tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) os[(32 * half + e) * kTcD + v] = __float2bfloat16_rn(__uint_as_float(y[e]));
+        __syncthreads();
+        const uint4 *src = reinterpret_cast<const uint4 *>(os);
+#pragma unroll
+        for (int e = tid; e < C * (kTcD * 2 / 16); e += kTcThreads) {
+            const int t = e >> 4, part = e & 15;
+            if (t < len) reinterpret_cast<uint4 *>(out + ((t0 + t) * H + h) * kTcD)[part] = src[e];
+        }
+        __syncthreads();
+    };
+
+    for (int32_t i = 0; i < n_chunks; ++i) {
+        const int st = i & 1;
+        wait_bar(&bars[st], (i >> 1) & 1);
+        const char *sb = smem + st * kStage;
+        const float4 *gam4 = reinterpret_cast<const float4 *>(sb + RT::GAMMA);
+        const uint32_t ycol = kColY + 64 * static_cast<uint32_t>(i & 1);
+
+        // (A) S^T row v, this warp's 64 columns -> bf16 operand (undecayed); decay the TMEM copy by gamma
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c0 = 64 * half + 32 * j;
+            uint32_t r[32];
+            tc::ld32(tl + kColS + c0, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(smem + kSA + op_off(128, v, c0 + 8 * q)) = pack8(r + 8 * q);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 gv = gam4[(c0 + e) >> 2];
+                r[e] = __float_as_uint(__uint_as_float(r[e]) * gv.x);
+                r[e + 1] = __float_as_uint(__uint_as_float(r[e + 1]) * gv.y);
+                r[e + 2] = __float_as_uint(__uint_as_float(r[e + 2]) * gv.z);
+                r[e + 3] = __float_as_uint(__uint_as_float(r[e + 3]) * gv.w);
+            }
+            tc::st32(tl + kColS + c0, r);
+        }
+        tc::wait_st();
+        fence_proxy_async_smem();  // generic-proxy operand writes -> visible to the tensor cores
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+
+        // (B) X^T = S^T W^T and Y^T = S^T Q~^T: M = 128, N = 64, K = 128 in 8 steps of 16
+        if (tid == 0) {
+            const uint32_t w = smem_u32(sb + RT::W), qt = smem_u32(sb + RT::QT);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t a = tc::sdesc_sw128(sa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
+                tc::mma_bf16(tmem + kColX, a, tc::sdesc_sw128(w + kb, 16, 1024), kIdN64, ks > 0 ? 1u : 0u);
+                tc::mma_bf16(tmem + ycol, a, tc::sdesc_sw128(qt + kb, 16, 1024), kIdN64, ks > 0 ? 1u : 0u);
+            }
+            tc::commit(&bars[2]);
+        }
+        if (i > 0) write_outputs(i - 1);  // the previous chunk's outputs, while these MMAs run
+        wait_bar(&bars[2], mma_phase);
+        mma_phase ^= 1u;
+        tc::fence_after_sync();
+
+        // (C) V_new^T row v, this warp's 32 columns = U^T - X^T -> bf16 operand (slab 0 of S^T's)
+        {
+            uint32_t x[32];
+            tc::ld32(tl + kColX + 32 * half, x);
+            tc::wait_ld();
+            const char *ut = sb + RT::UT;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t off = swz_off<128>(v, 32 * half + 8 * q);
+                const uint4 u = *reinterpret_cast<const uint4 *>(ut + off);
+                const uint32_t *xx = x + 8 * q;
+                uint4 w;
+                w.x = pack_bf16x2(bf16_lo(u.x) - __uint_as_float(xx[0]), bf16_hi(u.x) - __uint_as_float(xx[1]));
+                w.y = pack_bf16x2(bf16_lo(u.y) - __uint_as_float(xx[2]), bf16_hi(u.y) - __uint_as_float(xx[3]));
+                w.z = pack_bf16x2(bf16_lo(u.z) - __uint_as_float(xx[4]), bf16_hi(u.z) - __uint_as_float(xx[5]));
+                w.w = pack_bf16x2(bf16_lo(u.w) - __uint_as_float(xx[6]), bf16_hi(u.w) - __uint_as_float(xx[7]));
+                *reinterpret_cast<uint4 *>(smem + kSA + off) = w;
+            }
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+
+        // (D) Y^T += V_new^T A_qk^T (N = 64) and S^T += V_new^T K~ (N = 128, K~ MN-major), K = 64
+        if (tid == 0) {
+            const uint32_t aq = smem_u32(sb + RT::AQK), kt = smem_u32(sb + RT::KT);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t a = tc::sdesc_sw128(sa + ks * 32, 16, 1024);
+                tc::mma_bf16(tmem + ycol, a, tc::sdesc_sw128(aq + ks * 32, 16, 1024), kIdN64, 1u);
+                tc::mma_bf16(tmem + kColS, a, tc::sdesc_sw128(kt + ks * 2048, 8192, 1024), kIdN128Mn, 1u);
+            }
+            tc::commit(&bars[2]);
+        }
+        wait_bar(&bars[2], mma_phase);
+        mma_phase ^= 1u;
+        tc::fence_after_sync();
+        // Every read of this stage is over (gamma in A and U^T in C precede the barriers above,
+        // the MMAs have completed): refill it with chunk i + 2.
+        if (tid == 0 && i + 2 < n_chunks) issue(i + 2, st);
+    }
+    if (n_chunks > 0) write_outputs(n_chunks - 1);
+
+    if (p.final_state != nullptr) {
+        float *fs = p.final_state + ((b * H + h) * kTcD + v) * kTcD;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c0 = 64 * half + 32 * j;
+            uint32_t r[32];
+            tc::ld32(tl + kColS + c0, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4 *>(fs + c0 + e) = make_float4(
+                    __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_state_pass_tc(const PassParams &p, int64_t items, cudaStream_t st)
+{
+    cudaError_t e = cudaFuncSetAttribute(state_pass_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (e != cudaSuccess) return e;
+    state_pass_tc_kernel<<<static_cast<unsigned>(items), kTcThreads, kTcSmem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace prefill
+}  // namespace kda

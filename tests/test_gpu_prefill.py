@@ -65,6 +65,29 @@ def test_prefill_ragged_varlen(D, io, decay):
     assert torch.equal(fin[4], init[4])  # the empty sequence keeps its state bit for bit
 
 
+@pytest.mark.parametrize("init_kind", ["fp32", "bf16", "none"])
+def test_prefill_many_heads(init_kind):
+    """Enough (sequence, head) pairs for one CTA per pair (the tensor-memory state
+    pass at head size 128, bf16): ragged lengths, an empty sequence, every init kind."""
+    lengths, H, D = [1, 63, 64, 65, 0, 130], 64, 128
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    inp = wl.token_inputs(cu[-1], H, D, D, torch.bfloat16, seed=40, device=DEV, decay_scale=0.3)
+    init = None
+    if init_kind != "none":
+        init = torch.randn(len(lengths), H, D, D, generator=wl.generator(41, DEV), device=DEV)
+        if init_kind == "bf16":
+            init = init.to(torch.bfloat16)
+    out, fin = run_prefill(inp, cu, H, D, init=init, scale=D ** -0.5)
+    ref_init = None if init is None else init.float()
+    check_against_oracle(inp, cu, H, D, ref_init, out, fin, D ** -0.5, heads=[0, 17, 63])
+    if init is not None:
+        assert torch.equal(fin[4], init[4].float())  # the empty sequence keeps its state
+    else:
+        assert not torch.any(fin[4] != 0)
+
+
 def test_prefill_bf16_init_and_no_final():
     lengths, H, D = [130, 7], 2, 128
     cu = [0, 130, 137]
