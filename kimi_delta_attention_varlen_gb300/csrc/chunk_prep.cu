@@ -10,19 +10,21 @@
 // gamma = e^{G_last}.
 //
 // GPU mapping: one CTA (8 warps) per (chunk, head), two CTAs per SM.  All
-// global loads of the chunk are issued up front into registers (q/k/v rows
-// per warp, g columns per cumsum thread), so one memory latency covers the
-// whole chunk and the co-resident CTA's compute hides it.  The gated Gram
-// products and W, U run on the tensor cores (bf16 operands, fp32 accumulate);
-// W and U come from block forward substitution on (I + A_kk): only the four
-// 16x16 diagonal inverses are formed (fp32), every product is an MMA.
+// global loads of the chunk are issued up front: q/k/v rows by cp.async into
+// their operand tiles, each warp's 8 consecutive g rows into registers, where
+// the in-chunk cumulative sum runs (warp totals are exchanged once through
+// shared memory).  The gated Gram products and W, U run on the tensor cores
+// (bf16 operands, fp32 accumulate); W and U come from block forward
+// substitution on (I + A_kk), computed in place over their right-hand sides:
+// only the four 16x16 diagonal inverses are formed (fp32), every product is an
+// MMA.  W and U^T leave through two bulk copies.
 //
 // Exponents: e^{G_i - G_j} = P_i F_IJ R_j with P_i = e^{G_i - G_mI},
 // R_j = e^{G_mJ - G_j} (m = midpoint of the 16-row block) and F_IJ =
 // e^{G_mI - G_mJ} <= 1 applied to the A fragments; P and R each span at most 8
-// tokens of decay.  beta is folded into T (T' = T diag(beta)) and e^G = P L_I
-// (L_I = e^{G_mI}) is applied to the k P tile's B fragments, so neither
-// beta V nor beta k e^G needs a tile of its own.
+// tokens of decay.  beta is folded into the substitution's right-hand sides and
+// e^G = P L_I (L_I = e^{G_mI}), so neither beta V nor beta k e^G needs a tile
+// of its own.
 #include <type_traits>
 
 #include "prefill_common.cuh"
@@ -37,24 +39,24 @@ constexpr int kWarps = kThreads / 32;
 template <int D> struct PrepSmem {
     static constexpr int TILE = C * D * 2;                 // bf16 [64][D]
     static constexpr int XT = 16 * D * 2;                  // bf16 [16][D]
-    // G region: G fp32 [64][D] during the row pass; afterwards A_kk bf16, T_diag bf16,
-    // the diagonal blocks of A_kk in fp32 and the two substitution tiles X_W, X_U.
+    // Matrix region: A_kk bf16, T_diag bf16, the diagonal blocks of A_kk in fp32
+    // and the two substitution tiles X_W, X_U.  Before the Gram products it holds
+    // the cumulative-sum exchange (warp totals and first rows, fp32 [12][D]).
     static constexpr int AB = 0;                           // A_kk bf16 [64][64]
     static constexpr int TD = AB + C * C * 2;              // diag(T_00..T_33) bf16 [64][64]
     static constexpr int AD = TD + C * C * 2;              // A_II fp32 [4][16][17]
     static constexpr int XW = (AD + 4 * 16 * 17 * 4 + 127) / 128 * 128;
     static constexpr int XU = XW + XT;
-    static constexpr int GREG0 = C * D * 4 > XU + XT ? C * D * 4 : XU + XT;
-    static constexpr int GREG = (GREG0 + 127) / 128 * 128;
-    static constexpr int G = 0;
-    static constexpr int KP = GREG;      // k P: Gram A operand, W base
-    static constexpr int QP = KP + TILE; // q P: Gram A operand -> U tile
-    static constexpr int KR = QP + TILE; // k R: Gram B operand -> W tile
-    static constexpr int VS = KR + TILE; // v (bf16): U base
-    static constexpr int TAB = VS + TILE;                  // L[4][D], Z[4][D], F[6][D], L*scale[4][D]
-    static constexpr int BETA = TAB + 18 * D * 4;          // beta [64]
-    static constexpr int TOT = BETA + C * 4;               // cumsum segment totals
-    static constexpr int BYTES = TOT + kThreads * 4;
+    static constexpr int SUMS = 0;                         // fp32 [8][D] warp totals, [4][D] first rows
+    static constexpr int MREG0 = XU + XT > 12 * D * 4 ? XU + XT : 12 * D * 4;
+    static constexpr int MREG = (MREG0 + 127) / 128 * 128;
+    static constexpr int KP = MREG;      // k P: Gram A operand, W right-hand side -> W
+    static constexpr int QP = KP + TILE; // q P: Gram A operand -> U^T staging [D][64]
+    static constexpr int KR = QP + TILE; // k R: Gram B operand
+    static constexpr int VS = KR + TILE; // v (bf16): U right-hand side -> U
+    static constexpr int TAB = VS + TILE;                  // L[4][D] fp32, F[6][D] bf16
+    static constexpr int BETA = TAB + 4 * D * 4 + 6 * D * 2;  // beta [64]
+    static constexpr int BYTES = BETA + C * 4;
 };
 
 // CPL io elements of one row, kept packed in registers until used.
@@ -130,6 +132,34 @@ __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float f0, float f1)
 // Slot of the factor F_IJ (J < I) in the F table.
 __device__ __forceinline__ int fslot(int I, int J) { return I * (I - 1) / 2 + J; }
 
+// N consecutive fp32 values from global memory (N = 1, 2, 4; aligned to N floats).
+template <int N> __device__ __forceinline__ void ldg_f32(const float *p, float x[N])
+{
+    if constexpr (N == 4) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    } else if constexpr (N == 2) {
+        const float2 a = __ldg(reinterpret_cast<const float2 *>(p));
+        x[0] = a.x; x[1] = a.y;
+    } else {
+        x[0] = __ldg(p);
+    }
+}
+
+// N consecutive fp32 values to shared or global memory (aligned to N floats).
+template <int N> __device__ __forceinline__ void st_f32(float *p, const float x[N])
+{
+    if constexpr (N == 4) *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    else if constexpr (N == 2) *reinterpret_cast<float2 *>(p) = make_float2(x[0], x[1]);
+    else *p = x[0];
+}
+
+// v[idx] for a warp-uniform runtime idx in 0..3, without local-memory indexing.
+__device__ __forceinline__ float pick4(const float v0, const float v1, const float v2, const float v3, int idx)
+{
+    return idx == 0 ? v0 : idx == 1 ? v1 : idx == 2 ? v2 : v3;
+}
+
 template <int D, typename IO>
 __global__ void __launch_bounds__(kThreads, 2)
 chunk_prep_kernel(PrepParams p)
@@ -138,55 +168,39 @@ chunk_prep_kernel(PrepParams p)
     using R = Rec<D>;
     constexpr int ROWB = tile_row_bytes<D>();   // bytes per tile row
     constexpr int CPL = D / 32;                 // channels per lane in the row pass
-    constexpr int ROWS = C / kWarps;            // rows per warp
-    constexpr int PRE = (sizeof(IO) == 2 || CPL < 4) ? ROWS : ROWS / 2;  // rows loaded per batch
-    constexpr int SEG = kThreads / D;           // cumsum segments per channel
-    constexpr int RPS = C / SEG;                // rows per segment
+    constexpr int ROWS = C / kWarps;            // consecutive rows per warp (8: half a 16-row block)
+    constexpr int PRE = (sizeof(IO) == 2 || CPL < 4) ? ROWS : ROWS / 2;  // fp32 rows loaded per batch
     extern __shared__ __align__(1024) char smem[];
-    __shared__ int32_t s_seq[2];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, ri = lane & 7;
     const int64_t chunk = blockIdx.x;
     const int h = blockIdx.y;
-    if (chunk >= p.chunk_off[p.B]) return;
-    if (tid == 0) {  // the sequence b with chunk_off[b] <= chunk < chunk_off[b + 1]
-        int64_t lo = 0, hi = p.B;
-        while (lo < hi) {
-            const int64_t mid = (lo + hi + 1) / 2;
-            if (p.chunk_off[mid] <= chunk) lo = mid;
-            else hi = mid - 1;
-        }
-        const int32_t t0 = p.cu[lo] + static_cast<int32_t>(chunk - p.chunk_off[lo]) * C;
-        const int32_t left = p.cu[lo + 1] - t0;
-        s_seq[0] = t0;
-        s_seq[1] = left < C ? left : C;
-    }
-    __syncthreads();
-    const int64_t t0 = s_seq[0];
-    const int len = s_seq[1];
+    const int2 info = p.chunk_info[chunk];
+    const int len = info.y;
+    if (len <= 0) return;  // past the last chunk (uniform over the CTA)
+    const int64_t t0 = info.x;
     const int64_t H = p.H;
     char *rec = p.records + (chunk * H + h) * static_cast<int64_t>(R::BYTES);
 
-    float *sG = reinterpret_cast<float *>(smem + SM::G);
+    float *sSum = reinterpret_cast<float *>(smem + SM::SUMS);
     float *sL = reinterpret_cast<float *>(smem + SM::TAB);
-    float *sZ = sL + 4 * D;
-    float *sLs = sZ + 4 * D;
-    uint16_t *sFb = reinterpret_cast<uint16_t *>(sLs + 4 * D);  // F_IJ as bf16 [6][D]
+    uint16_t *sFb = reinterpret_cast<uint16_t *>(sL + 4 * D);  // F_IJ as bf16 [6][D]
     float *sBeta = reinterpret_cast<float *>(smem + SM::BETA);
-    float *sTot = reinterpret_cast<float *>(smem + SM::TOT);
 
-    // ---- 1. issue every load of the chunk: q/k/v rows (per warp), g columns (per thread) ----
+    // ---- 1. issue every load of the chunk ----
     const IO *qg = static_cast<const IO *>(p.q);
     const IO *kg = static_cast<const IO *>(p.k);
     const IO *vg = static_cast<const IO *>(p.v);
+    const int r0 = ROWS * warp;  // this warp's rows r0 .. r0 + ROWS - 1, all in block I
+    const int I = warp >> 1;
     const int cb = lane * CPL;
     constexpr bool kStage = sizeof(IO) == 2;  // bf16 rows are staged into their swizzled tiles
     Slice<IO, CPL> rq[kStage ? 1 : PRE], rk[kStage ? 1 : PRE], rv[kStage ? 1 : PRE];
     auto load_rows = [&](int j0) {
 #pragma unroll
         for (int j = 0; j < PRE; ++j) {
-            const int i = warp + kWarps * (j0 + j);
+            const int i = r0 + j0 + j;
             if (i < len) {
                 const int64_t off = ((t0 + i) * H + h) * D + cb;
                 rq[j].load(qg + off);
@@ -199,13 +213,6 @@ chunk_prep_kernel(PrepParams p)
             }
         }
     };
-    // g rows -> shared memory asynchronously (rows past the sequence end read as zeros)
-#pragma unroll
-    for (int e = tid; e < C * (D / 4); e += kThreads) {
-        const int i = e / (D / 4), c4 = e % (D / 4);
-        const int ii = i < len ? i : 0;
-        cp_async16(smem_u32(sG + i * D + 4 * c4), p.g + ((t0 + ii) * H + h) * D + 4 * c4, i < len ? 16u : 0u);
-    }
     if constexpr (kStage) {  // q -> QP, k -> KP, v -> VS tiles, 16-byte chunks, zeros past the end
         constexpr int CH = D / 8;    // 16-byte chunks per row
 #pragma unroll
@@ -222,51 +229,91 @@ chunk_prep_kernel(PrepParams p)
     } else {
         load_rows(0);
     }
+    float gr[ROWS][CPL];  // g of the warp's rows, then G (log2 units)
+#pragma unroll
+    for (int j = 0; j < ROWS; ++j) {
+        if (r0 + j < len) {
+            ldg_f32<CPL>(p.g + ((t0 + r0 + j) * H + h) * D + cb, gr[j]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) gr[j][c] = 0.f;
+        }
+    }
     if (tid < C) sBeta[tid] = tid < len ? p.beta[(t0 + tid) * H + h] : 0.f;
+
+    // in-chunk cumulative sum of g per channel, in log2 units: inside the warp's
+    // rows in registers, then across warps through their totals
+#pragma unroll
+    for (int j = 0; j < ROWS; ++j)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) gr[j][c] = j == 0 ? gr[0][c] * kLog2e : fmaf(gr[j][c], kLog2e, gr[j - 1][c]);
+    st_f32<CPL>(sSum + warp * D + cb, gr[ROWS - 1]);
+    if (warp & 1) st_f32<CPL>(sSum + (kWarps + I) * D + cb, gr[0]);  // row 16 I + 8: the block midpoint
     cp_async_wait_all();
     __syncthreads();
-    // in-chunk cumulative sum of g per channel, in log2 units: registers, then segment offsets
-    const int gc = tid % D, gs = tid / D;
-    float gr[RPS];
-    gr[0] = sG[(gs * RPS) * D + gc] * kLog2e;
-#pragma unroll
-    for (int r = 1; r < RPS; ++r) gr[r] = fmaf(sG[(gs * RPS + r) * D + gc], kLog2e, gr[r - 1]);
-    sTot[gs * D + gc] = gr[RPS - 1];
-    __syncthreads();
+    float gm[4][CPL], glast[CPL], off[CPL];
     {
-        float off = 0.f;
-        for (int s2 = 0; s2 < gs; ++s2) off += sTot[s2 * D + gc];
+        float run[CPL];
 #pragma unroll
-        for (int r = 0; r < RPS; ++r) sG[(gs * RPS + r) * D + gc] = gr[r] + off;
-    }
-    __syncthreads();
-    // per-channel factors at the block midpoints m_I = 16 I + 8 (G is in log2 units)
-    if (tid < D) {
-        const int c = tid;
-        const float gl = sG[(C - 1) * D + c];
-        float gm[4];
+        for (int c = 0; c < CPL; ++c) run[c] = off[c] = 0.f;
 #pragma unroll
-        for (int I = 0; I < 4; ++I) gm[I] = sG[(16 * I + 8) * D + c];
+        for (int w = 0; w < kWarps; ++w) {
+            float t[CPL];
+            load_f32<CPL>(sSum + w * D + cb, t);
+            if (w == warp) {
 #pragma unroll
-        for (int I = 0; I < 4; ++I) {
-            const float l = exp2f(gm[I]);
-            sL[I * D + c] = l;                  // e^{G_mI}          <= 1
-            sLs[I * D + c] = l * p.scale;       // scale e^{G_mI}
-            sZ[I * D + c] = exp2f(gl - gm[I]);  // e^{G_last - G_mI} <= 1
+                for (int c = 0; c < CPL; ++c) off[c] = run[c];
+            }
+            if (w & 1) {
+                float f[CPL];
+                load_f32<CPL>(sSum + (kWarps + (w >> 1)) * D + cb, f);
 #pragma unroll
-            for (int J = 0; J < I; ++J) sFb[fslot(I, J) * D + c] = f32_to_bf16_bits(exp2f(gm[I] - gm[J]));
+                for (int c = 0; c < CPL; ++c) gm[w >> 1][c] = run[c] + f[c];
+            }
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) run[c] += t[c];
         }
-        reinterpret_cast<float *>(rec + R::GAMMA)[c] = exp2f(gl);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) glast[c] = run[c];
     }
-    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < ROWS; ++j)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) gr[j][c] += off[c];
+
+    // per-channel factors: F_IJ (warps 0-5, one (I, J) each), L_I = e^{G_mI}
+    // (even warps), gamma = e^{G_last} (warp 7, to the record)
+    float gmi[CPL], lI[CPL], ls[CPL], zz[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        gmi[c] = pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], I);
+        lI[c] = exp2f(gmi[c]);             // e^{G_mI}           <= 1
+        ls[c] = lI[c] * p.scale;
+        zz[c] = exp2f(glast[c] - gmi[c]);  // e^{G_last - G_mI}  <= 1
+    }
+    if (!(warp & 1)) st_f32<CPL>(sL + I * D + cb, lI);
+    if (warp < 6) {
+        const int fI = warp < 1 ? 1 : warp < 3 ? 2 : 3, fJ = warp - fI * (fI - 1) / 2;
+        float f[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            f[c] = exp2f(pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], fI) -
+                         pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], fJ));
+        store_bf16<CPL>(reinterpret_cast<char *>(sFb + warp * D), static_cast<uint32_t>(cb * 2), f);
+    } else if (warp == 7) {
+        float gam[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) gam[c] = exp2f(glast[c]);
+        st_f32<CPL>(reinterpret_cast<float *>(rec + R::GAMMA) + cb, gam);
+    }
 
     // ---- 2. row pass: normalise q, k; operand tiles in shared memory; Q~, K~ to the record ----
-#pragma unroll 1
+#pragma unroll
     for (int j0 = 0; j0 < ROWS; j0 += PRE) {
         if (!kStage && j0 > 0) load_rows(j0);
 #pragma unroll
         for (int j = 0; j < PRE; ++j) {
-            const int i = warp + kWarps * (j0 + j);
+            const int i = r0 + j0 + j;
             const uint32_t o = tile_off<D, C>(i, cb);
             float qv[CPL], kv[CPL], vv[CPL];
             if constexpr (kStage) {
@@ -284,23 +331,18 @@ chunk_prep_kernel(PrepParams p)
                 sk += kv[c] * kv[c];
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o2);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o2);
             }
             const float nq = p.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
             const float nk = p.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
-            const int I = i >> 4, m = 16 * I + 8;
-            float gi[CPL], gmid[CPL], ls[CPL], zz[CPL];
-            load_f32<CPL>(sG + i * D + cb, gi);
-            load_f32<CPL>(sG + m * D + cb, gmid);
-            load_f32<CPL>(sLs + I * D + cb, ls);
-            load_f32<CPL>(sZ + I * D + cb, zz);
             float kp[CPL], qp[CPL], kr[CPL], qt[CPL], kt[CPL];
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
-                const float P = ex2_approx(gi[c] - gmid[c]);   // e^{G_i - G_m}
-                const float Rr = ex2_approx(gmid[c] - gi[c]);  // e^{G_m - G_i}
+                const float gi = gr[j0 + j][c];
+                const float P = ex2_approx(gi - gmi[c]);   // e^{G_i - G_m}
+                const float Rr = ex2_approx(gmi[c] - gi);  // e^{G_m - G_i}
                 const float qh = qv[c] * nq, kh = kv[c] * nk;
                 kp[c] = kh * P;
                 qp[c] = qh * P;
@@ -308,8 +350,7 @@ chunk_prep_kernel(PrepParams p)
                 qt[c] = qp[c] * ls[c];
                 kt[c] = kr[c] * zz[c];
             }
-            __syncwarp();  // every lane has read its q, k slice before the tiles are overwritten
-            store_bf16<CPL>(smem + SM::KP, o, kp);
+            store_bf16<CPL>(smem + SM::KP, o, kp);  // each lane rewrites exactly the bytes it read
             store_bf16<CPL>(smem + SM::QP, o, qp);
             store_bf16<CPL>(smem + SM::KR, o, kr);
             if constexpr (!kStage) store_bf16<CPL>(smem + SM::VS, o, vv);
@@ -420,14 +461,17 @@ chunk_prep_kernel(PrepParams p)
     // ---- 5. W = (I + A)^-1 diag(beta) K e^G and U = (I + A)^-1 diag(beta) V, by block
     //         forward substitution: X_I = base_I - sum_{K<I} A_IK Y_K, Y_I = T_II X_I.
     //         Warps 0-3: W, warps 4-7: U; each warp owns D / NW columns and, since
-    //         every product keeps columns apart, needs no other warp's results. ----
+    //         every product keeps columns apart, needs no other warp's results.
+    //         Y_I replaces base_I in its tile (k P -> W, v -> U); U^T is staged in
+    //         the q P tile in the record's layout. ----
     {
         constexpr int NW = D / 16 < 4 ? D / 16 : 4;  // warps per matrix with work
         constexpr int COLS = D / NW, NP = COLS / 16;
         const bool is_u = warp >= 4;
         const int q4 = warp & 3;
         const int c0 = q4 * COLS;
-        char *ytile = smem + (is_u ? SM::QP : SM::KR);  // Y = U or W, [64][D] bf16
+        char *ytile = smem + (is_u ? SM::VS : SM::KP);  // base rows in, Y = U or W rows out, [64][D] bf16
+        char *utile = smem + SM::QP;                    // U^T [D][64] bf16, 128-byte swizzled rows
         char *xtile = smem + (is_u ? SM::XU : SM::XW);  // X_I, [16][D] bf16
         // Swizzled byte offset of column c0 + 8n + 2tig within any row r with r % 8 == gid.
         // (64-row tiles and the 16-row X tile differ only in their slab stride.)
@@ -461,7 +505,7 @@ chunk_prep_kernel(PrepParams p)
                     for (int hr = 0; hr < 2; ++hr) {
                         const uint32_t rx = static_cast<uint32_t>(gid + 8 * hr) * ROWB;  // row within block I
                         const uint32_t base = *reinterpret_cast<const uint32_t *>(
-                            smem + (is_u ? SM::VS : SM::KP) + static_cast<uint32_t>(16 * I) * ROWB + rx + colo[n]);
+                            ytile + static_cast<uint32_t>(16 * I) * ROWB + rx + colo[n]);
                         const float b0 = bi[hr] * bf16_lo(base) * lf.x;  // beta_i k_i e^{G_i} or beta_i v_i
                         const float b1 = bi[hr] * bf16_hi(base) * lf.y;
                         *reinterpret_cast<uint32_t *>(xtile + rx + colx[n]) =
@@ -489,9 +533,9 @@ chunk_prep_kernel(PrepParams p)
                         const int c = c0 + 8 * n + 2 * tig;
                         const float y0 = acc[n][2 * hr], y1 = acc[n][2 * hr + 1];
                         *reinterpret_cast<uint32_t *>(ytile + static_cast<uint32_t>(i) * ROWB + colo[n]) = pack_bf16x2(y0, y1);
-                        if (is_u) {  // U^T [D][64] straight into the record
-                            *reinterpret_cast<uint16_t *>(rec + R::UT + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
-                            *reinterpret_cast<uint16_t *>(rec + R::UT + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);
+                        if (is_u) {
+                            *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
+                            *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);
                         }
                     }
                 }
@@ -499,14 +543,15 @@ chunk_prep_kernel(PrepParams p)
             __syncwarp();  // Y_I columns of this warp are complete
         }
     }
+    fence_proxy_async_smem();  // the W and U^T tiles are read by the bulk copies below
     __syncthreads();
 
-    // ---- 6. W out to the record (Q~, K~, A_qk, gamma and U^T are already there) ----
-    {
-        const uint4 *sw = reinterpret_cast<const uint4 *>(smem + SM::KR);
-        uint4 *gw = reinterpret_cast<uint4 *>(rec + R::W);
-#pragma unroll
-        for (int e = tid; e < R::TILE / 16; e += kThreads) gw[e] = sw[e];
+    // ---- 6. W and U^T out to the record (Q~, K~, A_qk and gamma are already there) ----
+    if (tid == 0) {
+        bulk_s2g(rec + R::W, smem + SM::KP, R::TILE);
+        bulk_s2g(rec + R::UT, smem + SM::QP, D * C * 2);
+        bulk_commit();
+        bulk_wait_all_read();  // shared memory stays valid until the copies have read it
     }
 }
 

@@ -42,7 +42,7 @@ cudaError_t launch_decode_step(const DecodeArgs &a, cudaStream_t st);
 // per (chunk, head) holding the chunk's W, Q~, K~, A_qk, gamma and U^T.
 struct PrefillLayout {
     int64_t n_chunk_max;
-    size_t off_chunk_off, off_seq_order, off_records, rec_bytes, total;
+    size_t off_chunk_off, off_seq_order, off_chunk_info, off_records, rec_bytes, total;
 };
 bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d, PrefillLayout *out);
 

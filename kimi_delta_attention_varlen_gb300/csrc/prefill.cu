@@ -47,8 +47,8 @@ constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier polls
 // ---------------------------------------------------------- chunk table ---
 
 __global__ void __launch_bounds__(1024)
-chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int32_t *__restrict__ chunk_off,
-                   int32_t *__restrict__ seq_order, int32_t *__restrict__ status)
+chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_max, int32_t *__restrict__ chunk_off,
+                   int32_t *__restrict__ seq_order, int2 *__restrict__ chunk_info, int32_t *__restrict__ status)
 {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
@@ -90,6 +90,25 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int32_t *__restric
         __syncthreads();
     }
     if (tid == 0) chunk_off[B] = carry;
+    __syncthreads();
+    // Per chunk: its first token and length ({0, 0} past the last chunk), so a
+    // chunk's CTA finds its rows with one load.
+    const int32_t total = carry;
+    for (int64_t c = tid; c < n_chunk_max; c += 1024) {
+        int2 info = make_int2(0, 0);
+        if (c < total) {
+            int64_t lo = 0, hi = B - 1;  // the b with chunk_off[b] <= c < chunk_off[b + 1]
+            while (lo < hi) {
+                const int64_t mid = (lo + hi + 1) / 2;
+                if (chunk_off[mid] <= c) lo = mid;
+                else hi = mid - 1;
+            }
+            const int32_t t0 = cu[lo] + static_cast<int32_t>(c - chunk_off[lo]) * C;
+            const int32_t left = cu[lo + 1] - t0;
+            info = make_int2(t0, left < C ? left : C);
+        }
+        chunk_info[c] = info;
+    }
     // Longest sequences first, so their serial chunk chains start early.
     if (B <= 4096) {
         for (int64_t b = tid; b < B; b += 1024) {
@@ -334,6 +353,7 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     int32_t *chunk_off = reinterpret_cast<int32_t *>(ws + L.off_chunk_off);
     int32_t *seq_order = reinterpret_cast<int32_t *>(ws + L.off_seq_order);
+    int2 *chunk_info = reinterpret_cast<int2 *>(ws + L.off_chunk_info);
     char *records = ws + L.off_records;
 
     auto mark = [&](int i) -> cudaError_t {
@@ -341,14 +361,14 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     };
     cudaError_t e = mark(0);
     if (e != cudaSuccess) return e;
-    chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.num_seqs, chunk_off, seq_order, status);
+    chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.num_seqs, L.n_chunk_max, chunk_off, seq_order, chunk_info,
+                                           status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if ((e = mark(1)) != cudaSuccess) return e;
 
     if (L.n_chunk_max > 0) {
-        const prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, a.cu_seqlens, chunk_off, a.num_seqs,
-                                     a.h, a.scale, a.l2norm, records};
+        const prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, chunk_info, a.h, a.scale, a.l2norm, records};
         e = prefill::launch_chunk_prep(D, a.io_dtype, pp, L.n_chunk_max, a.h, st);
         if (e != cudaSuccess) return e;
     }
@@ -396,7 +416,8 @@ bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d
     L.rec_bytes = static_cast<size_t>(rb);
     L.off_chunk_off = 256;
     L.off_seq_order = up(L.off_chunk_off + 4 * static_cast<size_t>(num_seqs + 1), 256);
-    L.off_records = up(L.off_seq_order + 4 * static_cast<size_t>(num_seqs), 1024);
+    L.off_chunk_info = up(L.off_seq_order + 4 * static_cast<size_t>(num_seqs), 256);
+    L.off_records = up(L.off_chunk_info + 8 * static_cast<size_t>(L.n_chunk_max), 1024);
     L.total = L.off_records + static_cast<size_t>(L.n_chunk_max) * static_cast<size_t>(h) * L.rec_bytes;
     *out = L;
     return true;

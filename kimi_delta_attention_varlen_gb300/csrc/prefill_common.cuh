@@ -51,9 +51,7 @@ inline int rec_bytes_for(int d)
 struct PrepParams {
     const void *q, *k, *v;
     const float *g, *beta;
-    const int32_t *cu;
-    const int32_t *chunk_off;
-    int64_t B;
+    const int2 *chunk_info;  // per chunk {first token, length}; length 0 past the last chunk
     int32_t H;
     float scale;
     int32_t l2norm;
