@@ -418,34 +418,42 @@ chunk_prep_kernel(PrepParams p)
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) step(2, ks);
         }
-#pragma unroll
-        for (int u = 0; u < MAXP; ++u) {
-            if (u >= npairs) continue;
+        // Epilogue of pair u (one branch per pair on its kind, none per element).
+        auto epilogue = [&](int u) {
             const int I = pI[u], J = pJ[u];
+            if (!pqk[u]) {  // beta_i A_kk, strictly lower -> bf16 tile (+ fp32 copy of a diagonal block)
+                float *d = I == J ? sAd + I * 16 * 17 : nullptr;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int i = 16 * I + gid + 8 * hr;
-                    const int j = 16 * J + 8 * nt + 2 * tig;
-                    const float x0 = acc[u][nt][2 * hr], x1 = acc[u][nt][2 * hr + 1];
-                    if (!pqk[u]) {
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int i = 16 * I + gid + 8 * hr, j = 16 * J + 8 * nt + 2 * tig;
                         const float bi = sBeta[i];
-                        const float y0 = j < i ? x0 * bi : 0.f, y1 = j + 1 < i ? x1 * bi : 0.f;
+                        const float y0 = j < i ? acc[u][nt][2 * hr] * bi : 0.f;
+                        const float y1 = j + 1 < i ? acc[u][nt][2 * hr + 1] * bi : 0.f;
                         *reinterpret_cast<uint32_t *>(smem + SM::AB + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
-                        if (I == J) {
-                            float *d = sAd + I * 16 * 17 + (i - 16 * I) * 17 + (j - 16 * J);
-                            d[0] = y0;
-                            d[1] = y1;
+                        if (d) {  // rows of 17 floats: scalar stores (odd rows are not 8-byte aligned)
+                            d[(i - 16 * I) * 17 + (j - 16 * J)] = y0;
+                            d[(i - 16 * I) * 17 + (j - 16 * J) + 1] = y1;
                         }
-                    } else {
-                        const float y0 = j <= i ? x0 * p.scale : 0.f;
-                        const float y1 = j + 1 <= i ? x1 * p.scale : 0.f;
+                    }
+                }
+            } else {  // scale A_qk, causal -> the record
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int i = 16 * I + gid + 8 * hr, j = 16 * J + 8 * nt + 2 * tig;
+                        const float y0 = j <= i ? acc[u][nt][2 * hr] * p.scale : 0.f;
+                        const float y1 = j + 1 <= i ? acc[u][nt][2 * hr + 1] * p.scale : 0.f;
                         *reinterpret_cast<uint32_t *>(rec + R::AQK + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
                     }
                 }
             }
-        }
+        };
+        epilogue(0);
+        epilogue(1);
+        if (npairs > 2) epilogue(2);
     }
     __syncthreads();
 
@@ -476,12 +484,8 @@ chunk_prep_kernel(PrepParams p)
     {
         constexpr int NW = D / 16 < 4 ? D / 16 : 4;  // warps per matrix with work
         constexpr int COLS = D / NW, NP = COLS / 16;
-        const bool is_u = warp >= 4;
         const int q4 = warp & 3;
         const int c0 = q4 * COLS;
-        char *ytile = smem + (is_u ? SM::VS : SM::KP);  // base rows in, Y = U or W rows out, [64][D] bf16
-        char *utile = smem + SM::QP;                    // U^T [D][64] bf16, 128-byte swizzled rows
-        char *xtile = smem + (is_u ? SM::XU : SM::XW);  // X_I, [16][D] bf16
         // Swizzled byte offset of column c0 + 8n + 2tig within any row r with r % 8 == gid.
         // (64-row tiles and the 16-row X tile differ only in their slab stride.)
         uint32_t colo[2 * NP], colx[2 * NP];
@@ -490,67 +494,84 @@ chunk_prep_kernel(PrepParams p)
             colo[n] = tile_off<D, C>(gid, c0 + 8 * n + 2 * tig) - gid * ROWB;
             colx[n] = tile_off<D, 16>(gid, c0 + 8 * n + 2 * tig) - gid * ROWB;
         }
+        // The whole substitution of one matrix, specialised at compile time (no
+        // per-element branches on the matrix kind).
+        auto substitute = [&](auto is_u_tag) {
+            constexpr bool kU = decltype(is_u_tag)::value;
+            char *ytile = smem + (kU ? SM::VS : SM::KP);  // base rows in, Y = U or W rows out, [64][D] bf16
+            char *xtile = smem + (kU ? SM::XU : SM::XW);  // X_I, [16][D] bf16
+            char *utile = smem + SM::QP;                  // U^T [D][64] bf16, 128-byte swizzled rows
 #pragma unroll
-        for (int I = 0; I < 4; ++I) {
-            if (q4 < NW) {
-                float acc[2 * NP][4] = {};
-                for (int K = 0; K < I; ++K) {
-                    uint32_t a[4];
-                    ldmatrix_x4(a, smem_u32(smem + SM::AB + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * K + 8 * (mi >> 1))));
+            for (int I = 0; I < 4; ++I) {
+                {
+                    float acc[2 * NP][4] = {};
 #pragma unroll
-                    for (int np = 0; np < NP; ++np) {
-                        uint32_t b[4];
-                        ldmatrix_x4_trans(b, smem_u32(ytile + tile_off<D, C>(16 * K + ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
-                        mma_bf16(acc[2 * np], a, b[0], b[1]);
-                        mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+                    for (int K = 0; K < I; ++K) {
+                        uint32_t a[4];
+                        ldmatrix_x4(a, smem_u32(smem + SM::AB + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * K + 8 * (mi >> 1))));
+#pragma unroll
+                        for (int np = 0; np < NP; ++np) {
+                            uint32_t b[4];
+                            ldmatrix_x4_trans(b, smem_u32(ytile + tile_off<D, C>(16 * K + ri + 8 * (mi & 1),
+                                                                                 c0 + 16 * np + 8 * (mi >> 1))));
+                            mma_bf16(acc[2 * np], a, b[0], b[1]);
+                            mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+                        }
                     }
-                }
-                const float bi[2] = {sBeta[16 * I + gid], sBeta[16 * I + gid + 8]};
+                    const float bi[2] = {sBeta[16 * I + gid], sBeta[16 * I + gid + 8]};
 #pragma unroll
-                for (int n = 0; n < 2 * NP; ++n) {
-                    const int c = c0 + 8 * n + 2 * tig;
-                    float2 lf = make_float2(1.f, 1.f);
-                    if (!is_u) lf = *reinterpret_cast<const float2 *>(sL + I * D + c);
+                    for (int n = 0; n < 2 * NP; ++n) {
+                        float2 lf = make_float2(1.f, 1.f);
+                        if constexpr (!kU) lf = *reinterpret_cast<const float2 *>(sL + I * D + c0 + 8 * n + 2 * tig);
 #pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const uint32_t rx = static_cast<uint32_t>(gid + 8 * hr) * ROWB;  // row within block I
-                        const uint32_t base = *reinterpret_cast<const uint32_t *>(
-                            ytile + static_cast<uint32_t>(16 * I) * ROWB + rx + colo[n]);
-                        const float b0 = bi[hr] * bf16_lo(base) * lf.x;  // beta_i k_i e^{G_i} or beta_i v_i
-                        const float b1 = bi[hr] * bf16_hi(base) * lf.y;
-                        *reinterpret_cast<uint32_t *>(xtile + rx + colx[n]) =
-                            pack_bf16x2(b0 - acc[n][2 * hr], b1 - acc[n][2 * hr + 1]);
-                    }
-                }
-            }
-            __syncwarp();  // X_I columns of this warp are complete (no other warp reads them)
-            if (q4 < NW) {
-                float acc[2 * NP][4] = {};
-                uint32_t a[4];
-                ldmatrix_x4(a, smem_u32(smem + SM::TD + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * I + 8 * (mi >> 1))));
-#pragma unroll
-                for (int np = 0; np < NP; ++np) {
-                    uint32_t b[4];
-                    ldmatrix_x4_trans(b, smem_u32(xtile + tile_off<D, 16>(ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
-                    mma_bf16(acc[2 * np], a, b[0], b[1]);
-                    mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
-                }
-#pragma unroll
-                for (int n = 0; n < 2 * NP; ++n) {
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int i = 16 * I + gid + 8 * hr;
-                        const int c = c0 + 8 * n + 2 * tig;
-                        const float y0 = acc[n][2 * hr], y1 = acc[n][2 * hr + 1];
-                        *reinterpret_cast<uint32_t *>(ytile + static_cast<uint32_t>(i) * ROWB + colo[n]) = pack_bf16x2(y0, y1);
-                        if (is_u) {
-                            *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
-                            *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const uint32_t rx = static_cast<uint32_t>(gid + 8 * hr) * ROWB;  // row within block I
+                            const uint32_t base = *reinterpret_cast<const uint32_t *>(
+                                ytile + static_cast<uint32_t>(16 * I) * ROWB + rx + colo[n]);
+                            float b0 = bi[hr] * bf16_lo(base), b1 = bi[hr] * bf16_hi(base);  // beta_i v_i or
+                            if constexpr (!kU) {                                                // beta_i k_i e^{G_i}
+                                b0 *= lf.x;
+                                b1 *= lf.y;
+                            }
+                            *reinterpret_cast<uint32_t *>(xtile + rx + colx[n]) =
+                                pack_bf16x2(b0 - acc[n][2 * hr], b1 - acc[n][2 * hr + 1]);
                         }
                     }
                 }
+                __syncwarp();  // X_I columns of this warp are complete (no other warp reads them)
+                {
+                    float acc[2 * NP][4] = {};
+                    uint32_t a[4];
+                    ldmatrix_x4(a, smem_u32(smem + SM::TD + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * I + 8 * (mi >> 1))));
+#pragma unroll
+                    for (int np = 0; np < NP; ++np) {
+                        uint32_t b[4];
+                        ldmatrix_x4_trans(b, smem_u32(xtile + tile_off<D, 16>(ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
+                        mma_bf16(acc[2 * np], a, b[0], b[1]);
+                        mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+                    }
+#pragma unroll
+                    for (int n = 0; n < 2 * NP; ++n) {
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int i = 16 * I + gid + 8 * hr;
+                            const float y0 = acc[n][2 * hr], y1 = acc[n][2 * hr + 1];
+                            *reinterpret_cast<uint32_t *>(ytile + static_cast<uint32_t>(i) * ROWB + colo[n]) =
+                                pack_bf16x2(y0, y1);
+                            if constexpr (kU) {
+                                const int c = c0 + 8 * n + 2 * tig;
+                                *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
+                                *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();  // Y_I columns of this warp are complete
             }
-            __syncwarp();  // Y_I columns of this warp are complete
+        };
+        if (q4 < NW) {
+            if (warp >= 4) substitute(std::true_type{});
+            else substitute(std::false_type{});
         }
     }
     fence_proxy_async_smem();  // the W and U^T tiles are read by the bulk copies below
