@@ -70,6 +70,9 @@ def _load():
                                            ctypes.c_double, ctypes.c_int, ctypes.c_double, _D, _D,
                                            ctypes.c_int]
             lib.oracle_prefill.restype = ctypes.c_int
+            lib.oracle_prefill_ckpt.argtypes = lib.oracle_prefill.argtypes[:16] + [ctypes.c_int64, _D,
+                                                                                 ctypes.c_int]
+            lib.oracle_prefill_ckpt.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [_D, _D, _D, _D, _D, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
                                           ctypes.c_int, ctypes.c_double, _VP, ctypes.c_int,
@@ -176,6 +179,35 @@ def prefill(q, k, v, g, beta, cu_seqlens, init=None, scale=1.0, l2norm=True, eps
     if rc != 0:
         raise ValueError(f"oracle_prefill failed ({rc})")
     return out, final
+
+
+def prefill_ckpt(q, k, v, g, beta, cu_seqlens, every, init=None, scale=1.0, l2norm=True, eps=EPS,
+                 nthreads=None):
+    """prefill plus checkpoints: returns (out, final, ckpt [slots, H, V, K]) where slot
+    first_b + m - 1 holds the state of sequence b after its first m * every tokens
+    (m = 1 .. len_b // every) and first_b = sum of len_b' // every over b' < b."""
+    q, k, v, g, beta = (_f64(a) for a in (q, k, v, g, beta))
+    cu = _i64(cu_seqlens).reshape(-1)
+    T, H, K = q.shape
+    V = v.shape[2]
+    B = cu.size - 1
+    assert cu[0] == 0 and cu[-1] == T and every > 0
+    ini = None
+    if init is not None:
+        ini = _f64(init)
+        assert ini.shape == (B, H, V, K)
+    slots = int(sum((cu[b + 1] - cu[b]) // every for b in range(B)))
+    out = np.zeros((T, H, V), dtype=np.float64)
+    final = np.zeros((B, H, V, K), dtype=np.float64)
+    ckpt = np.zeros((max(slots, 1), H, V, K), dtype=np.float64)
+    rc = _load().oracle_prefill_ckpt(_ptr(q, _D), _ptr(k, _D), _ptr(v, _D), _ptr(g, _D),
+                                     _ptr(beta, _D), _ptr(cu, _I64), B, H, K, V,
+                                     None if ini is None else _ptr(ini, _D), float(scale),
+                                     1 if l2norm else 0, float(eps), _ptr(out, _D), _ptr(final, _D),
+                                     int(every), _ptr(ckpt, _D), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_prefill_ckpt failed ({rc})")
+    return out, final, ckpt[:slots]
 
 
 def decode(q, k, v, g, beta, cache_flat: np.ndarray, n_rows: int, row_stride: int, idx,

@@ -27,6 +27,8 @@
  *                   varlen batch.  q and k are L2-normalised per (token,
  *                   head) first, as the "Support Kimi-K3 on NPU" report's
  *                   extend listing does before its chunk math.
+ *   oracle_prefill_ckpt  oracle_prefill plus the state after every `every`
+ *                   tokens of each sequence (chunk-boundary checkpoints).
  *   oracle_decode   one token of the same recurrence per request, reading
  *                   the state from a cache row by index and writing it back
  *                   in the cache dtype (the decode route named on the state
@@ -208,6 +210,9 @@ typedef struct {
     int64_t B, H, K, V;
     double scale, eps;
     int l2norm;
+    int64_t every;            /* checkpoint interval in tokens, 0: none */
+    double *ckpt;             /* [slots, H, V, K] or NULL */
+    const int64_t *ckpt_first;/* [B] first checkpoint slot of each sequence */
     int64_t n_items;
     int64_t next; /* work counter, atomically advanced */
 } orc_prefill_job;
@@ -224,6 +229,13 @@ static void orc_prefill_item(orc_prefill_job *a, int64_t item, double *S, double
         orc_token_step(S, K, V, a->q + (t * H + h) * K, a->k + (t * H + h) * K,
                        a->v + (t * H + h) * V, a->g + (t * H + h) * K, a->beta[t * H + h],
                        a->scale, a->l2norm, a->eps, a->out + (t * H + h) * V, qn, kn, p);
+        const int64_t done = t - a->cu_seqlens[b] + 1; /* tokens of sequence b processed */
+        if (a->ckpt && done % a->every == 0) {
+            const int64_t slot = a->ckpt_first[b] + done / a->every - 1;
+            for (int64_t j = 0; j < V; ++j)
+                for (int64_t c = 0; c < K; ++c)
+                    a->ckpt[((slot * H + h) * V + j) * K + c] = S[c * V + j];
+        }
     }
     for (int64_t j = 0; j < V; ++j)
         for (int64_t c = 0; c < K; ++c)
@@ -276,8 +288,38 @@ int oracle_prefill(const double *q, const double *k, const double *v, const doub
     for (int64_t b = 0; b < B; ++b)
         if (cu_seqlens[b + 1] < cu_seqlens[b]) return -1;
     orc_prefill_job a = {q, k, v, g, beta, cu_seqlens, init, out, final_state,
-                         B, H, K, V, scale, eps, l2norm, B * H, 0};
+                         B, H, K, V, scale, eps, l2norm, 0, NULL, NULL, B * H, 0};
     return orc_run_threads(orc_prefill_worker, &a, nthreads);
+}
+
+/* oracle_prefill that also records checkpoints: the state after the first
+ * m * every tokens of sequence b, m = 1 .. len_b / every, goes to slot
+ * first_b + m - 1 of ckpt [slots, H, V, K], first_b = sum over b' < b of
+ * len_b' / every (sequence-major).  The chunk-boundary states that the
+ * "Support Kimi-K3 on NPU" report's extend listing returns for state
+ * tracking, and the recurrent checkpoints written during prefill on the
+ * infra page (section 8.2.4), at a fixed token interval. */
+int oracle_prefill_ckpt(const double *q, const double *k, const double *v, const double *g,
+                        const double *beta, const int64_t *cu_seqlens, int64_t B, int64_t H,
+                        int64_t K, int64_t V, const double *init, double scale, int l2norm,
+                        double eps, double *out, double *final_state, int64_t every, double *ckpt,
+                        int nthreads)
+{
+    if (B < 0 || H <= 0 || K <= 0 || V <= 0 || every <= 0 || ckpt == NULL) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        if (cu_seqlens[b + 1] < cu_seqlens[b]) return -1;
+    int64_t *first = (int64_t *)malloc(sizeof(int64_t) * (size_t)(B > 0 ? B : 1));
+    if (!first) return -2;
+    int64_t n = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        first[b] = n;
+        n += (cu_seqlens[b + 1] - cu_seqlens[b]) / every;
+    }
+    orc_prefill_job a = {q, k, v, g, beta, cu_seqlens, init, out, final_state,
+                         B, H, K, V, scale, eps, l2norm, every, ckpt, first, B * H, 0};
+    const int rc = orc_run_threads(orc_prefill_worker, &a, nthreads);
+    free(first);
+    return rc;
 }
 
 typedef struct {

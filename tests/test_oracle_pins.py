@@ -486,3 +486,36 @@ def test_l2norm_ignores_positive_scaling_of_q_and_k():
     o2, f2 = oracle.prefill(q * 3.0, k * 0.5, v, g, beta, cu)
     np.testing.assert_allclose(o2, o1, rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(f2, f1, rtol=1e-5, atol=1e-6)
+
+
+# --------------------------------------------------------------------------
+# Chunk-boundary checkpoints
+# --------------------------------------------------------------------------
+
+def test_checkpoints_are_prefix_final_states():
+    """Slot first_b + m - 1 holds sequence b's state after its first m * every tokens,
+    i.e. the final state of a run over just those tokens from the same initial state;
+    recording checkpoints changes neither the outputs nor the final states."""
+    lengths, every = [130, 0, 64, 63, 200], 64
+    q, k, v, g, beta, cu = rand_tokens(40, lengths, 2, 6, 5)
+    init = np.random.default_rng(41).standard_normal((5, 2, 5, 6))
+    out, final, ck = oracle.prefill_ckpt(q, k, v, g, beta, cu, every, init=init, scale=0.7)
+    assert ck.shape == (sum(n // every for n in lengths), 2, 5, 6)
+    slot = 0
+    for b, n in enumerate(lengths):
+        for m in range(1, n // every + 1):
+            t0, t1 = cu[b], cu[b] + m * every
+            _, f = oracle.prefill(q[t0:t1], k[t0:t1], v[t0:t1], g[t0:t1], beta[t0:t1], [0, t1 - t0],
+                                  init=init[b:b + 1], scale=0.7)
+            np.testing.assert_array_equal(ck[slot], f[0])
+            slot += 1
+    o2, f2 = oracle.prefill(q, k, v, g, beta, cu, init=init, scale=0.7)
+    np.testing.assert_array_equal(out, o2)
+    np.testing.assert_array_equal(final, f2)
+    np.testing.assert_array_equal(ck[2], final[2])  # length 64 = every: its only checkpoint is its final state
+
+
+def test_checkpoint_interval_longer_than_every_sequence_records_nothing():
+    q, k, v, g, beta, cu = rand_tokens(42, [10, 127], 1, 4, 4)
+    _, _, ck = oracle.prefill_ckpt(q, k, v, g, beta, cu, 128)
+    assert ck.shape[0] == 0
