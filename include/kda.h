@@ -198,6 +198,69 @@ int kda_prefill_varlen_timed(const void *q, const void *k, const void *v, int32_
                              size_t ws_bytes, void *stream, void *const *events);
 
 /* ------------------------------------------------------------------------
+ * kda_prefill_varlen_cached
+ *
+ * kda_prefill_varlen with its initial and final states in the state cache,
+ * the fused form named in the "Support Kimi-K3 on NPU" report's extend
+ * listing (the state pass takes the cache and the per-sequence cache indices
+ * directly, step 3), plus optional chunk-boundary checkpoints - the states
+ * the same listing returns on request for state tracking and the recurrent
+ * checkpoints the infra page's vLLM section (8.2.4) writes during prefill.
+ * Equivalent to, and bit-identical with, the unfused composition
+ *   kda_state_gather(cache, idx_in, flags) -> kda_prefill_varlen ->
+ *   kda_state_scatter(cache, idx_out)
+ * without the two packed round trips:
+ *   initial state of b = cache row idx_in[b] (upcast to fp32) when
+ *       0 <= idx_in[b] < n_rows and (flags == NULL or flags[b] != 0),
+ *       else zeros (the gather rule);
+ *   final state of b   -> cache row idx_out[b], cast to the cache dtype
+ *       (fp32 -> bf16 rounds to nearest even), when idx_out != NULL and
+ *       0 <= idx_out[b] < n_rows (the scatter rule); other rows untouched;
+ *       and -> final_state[b] (fp32, packed) when final_state != NULL.
+ *   checkpoints: when checkpoints != NULL, the state after the first
+ *       m * ckpt_every tokens of sequence b, for m = 1 .. len_b / ckpt_every
+ *       (the final state too when len_b is a multiple), goes to slot
+ *       first_b + m - 1, first_b = sum over b' < b of len_b' / ckpt_every,
+ *       cast to ckpt_dtype.  ckpt_every is a multiple of 64 (checkpoints sit
+ *       on chunk boundaries).  Slots >= ckpt_slots are not written;
+ *       kda_prefill_checkpoint_count gives the number needed.
+ *
+ *   cache       [n_rows, h, dv, dk] rows with row_stride, cache->h == h,
+ *               ->v == dv, ->k == dk; data and row stride 16-byte aligned.
+ *   idx_in      [num_seqs] device, idx_type; required.
+ *   flags       [num_seqs] device uint8, or NULL (all set).
+ *   idx_out     [num_seqs] device, idx_type, or NULL (no write-back).
+ *   final_state [num_seqs, h, dv, dk] device fp32, or NULL.
+ *   checkpoints [ckpt_slots, h, dv, dk] device, ckpt_dtype, or NULL.
+ *   Other arguments as kda_prefill_varlen (same workspace size).
+ *   Preconditions (not checked, no host sync): valid idx_out rows are
+ *   unique; no row is read as an initial state by one sequence and written
+ *   by another (idx_in[b] == idx_out[b], an in-place update, is fine).
+ *   Errors as kda_prefill_varlen, plus check_cache's layout errors,
+ *   KDA_ERR_SHAPE when the cache does not match h, dk, dv or ckpt_every is
+ *   not a positive multiple of 64, KDA_ERR_ALIGN for misaligned rows.
+ * ---------------------------------------------------------------------- */
+int kda_prefill_varlen_cached(const void *q, const void *k, const void *v, int32_t io_dtype,
+                              const float *g, const float *beta, const int32_t *cu_seqlens,
+                              int64_t num_seqs, int64_t total_tokens, int32_t h, int32_t dk,
+                              int32_t dv, float scale, int32_t qk_l2norm, const kda_cache *cache,
+                              const void *idx_in, const uint8_t *flags, const void *idx_out,
+                              int32_t idx_type, float *final_state, void *checkpoints,
+                              int32_t ckpt_dtype, int32_t ckpt_every, int64_t ckpt_slots, void *out,
+                              void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * kda_prefill_checkpoint_count
+ *
+ * Host helper: checkpoint slots kda_prefill_varlen_cached writes for the
+ * sequences of a HOST copy of cu_seqlens, sum over b of len_b / ckpt_every.
+ * Returns -1 for a NULL pointer, num_seqs < 1, a decreasing cu_seqlens or a
+ * ckpt_every that is not a positive multiple of 64.
+ * ---------------------------------------------------------------------- */
+int64_t kda_prefill_checkpoint_count(const int32_t *cu_seqlens_host, int64_t num_seqs,
+                                     int32_t ckpt_every);
+
+/* ------------------------------------------------------------------------
  * kda_prefill_varlen_noalloc
  *
  * The reference pages have no counterpart to this entry point; it exists for

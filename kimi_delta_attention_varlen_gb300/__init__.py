@@ -25,7 +25,7 @@ from ._abi import (EXPORTED, KDA_BF16, KDA_F32, KDA_I32, KDA_I64, LIB_PATH, KdaC
 
 __all__ = [
     "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
-    "kda_decode_step", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
+    "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc", "kda_decode_step", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
     "KdaError", "EXPORTED", "LIB_PATH",
 ]
 
@@ -155,6 +155,64 @@ def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, out, workspace, *, scale: f
         handles.append(ev.cuda_event)
     arr = (ctypes.c_void_p * 4)(*handles)
     _check(lib().kda_prefill_varlen_timed(*args, arr), "kda_prefill_varlen_timed")
+
+
+def kda_prefill_checkpoint_count(cu_seqlens, ckpt_every: int) -> int:
+    """Checkpoint slots kda_prefill_varlen_cached writes: sum of len_b // ckpt_every over
+    the sequences of cu_seqlens (a host int32 tensor or a list of offsets)."""
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu().contiguous()
+    n = lib().kda_prefill_checkpoint_count(ctypes.cast(cu.data_ptr(), ctypes.POINTER(ctypes.c_int32)),
+                                           cu.numel() - 1, int(ckpt_every))
+    _need(n >= 0, "cu_seqlens must be non-decreasing and ckpt_every a positive multiple of 64")
+    return int(n)
+
+
+def kda_prefill_varlen_cached(q, k, v, g, beta, cu_seqlens, out, workspace, cache, idx_in, *,
+                              flags=None, idx_out=None, final_state=None, checkpoints=None,
+                              ckpt_every: int = 0, scale: float | None = None, qk_l2norm: bool = True,
+                              stream=None) -> None:
+    """kda_prefill_varlen with initial states read from cache rows idx_in (with flags, the
+    gather rule) and final states written to cache rows idx_out (the scatter rule, cast
+    to the cache dtype), in one pass; optional checkpoints [slots, H, V, K] (fp32 or bf16)
+    hold the state after every ckpt_every tokens of each sequence (sequence-major; see
+    kda_prefill_checkpoint_count)."""
+    T, H, K = q.shape
+    V = v.shape[2]
+    B = cu_seqlens.numel() - 1
+    for name, t, shape in (("q", q, (T, H, K)), ("k", k, (T, H, K)), ("v", v, (T, H, V)),
+                           ("out", out, (T, H, V)), ("g", g, (T, H, K)), ("beta", beta, (T, H))):
+        _need(tuple(t.shape) == shape and t.is_contiguous(), f"{name} must be contiguous {shape}")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype and out.dtype == q.dtype, "q, k, v, out share a dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g and beta must be float32")
+    _need(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous() and B >= 1,
+          "cu_seqlens must be a contiguous int32 tensor of B + 1 >= 2 offsets")
+    d = cache_descriptor(cache)
+    _index_vector(idx_in)
+    _need(idx_in.numel() == B, "idx_in must hold one index per sequence")
+    if idx_out is not None:
+        _index_vector(idx_out)
+        _need(idx_out.numel() == B and idx_out.dtype == idx_in.dtype,
+              "idx_out: one index per sequence, idx_in's dtype")
+    if flags is not None:
+        _need(flags.dtype in (torch.bool, torch.uint8) and flags.is_contiguous() and flags.numel() == B,
+              "flags must be a contiguous bool tensor of length B")
+    if final_state is not None:
+        _need(tuple(final_state.shape) == (B, H, V, K) and final_state.is_contiguous() and
+              final_state.dtype == torch.float32, "final_state must be contiguous float32 [B, H, V, K]")
+    slots, ck_code = 0, 0
+    if checkpoints is not None:
+        _need(checkpoints.dim() == 4 and tuple(checkpoints.shape[1:]) == (H, V, K) and checkpoints.is_contiguous(),
+              "checkpoints must be contiguous [slots, H, V, K]")
+        slots, ck_code = checkpoints.shape[0], _dtype_code(checkpoints)
+    _need(workspace.dtype == torch.uint8 and workspace.is_contiguous(), "workspace must be a uint8 tensor")
+    if scale is None:
+        scale = K ** -0.5
+    rc = lib().kda_prefill_varlen_cached(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g), _ptr(beta), _ptr(cu_seqlens), B, T, H, K, V,
+        float(scale), 1 if qk_l2norm else 0, ctypes.byref(d), _ptr(idx_in), _ptr(flags), _ptr(idx_out),
+        _itype_code(idx_in), _ptr(final_state), _ptr(checkpoints), ck_code, int(ckpt_every), slots, _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "kda_prefill_varlen_cached")
 
 
 def kda_decode_step(q, k, v, g, beta, cache, idx, out, *, scale: float | None = None,

@@ -29,6 +29,8 @@ EXPORTED = (
     "kda_prefill_varlen",
     "kda_prefill_varlen_timed",
     "kda_prefill_varlen_noalloc",
+    "kda_prefill_varlen_cached",
+    "kda_prefill_checkpoint_count",
     "kda_decode_step",
     "kda_status_string",
     "kda_last_cuda_error_string",
@@ -89,6 +91,11 @@ def lib():
         L.kda_prefill_varlen_timed.restype = ctypes.c_int
         L.kda_prefill_varlen_noalloc.argtypes = L.kda_prefill_varlen.argtypes[:18] + [vp]
         L.kda_prefill_varlen_noalloc.restype = ctypes.c_int
+        L.kda_prefill_varlen_cached.argtypes = [vp, vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, i32, f32, i32,
+                                                cache_p, vp, vp, vp, i32, vp, vp, i32, i32, i64, vp, vp, sz, vp]
+        L.kda_prefill_varlen_cached.restype = ctypes.c_int
+        L.kda_prefill_checkpoint_count.argtypes = [ctypes.POINTER(ctypes.c_int32), i64, i32]
+        L.kda_prefill_checkpoint_count.restype = i64
         L.kda_decode_step.argtypes = [vp, vp, vp, i32, vp, vp, i64, i32, i32, i32, f32, i32, cache_p, vp, i32,
                                       vp, vp]
         L.kda_decode_step.restype = ctypes.c_int

@@ -106,14 +106,15 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_
 }
 
 namespace {
+// Shared by every prefill entry point; `se` says where states come from and go
+// (its cache fields are validated by the caller).
 int prefill_impl(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g, const float *beta,
                  const int32_t *cu_seqlens, int64_t num_seqs, int64_t total_tokens, int32_t h, int32_t dk,
-                 int32_t dv, float scale, int32_t qk_l2norm, const void *init_state, int32_t init_dtype,
-                 float *final_state, void *out, void *workspace, size_t ws_bytes, void *stream,
-                 void *const *events)
+                 int32_t dv, float scale, int32_t qk_l2norm, const kda::StateEnds &se, void *out, void *workspace,
+                 size_t ws_bytes, void *stream, void *const *events)
 {
     if (!valid_dtype(io_dtype)) return KDA_ERR_DTYPE;
-    if (init_state != nullptr && !valid_dtype(init_dtype)) return KDA_ERR_DTYPE;
+    if (se.init != nullptr && !valid_dtype(se.init_dtype)) return KDA_ERR_DTYPE;
     if (num_seqs < 1 || total_tokens < 0 || h < 1 || dk < 1 || dv < 1) return KDA_ERR_SHAPE;
     if (!built_head_size(dk, dv)) return KDA_ERR_UNSUPPORTED;
     if (total_tokens >= (INT64_C(1) << 31) || num_seqs >= (INT64_C(1) << 30) || h > 65535)
@@ -123,7 +124,7 @@ int prefill_impl(const void *q, const void *k, const void *v, int32_t io_dtype, 
     if (total_tokens > 0 && (q == nullptr || k == nullptr || v == nullptr || g == nullptr || beta == nullptr ||
                              out == nullptr))
         return KDA_ERR_NULL;
-    const void *vec16[] = {q, k, v, g, out, init_state, final_state};
+    const void *vec16[] = {q, k, v, g, out, se.init, se.final_state, se.out_cache, se.ckpt};
     for (const void *p : vec16)
         if (p != nullptr && !aligned(p, 16)) return KDA_ERR_ALIGN;
     if (!aligned(beta, 4) || !aligned(cu_seqlens, 4)) return KDA_ERR_ALIGN;
@@ -133,8 +134,17 @@ int prefill_impl(const void *q, const void *k, const void *v, int32_t io_dtype, 
     if (!aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
     if (ws_bytes < L.total) return KDA_ERR_WORKSPACE;
     kda::PrefillArgs a{q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, scale,
-                       qk_l2norm ? 1 : 0, init_state, init_dtype, final_state, out, workspace, events};
+                       qk_l2norm ? 1 : 0, se, out, workspace, events};
     return cuda_status(kda::launch_prefill(a, L, static_cast<cudaStream_t>(stream)));
+}
+
+kda::StateEnds packed_ends(const void *init_state, int32_t init_dtype, float *final_state)
+{
+    kda::StateEnds se{};
+    se.init = init_state;
+    se.init_dtype = init_dtype;
+    se.final_state = final_state;
+    return se;
 }
 }  // namespace
 
@@ -145,8 +155,8 @@ int kda_prefill_varlen(const void *q, const void *k, const void *v, int32_t io_d
                        void *stream)
 {
     return prefill_impl(q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, dv, scale,
-                        qk_l2norm, init_state, init_dtype, final_state, out, workspace, ws_bytes, stream,
-                        nullptr);
+                        qk_l2norm, packed_ends(init_state, init_dtype, final_state), out, workspace, ws_bytes,
+                        stream, nullptr);
 }
 
 int kda_prefill_varlen_timed(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,
@@ -159,7 +169,60 @@ int kda_prefill_varlen_timed(const void *q, const void *k, const void *v, int32_
     for (int i = 0; i < 4; ++i)
         if (events[i] == nullptr) return KDA_ERR_NULL;
     return prefill_impl(q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, dv, scale,
-                        qk_l2norm, init_state, init_dtype, final_state, out, workspace, ws_bytes, stream, events);
+                        qk_l2norm, packed_ends(init_state, init_dtype, final_state), out, workspace, ws_bytes,
+                        stream, events);
+}
+
+int kda_prefill_varlen_cached(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,
+                              const float *beta, const int32_t *cu_seqlens, int64_t num_seqs, int64_t total_tokens,
+                              int32_t h, int32_t dk, int32_t dv, float scale, int32_t qk_l2norm,
+                              const kda_cache *cache, const void *idx_in, const uint8_t *flags,
+                              const void *idx_out, int32_t idx_type, float *final_state, void *checkpoints,
+                              int32_t ckpt_dtype, int32_t ckpt_every, int64_t ckpt_slots, void *out,
+                              void *workspace, size_t ws_bytes, void *stream)
+{
+    kda::CacheDesc c{};
+    int rc = check_cache(cache, &c);
+    if (rc != KDA_OK) return rc;
+    if (!valid_itype(idx_type)) return KDA_ERR_DTYPE;
+    if (c.h != h || c.k != dk || c.v != dv) return KDA_ERR_SHAPE;
+    if (!aligned(c.data, 16) || (c.row_stride * esize(c.dtype)) % 16 != 0) return KDA_ERR_ALIGN;
+    if ((rc = check_index_array(idx_in, idx_type)) != KDA_OK) return rc;
+    if (idx_out != nullptr && (rc = check_index_array(idx_out, idx_type)) != KDA_OK) return rc;
+    if (checkpoints != nullptr) {
+        if (!valid_dtype(ckpt_dtype)) return KDA_ERR_DTYPE;
+        if (ckpt_every <= 0 || ckpt_every % 64 != 0 || ckpt_slots < 0) return KDA_ERR_SHAPE;
+    }
+    kda::StateEnds se{};
+    se.init = c.data;
+    se.init_dtype = c.dtype;
+    se.in_idx = idx_in;
+    se.in_flags = flags;
+    se.idx_type = idx_type;
+    se.n_rows = c.n_rows;
+    se.row_stride = c.row_stride;
+    se.final_state = final_state;
+    se.out_cache = idx_out != nullptr ? c.data : nullptr;
+    se.out_dtype = c.dtype;
+    se.out_idx = idx_out;
+    se.ckpt = checkpoints;
+    se.ckpt_dtype = ckpt_dtype;
+    se.ckpt_every = checkpoints != nullptr ? ckpt_every : 0;
+    se.ckpt_slots = ckpt_slots;
+    return prefill_impl(q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, dv, scale,
+                        qk_l2norm, se, out, workspace, ws_bytes, stream, nullptr);
+}
+
+int64_t kda_prefill_checkpoint_count(const int32_t *cu_seqlens_host, int64_t num_seqs, int32_t ckpt_every)
+{
+    if (cu_seqlens_host == nullptr || num_seqs < 1 || ckpt_every <= 0 || ckpt_every % 64 != 0) return -1;
+    int64_t n = 0;
+    for (int64_t b = 0; b < num_seqs; ++b) {
+        const int64_t len = static_cast<int64_t>(cu_seqlens_host[b + 1]) - cu_seqlens_host[b];
+        if (len < 0) return -1;
+        n += len / ckpt_every;
+    }
+    return n;
 }
 
 int kda_decode_step(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,

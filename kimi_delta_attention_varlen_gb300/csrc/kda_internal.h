@@ -42,8 +42,31 @@ cudaError_t launch_decode_step(const DecodeArgs &a, cudaStream_t st);
 // per (chunk, head) holding the chunk's W, Q~, K~, A_qk, gamma and U^T.
 struct PrefillLayout {
     int64_t n_chunk_max;
-    size_t off_chunk_off, off_seq_order, off_chunk_info, off_records, rec_bytes, total;
+    size_t off_chunk_off, off_seq_order, off_chunk_info, off_ckpt_off, off_records, rec_bytes, total;
 };
+
+// Where each sequence's initial state comes from and where its final state and
+// checkpoints go.  A state of head h is [V][K] (the cache orientation): element
+// (v, k) of the state at base element offset o sits at o + (h * D + v) * D + k.
+struct StateEnds {
+    const void *init;         // nullable (zeros): packed [B][H][V][K], or cache rows when in_idx is set
+    int32_t init_dtype;       // KDA_F32 / KDA_BF16
+    const void *in_idx;       // nullable: initial state of sequence b = cache row in_idx[b]
+    const uint8_t *in_flags;  // nullable: flags[b] == 0 -> zeros
+    int32_t idx_type;         // KDA_I32 / KDA_I64, for in_idx and out_idx
+    int64_t n_rows;           // cache rows; an index outside [0, n_rows) means "no row"
+    int64_t row_stride;       // elements between cache rows
+    float *final_state;       // nullable: packed fp32 [B][H][V][K]
+    void *out_cache;          // nullable: final state -> cache row out_idx[b], cast to out_dtype
+    int32_t out_dtype;
+    const void *out_idx;
+    void *ckpt;               // nullable: [ckpt_slots][H][V][K] in ckpt_dtype
+    int32_t ckpt_dtype;
+    int32_t ckpt_every;       // tokens between checkpoints, a multiple of 64 (0: none)
+    int64_t ckpt_slots;       // capacity of ckpt; slots at or beyond it are not written
+    const int32_t *ckpt_off;  // [B + 1] first checkpoint slot of each sequence
+};
+
 bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d, PrefillLayout *out);
 
 struct PrefillArgs {
@@ -55,9 +78,7 @@ struct PrefillArgs {
     int32_t h, d;
     float scale;
     int32_t l2norm;
-    const void *init_state;
-    int32_t init_dtype;
-    float *final_state;
+    StateEnds se;  // ckpt_off is filled in from the workspace
     void *out;
     void *workspace;
     void *const *events;  // NULL, or 4 cudaEvent_t recorded at the kernel boundaries

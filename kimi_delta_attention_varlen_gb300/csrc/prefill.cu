@@ -42,29 +42,27 @@ using prefill::C;
 using prefill::Rec;
 using prefill::tile_off;
 using prefill::PassParams;
+using prefill::init_base;
+using prefill::out_base;
+using prefill::ckpt_slot;
+using prefill::load_state2;
+using prefill::store_state2;
 constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier polls
 
 // ---------------------------------------------------------- chunk table ---
 
-__global__ void __launch_bounds__(1024)
-chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_max, int32_t *__restrict__ chunk_off,
-                   int32_t *__restrict__ seq_order, int2 *__restrict__ chunk_info, int32_t *__restrict__ status)
+// Exclusive prefix sum of count(len_b) over the sequences into off[0 .. B]
+// (off[B] = total), by one block of 1024 threads.  Returns the total.
+template <typename F>
+__device__ int32_t block_prefix(const int32_t *__restrict__ cu, int64_t B, int32_t *__restrict__ off, F count,
+                                int32_t *warp_tot, int32_t *carry)
 {
-    __shared__ int32_t warp_tot[32];
-    __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        carry = 0;
-        *status = 0;
-    }
+    if (tid == 0) *carry = 0;
     __syncthreads();
     for (int64_t base = 0; base < B; base += 1024) {
         const int64_t b = base + tid;
-        int32_t n = 0;
-        if (b < B) {
-            const int32_t len = cu[b + 1] - cu[b];
-            n = len > 0 ? (len + C - 1) / C : 0;
-        }
+        const int32_t n = b < B ? count(cu[b + 1] - cu[b]) : 0;
         int32_t x = n;  // inclusive warp scan
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -83,17 +81,34 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_ma
             warp_tot[lane] = w;  // inclusive over warps
         }
         __syncthreads();
-        const int32_t before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - n;
-        if (b < B) chunk_off[b] = before;
+        const int32_t before = *carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - n;
+        if (b < B) off[b] = before;
         __syncthreads();
-        if (tid == 1023) carry = before + n;
+        if (tid == 1023) *carry = before + n;
         __syncthreads();
     }
-    if (tid == 0) chunk_off[B] = carry;
+    const int32_t total = *carry;
+    if (tid == 0) off[B] = total;
     __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(1024)
+chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_max, int32_t *__restrict__ chunk_off,
+                   int32_t *__restrict__ seq_order, int2 *__restrict__ chunk_info, int32_t ckpt_every,
+                   int32_t *__restrict__ ckpt_off, int32_t *__restrict__ status)
+{
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x;
+    if (tid == 0) *status = 0;
+    const int32_t total = block_prefix(
+        cu, B, chunk_off, [](int32_t len) { return len > 0 ? (len + C - 1) / C : 0; }, warp_tot, &carry);
+    if (ckpt_every > 0)  // checkpoints of sequence b: after every ckpt_every tokens, up to its length
+        block_prefix(
+            cu, B, ckpt_off, [ckpt_every](int32_t len) { return len > 0 ? len / ckpt_every : 0; }, warp_tot, &carry);
     // Per chunk: its first token and length ({0, 0} past the last chunk), so a
     // chunk's CTA finds its rows with one load.
-    const int32_t total = carry;
     for (int64_t c = tid; c < n_chunk_max; c += 1024) {
         int2 info = make_int2(0, 0);
         if (c < total) {
@@ -157,27 +172,28 @@ state_pass_kernel(PassParams p)
 
     // S^T accumulator fragments: s[n][e] = S^T(v = vg0 + gid + 8 (e >> 1), k = 8 n + 2 tig + (e & 1))
     float s[D / 8][4];
+    const int64_t per_seq = H * D * D;
+    // element offset of (v = vg0 + gid + 8 hr, k = 8 n + 2 tig) within a state
+    auto elem = [&](int n, int hr) {
+        return (static_cast<int64_t>(h) * D + vg0 + gid + 8 * hr) * D + 8 * n + 2 * tig;
+    };
+    auto put_state = [&](void *dst, int32_t dtype, int64_t base) {
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr)
+                store_state2(dst, dtype, base + elem(n, hr), make_float2(s[n][2 * hr], s[n][2 * hr + 1]));
+    };
     {
-        const int64_t base = ((b * H + h) * D) * D;
+        const int64_t base = init_base(p.se, b, per_seq);
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
-                const int64_t e = base + static_cast<int64_t>(vg0 + gid + 8 * hr) * D + 8 * n + 2 * tig;
-                float x0 = 0.f, x1 = 0.f;
-                if (p.init != nullptr) {
-                    if (p.init_dtype == KDA_F32) {
-                        const float2 t = *reinterpret_cast<const float2 *>(static_cast<const float *>(p.init) + e);
-                        x0 = t.x;
-                        x1 = t.y;
-                    } else {
-                        const uint32_t t = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(p.init) + e);
-                        x0 = bf16_lo(t);
-                        x1 = bf16_hi(t);
-                    }
-                }
-                s[n][2 * hr] = x0;
-                s[n][2 * hr + 1] = x1;
+                float2 x = make_float2(0.f, 0.f);
+                if (base >= 0) x = load_state2(p.se.init, p.se.init_dtype, base + elem(n, hr));
+                s[n][2 * hr] = x.x;
+                s[n][2 * hr + 1] = x.y;
             }
         }
     }
@@ -318,19 +334,13 @@ state_pass_kernel(PassParams p)
         }
         __syncthreads();  // every warp is done with this stage
         if (tid == 0 && i + 2 < n_chunks) issue(i + 2, st);
+        const int64_t ck = ckpt_slot(p.se, b, i, tok_end - tok_begin);  // S is the state after chunk i
+        if (ck >= 0) put_state(p.se.ckpt, p.se.ckpt_dtype, ck * per_seq);
     }
 
-    if (p.final_state != nullptr) {
-        const int64_t base = ((b * H + h) * D) * D;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int64_t e = base + static_cast<int64_t>(vg0 + gid + 8 * hr) * D + 8 * n + 2 * tig;
-                *reinterpret_cast<float2 *>(p.final_state + e) = make_float2(s[n][2 * hr], s[n][2 * hr + 1]);
-            }
-        }
-    }
+    if (p.se.final_state != nullptr) put_state(p.se.final_state, KDA_F32, b * per_seq);
+    const int64_t ob = out_base(p.se, b);
+    if (ob >= 0) put_state(p.se.out_cache, p.se.out_dtype, ob);
 }
 
 template <int D, typename IO, int WARPS>
@@ -354,7 +364,9 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     int32_t *chunk_off = reinterpret_cast<int32_t *>(ws + L.off_chunk_off);
     int32_t *seq_order = reinterpret_cast<int32_t *>(ws + L.off_seq_order);
     int2 *chunk_info = reinterpret_cast<int2 *>(ws + L.off_chunk_info);
+    int32_t *ckpt_off = reinterpret_cast<int32_t *>(ws + L.off_ckpt_off);
     char *records = ws + L.off_records;
+    const int32_t ckpt_every = a.se.ckpt != nullptr ? a.se.ckpt_every : 0;
 
     auto mark = [&](int i) -> cudaError_t {
         return a.events ? cudaEventRecord(static_cast<cudaEvent_t>(a.events[i]), st) : cudaSuccess;
@@ -362,7 +374,7 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     cudaError_t e = mark(0);
     if (e != cudaSuccess) return e;
     chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.num_seqs, L.n_chunk_max, chunk_off, seq_order, chunk_info,
-                                           status);
+                                           ckpt_every, ckpt_off, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if ((e = mark(1)) != cudaSuccess) return e;
@@ -374,8 +386,10 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     }
 
     if ((e = mark(2)) != cudaSuccess) return e;
-    PassParams sp{a.cu_seqlens, chunk_off, seq_order, status, records, a.h, a.init_state, a.init_dtype,
-                  a.final_state, a.out};
+    StateEnds se = a.se;
+    se.ckpt_every = ckpt_every;
+    se.ckpt_off = ckpt_off;
+    PassParams sp{a.cu_seqlens, chunk_off, seq_order, status, records, a.h, se, a.out};
     // Enough CTAs to cover the SMs: split the value columns when there are few
     // (sequence, head) pairs.  Columns of S evolve independently.
     const int64_t items = a.num_seqs * a.h;
@@ -417,7 +431,8 @@ bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d
     L.off_chunk_off = 256;
     L.off_seq_order = up(L.off_chunk_off + 4 * static_cast<size_t>(num_seqs + 1), 256);
     L.off_chunk_info = up(L.off_seq_order + 4 * static_cast<size_t>(num_seqs), 256);
-    L.off_records = up(L.off_chunk_info + 8 * static_cast<size_t>(L.n_chunk_max), 1024);
+    L.off_ckpt_off = up(L.off_chunk_info + 8 * static_cast<size_t>(L.n_chunk_max), 256);
+    L.off_records = up(L.off_ckpt_off + 4 * static_cast<size_t>(num_seqs + 1), 1024);
     L.total = L.off_records + static_cast<size_t>(L.n_chunk_max) * static_cast<size_t>(h) * L.rec_bytes;
     *out = L;
     return true;

@@ -65,11 +65,70 @@ struct PassParams {
     int32_t *status;
     const char *records;
     int32_t H;
-    const void *init;
-    int32_t init_dtype;
-    float *final_state;
+    StateEnds se;
     void *out;
 };
+
+__device__ __forceinline__ int64_t row_index(const void *idx, int32_t it, int64_t b)
+{
+    return it == KDA_I64 ? static_cast<const int64_t *>(idx)[b] : static_cast<const int32_t *>(idx)[b];
+}
+
+// Base element offset of sequence b's initial state, or -1 for zeros.
+__device__ __forceinline__ int64_t init_base(const StateEnds &e, int64_t b, int64_t per_seq)
+{
+    if (e.init == nullptr) return -1;
+    if (e.in_idx == nullptr) return b * per_seq;
+    const int64_t r = row_index(e.in_idx, e.idx_type, b);
+    if (r < 0 || r >= e.n_rows || (e.in_flags != nullptr && e.in_flags[b] == 0)) return -1;
+    return r * e.row_stride;
+}
+
+// Base element offset of the cache row that receives sequence b's final state, or -1.
+__device__ __forceinline__ int64_t out_base(const StateEnds &e, int64_t b)
+{
+    if (e.out_cache == nullptr) return -1;
+    const int64_t r = row_index(e.out_idx, e.idx_type, b);
+    return (r < 0 || r >= e.n_rows) ? -1 : r * e.row_stride;
+}
+
+// Checkpoint slot written after chunk c (0-based) of sequence b, or -1.
+__device__ __forceinline__ int64_t ckpt_slot(const StateEnds &e, int64_t b, int32_t c, int64_t len)
+{
+    if (e.ckpt == nullptr || e.ckpt_every <= 0) return -1;
+    const int64_t end = static_cast<int64_t>(c + 1) * kChunk;  // tokens done after chunk c
+    if (end > len || end % e.ckpt_every != 0) return -1;
+    const int64_t s = e.ckpt_off[b] + end / e.ckpt_every - 1;
+    return s < e.ckpt_slots ? s : -1;
+}
+
+// Four consecutive state elements: load as fp32 / store with the dtype's cast (bf16: RNE).
+__device__ __forceinline__ float4 load_state4(const void *base, int32_t dtype, int64_t e)
+{
+    if (dtype == KDA_F32) return *reinterpret_cast<const float4 *>(static_cast<const float *>(base) + e);
+    const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(base) + e);
+    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+__device__ __forceinline__ void store_state4(void *base, int32_t dtype, int64_t e, float4 x)
+{
+    if (dtype == KDA_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(base) + e) = x;
+    } else {
+        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(base) + e) =
+            make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+    }
+}
+__device__ __forceinline__ float2 load_state2(const void *base, int32_t dtype, int64_t e)
+{
+    if (dtype == KDA_F32) return *reinterpret_cast<const float2 *>(static_cast<const float *>(base) + e);
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(base) + e);
+    return make_float2(bf16_lo(u), bf16_hi(u));
+}
+__device__ __forceinline__ void store_state2(void *base, int32_t dtype, int64_t e, float2 x)
+{
+    if (dtype == KDA_F32) *reinterpret_cast<float2 *>(static_cast<float *>(base) + e) = x;
+    else *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(base) + e) = pack_bf16x2(x.x, x.y);
+}
 
 // Launches the tensor-memory state pass (D = 128, bf16 output, one CTA per
 // (sequence, head)) over `items` = num_seqs x h CTAs.

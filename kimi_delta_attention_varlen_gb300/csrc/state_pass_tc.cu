@@ -86,9 +86,19 @@ state_pass_tc_kernel(PassParams p)
     const uint32_t tmem = tmem_base;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);  // this warp's lanes
 
+    const int64_t row_v = (static_cast<int64_t>(h) * kTcD + v) * kTcD;  // element offset of [v][0] within a state
+    // 32 consecutive fp32 values of S^T row v (columns c0 ...) -> a state buffer, with its dtype's cast
+    auto put_row = [&](void *dst, int32_t dtype, int64_t base, int c0, const uint32_t r[32]) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+            store_state4(dst, dtype, base + row_v + c0 + e,
+                         make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                     __uint_as_float(r[e + 3])));
+    };
+
     // initial state: columns [64 half, 64 half + 64) of S^T row v (= cache row [v][k])
     {
-        const int64_t base = ((b * H + h) * kTcD + v) * kTcD;
+        const int64_t base = init_base(p.se, b, H * kTcD * kTcD);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int c0 = 64 * half + 32 * j;
@@ -96,14 +106,7 @@ state_pass_tc_kernel(PassParams p)
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.init != nullptr) {
-                    if (p.init_dtype == KDA_F32) {
-                        x = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.init) + base + c0 + e);
-                    } else {
-                        const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.init) + base + c0 + e);
-                        x = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-                    }
-                }
+                if (base >= 0) x = load_state4(p.se.init, p.se.init_dtype, base + row_v + c0 + e);
                 r[e] = __float_as_uint(x.x);
                 r[e + 1] = __float_as_uint(x.y);
                 r[e + 2] = __float_as_uint(x.z);
@@ -164,6 +167,20 @@ state_pass_tc_kernel(PassParams p)
         const float4 *gam4 = reinterpret_cast<const float4 *>(sb + RT::GAMMA);
         const uint32_t ycol = kColY + 64 * static_cast<uint32_t>(i & 1);
 
+        // S is now the state after chunk i - 1: a checkpoint when that chunk ends on one.
+        if (p.se.ckpt != nullptr && i > 0) {
+            const int64_t ck = ckpt_slot(p.se, b, i - 1, tok_end - tok_begin);
+            if (ck >= 0) {
+#pragma unroll 1
+                for (int j = 0; j < 2; ++j) {
+                    const int c0 = 64 * half + 32 * j;
+                    uint32_t r[32];
+                    tc::ld32(tl + kColS + c0, r);
+                    tc::wait_ld();
+                    put_row(p.se.ckpt, p.se.ckpt_dtype, ck * H * kTcD * kTcD, c0, r);
+                }
+            }
+        }
         // (A) S^T row v, this warp's 64 columns -> bf16 operand (undecayed); decay the TMEM copy by gamma
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -251,18 +268,22 @@ state_pass_tc_kernel(PassParams p)
     }
     if (n_chunks > 0) write_outputs(n_chunks - 1);
 
-    if (p.final_state != nullptr) {
-        float *fs = p.final_state + ((b * H + h) * kTcD + v) * kTcD;
+    // final state -> packed fp32, the cache row out_idx[b], and the last checkpoint if it ends there
+    {
+        const int64_t per_seq = H * kTcD * kTcD;
+        const int64_t ob = out_base(p.se, b);
+        const int64_t ck = n_chunks > 0 ? ckpt_slot(p.se, b, n_chunks - 1, tok_end - tok_begin) : -1;
+        if (p.se.final_state != nullptr || ob >= 0 || ck >= 0) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int c0 = 64 * half + 32 * j;
-            uint32_t r[32];
-            tc::ld32(tl + kColS + c0, r);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4 *>(fs + c0 + e) = make_float4(
-                    __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+            for (int j = 0; j < 2; ++j) {
+                const int c0 = 64 * half + 32 * j;
+                uint32_t r[32];
+                tc::ld32(tl + kColS + c0, r);
+                tc::wait_ld();
+                if (p.se.final_state != nullptr) put_row(p.se.final_state, KDA_F32, b * per_seq, c0, r);
+                if (ob >= 0) put_row(p.se.out_cache, p.se.out_dtype, ob, c0, r);
+                if (ck >= 0) put_row(p.se.ckpt, p.se.ckpt_dtype, ck * per_seq, c0, r);
+            }
         }
     }
     tc::fence_before_sync();

@@ -131,6 +131,54 @@ def test_prefill_rejections(L):
     assert prefill(L, ws_bytes=need - 1) == WORKSPACE
 
 
+def cached(L, c, **kw):
+    a = dict(q=A, k=A, v=A, io=1, g=A, beta=A, cu=A, B=2, T=100, h=2, dk=32, dv=32, scale=0.1, l2=1, idx_in=A,
+             flags=None, idx_out=None, it=0, final=None, ckpt=None, ckpt_dtype=0, every=0, slots=0, out=A, ws=A,
+             ws_bytes=1 << 40)
+    a.update(kw)
+    return L.kda_prefill_varlen_cached(a["q"], a["k"], a["v"], a["io"], a["g"], a["beta"], a["cu"], a["B"], a["T"],
+                                       a["h"], a["dk"], a["dv"], a["scale"], a["l2"],
+                                       ctypes.byref(c) if c is not None else None, a["idx_in"], a["flags"],
+                                       a["idx_out"], a["it"], a["final"], a["ckpt"], a["ckpt_dtype"], a["every"],
+                                       a["slots"], a["out"], a["ws"], a["ws_bytes"], None)
+
+
+def test_cached_prefill_rejections(L):
+    c = cache()
+    assert cached(L, None) == NULL
+    assert cached(L, cache(data=0)) == NULL
+    assert cached(L, cache(h=3)) == SHAPE           # cache heads != h
+    assert cached(L, c, dk=64, dv=64) == SHAPE
+    assert cached(L, c, it=5) == DTYPE
+    assert cached(L, c, idx_in=None) == NULL
+    assert cached(L, c, idx_in=A + 2) == ALIGN
+    assert cached(L, c, idx_out=A + 4, it=1) == ALIGN
+    assert cached(L, cache(data=A + 4)) == ALIGN    # rows must be 16-byte aligned
+    assert cached(L, cache(stride=2 * 32 * 32 + 2)) == ALIGN
+    assert cached(L, c, ckpt=A, every=100) == SHAPE  # not a multiple of 64
+    assert cached(L, c, ckpt=A, every=0) == SHAPE
+    assert cached(L, c, ckpt=A, every=64, slots=-1) == SHAPE
+    assert cached(L, c, ckpt=A, every=64, ckpt_dtype=5) == DTYPE
+    assert cached(L, c, ckpt=A + 8, every=64, slots=4) == ALIGN
+    assert cached(L, c, io=4) == DTYPE
+    assert cached(L, c, final=A + 8) == ALIGN
+    need = L.kda_prefill_workspace_size(100, 2, 2, 32, 32)
+    assert cached(L, c, ws_bytes=need - 1) == WORKSPACE
+
+
+def test_checkpoint_count(L):
+    def count(offsets, every):
+        arr = (ctypes.c_int32 * len(offsets))(*offsets)
+        return L.kda_prefill_checkpoint_count(arr, len(offsets) - 1, every)
+    assert count([0, 130, 130, 384], 64) == 2 + 0 + 3
+    assert count([0, 130, 130, 384], 128) == 1 + 0 + 1
+    assert count([0, 63], 64) == 0
+    assert count([0, 10, 5], 64) == -1   # decreasing
+    assert count([0, 64], 100) == -1     # not a multiple of 64
+    assert L.kda_prefill_checkpoint_count(None, 1, 64) == -1
+    assert kda.kda_prefill_checkpoint_count([0, 256, 320], 64) == 5
+
+
 def decode(L, c, **kw):
     a = dict(q=A, k=A, v=A, io=1, g=A, beta=A, R=8, h=2, dk=32, dv=32, scale=0.1, l2=1, idx=A, it=0, out=A)
     a.update(kw)
