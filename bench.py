@@ -246,6 +246,38 @@ def prefill_flops(P) -> float:
     return float(n_chunks * H * per)
 
 
+def cached_measure(P, steps: int, warmup: int, ckpt_every: int = 1024) -> dict:
+    """The fused cache-indexed prefill on the step's inputs (initial states read from
+    cache rows, final states written back), without and with checkpoints every
+    `ckpt_every` tokens (fp32); median device time of `steps` calls each."""
+    import kimi_delta_attention_varlen_gb300 as kda
+    inp, T = P["inp"], P["cu_list"][-1]
+    n_ck = kda.kda_prefill_checkpoint_count(P["cu_list"], ckpt_every)
+    w = P["w"]
+    ck = torch.empty(n_ck, w.H, w.V, w.K, dtype=torch.float32, device=P["out"].device)
+    res = {}
+    for name, kw in (("no_checkpoints", {}), ("checkpoints", {"checkpoints": ck, "ckpt_every": ckpt_every})):
+        def call():
+            kda.kda_prefill_varlen_cached(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], P["cu"], P["out"],
+                                          P["ws"], P["cache3"].view, P["gidx"], flags=P["gflags"],
+                                          idx_out=P["sidx"], **kw)
+        for _ in range(warmup):
+            call()
+        times = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        res[name] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3)}
+    res["checkpoints"].update({"every_tokens": ckpt_every, "slots": n_ck, "dtype": "f32",
+                               "bytes": n_ck * w.H * w.V * w.K * 4})
+    return res
+
+
 def copy_measure(dev, steps: int, warmup: int) -> dict:
     import kimi_delta_attention_varlen_gb300 as kda
     from kimi_delta_attention_varlen_gb300 import workloads as wl
@@ -406,6 +438,7 @@ def native(args, ranks: Ranks) -> dict | None:
     e2e_value, _ = aggregate(T * e2e_steps, a.elapsed_time(b) * 1e-3, ranks)
 
     copy = copy_measure(dev, max(5, args.steps), max(3, args.warmup))
+    fused = cached_measure(P, max(5, args.steps), max(3, args.warmup))
     pk, pk_kind = peaks()
     nb = prefill_bytes(P)
     flops = prefill_flops(P)
@@ -446,6 +479,7 @@ def native(args, ranks: Ranks) -> dict | None:
                        "gather_frac": copy["gather"]["gbs"] / pk["hbm_gbs"],
                        "scatter_frac": copy["scatter"]["gbs"] / pk["hbm_gbs"]},
         "decode": {"ms": br["decode"], "requests_per_s": P["dw"].R / (br["decode"] * 1e-3)},
+        "cached_prefill": {**fused, "unfused_ms": br["gather"] + prefill_ms + br["scatter"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk,

@@ -73,6 +73,14 @@ def _load():
             lib.oracle_prefill_ckpt.argtypes = lib.oracle_prefill.argtypes[:16] + [ctypes.c_int64, _D,
                                                                                  ctypes.c_int]
             lib.oracle_prefill_ckpt.restype = ctypes.c_int
+            lib.oracle_ckpt_store_int8.argtypes = [_VP, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _I64, _I64,
+                                                   ctypes.c_int64, _VP, _VP, ctypes.c_int64]
+            lib.oracle_ckpt_store_int8.restype = ctypes.c_int
+            lib.oracle_ckpt_load_int8.argtypes = [_VP, _VP, ctypes.c_int64, _I64, _I64, ctypes.c_int64, _VP,
+                                                  ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_int64]
+            lib.oracle_ckpt_load_int8.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [_D, _D, _D, _D, _D, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
                                           ctypes.c_int, ctypes.c_double, _VP, ctypes.c_int,
@@ -208,6 +216,35 @@ def prefill_ckpt(q, k, v, g, beta, cu_seqlens, every, init=None, scale=1.0, l2no
     if rc != 0:
         raise ValueError(f"oracle_prefill_ckpt failed ({rc})")
     return out, final, ckpt[:slots]
+
+
+def ckpt_store_int8(active_flat: np.ndarray, n_rows: int, row_stride: int, H: int, V: int, K: int,
+                    src, dst, qdata: np.ndarray, scale: np.ndarray) -> None:
+    """Quantise active rows (float32, or bf16 as uint16 bits; rows of row_stride elements
+    holding [H, V, K]) into qdata [slots, H, V, K] int8 and scale [slots, H, K] float32, in
+    place, for pairs (src[s], dst[s]) with valid indices."""
+    assert active_flat.flags.c_contiguous and qdata.flags.c_contiguous and scale.flags.c_contiguous
+    assert qdata.dtype == np.int8 and scale.dtype == np.float32
+    src, dst = _i64(src).reshape(-1), _i64(dst).reshape(-1)
+    assert src.size == dst.size
+    rc = _load().oracle_ckpt_store_int8(active_flat.ctypes.data, _dtype_code(active_flat), n_rows, row_stride,
+                                        H, V, K, _ptr(src, _I64), _ptr(dst, _I64), src.size,
+                                        qdata.ctypes.data, scale.ctypes.data, qdata.shape[0])
+    if rc != 0:
+        raise ValueError(f"oracle_ckpt_store_int8 failed ({rc})")
+
+
+def ckpt_load_int8(qdata: np.ndarray, scale: np.ndarray, src, dst, active_flat: np.ndarray, n_rows: int,
+                   row_stride: int, H: int, V: int, K: int) -> None:
+    """Dequantise checkpoint slots src[s] into active rows dst[s] (in place)."""
+    assert active_flat.flags.c_contiguous and qdata.flags.c_contiguous and scale.flags.c_contiguous
+    src, dst = _i64(src).reshape(-1), _i64(dst).reshape(-1)
+    assert src.size == dst.size
+    rc = _load().oracle_ckpt_load_int8(qdata.ctypes.data, scale.ctypes.data, qdata.shape[0], _ptr(src, _I64),
+                                       _ptr(dst, _I64), src.size, active_flat.ctypes.data,
+                                       _dtype_code(active_flat), n_rows, row_stride, H, V, K)
+    if rc != 0:
+        raise ValueError(f"oracle_ckpt_load_int8 failed ({rc})")
 
 
 def decode(q, k, v, g, beta, cache_flat: np.ndarray, n_rows: int, row_stride: int, idx,

@@ -29,6 +29,11 @@
  *                   extend listing does before its chunk math.
  *   oracle_prefill_ckpt  oracle_prefill plus the state after every `every`
  *                   tokens of each sequence (chunk-boundary checkpoints).
+ *   oracle_ckpt_store_int8 / oracle_ckpt_load_int8
+ *                   the INT8 checkpoint of the infra page, section 6.6.2
+ *                   (Int8CheckpointStore): per (slot, head, k) a scale from
+ *                   the max-abs over d_v, symmetric codes in [-127, 127];
+ *                   loading multiplies back into an active state row.
  *   oracle_decode   one token of the same recurrence per request, reading
  *                   the state from a cache row by index and writing it back
  *                   in the cache dtype (the decode route named on the state
@@ -147,6 +152,81 @@ int oracle_scatter(void *cache, int cache_dtype, int64_t n_rows, int64_t payload
                 ((uint16_t *)cache)[dst] = orc_f32_to_bf16(((const float *)packed)[src]);
             }
         }
+    }
+    return 0;
+}
+
+/* ---------------------------- INT8 checkpoints ---------------------------- */
+
+static float orc_load_f32(const void *base, int dtype, int64_t e)
+{
+    return dtype == ORC_F32 ? ((const float *)base)[e] : orc_bf16_to_f32(((const uint16_t *)base)[e]);
+}
+
+/* Quantise active state rows into checkpoint slots: for each pair s with
+ * 0 <= src[s] < n_rows and 0 <= dst[s] < n_slots, and each head h and key
+ * channel k of the row's [H, V, K] block x (upcast to fp32):
+ *   amax = max over v of |x[h][v][k]|;  scale = amax / 127;
+ *   code[v] = round_half_even(x[h][v][k] / scale), clamped to [-127, 127]
+ *             (all codes 0 when amax == 0);
+ * qdata[dst][h][v][k] = code, scale_out[dst][h][k] = scale.  Every operation
+ * is one correctly rounded fp32 operation (the precision in which the codes
+ * are decided on the GPU as well).  Pairs with an invalid index are skipped. */
+int oracle_ckpt_store_int8(const void *active, int dtype, int64_t n_rows, int64_t row_stride,
+                           int64_t H, int64_t V, int64_t K, const int64_t *src, const int64_t *dst,
+                           int64_t count, int8_t *qdata, float *scale_out, int64_t n_slots)
+{
+    if (dtype != ORC_F32 && dtype != ORC_BF16) return -1;
+    if (n_rows <= 0 || H <= 0 || V <= 0 || K <= 0 || row_stride < H * V * K || count < 0) return -1;
+    for (int64_t s = 0; s < count; ++s) {
+        const int64_t r = src[s], c = dst[s];
+        if (r < 0 || r >= n_rows || c < 0 || c >= n_slots) continue;
+        for (int64_t h = 0; h < H; ++h) {
+            for (int64_t k = 0; k < K; ++k) {
+                float amax = 0.0f;
+                for (int64_t v = 0; v < V; ++v) {
+                    const float a = fabsf(orc_load_f32(active, dtype, r * row_stride + (h * V + v) * K + k));
+                    if (a > amax) amax = a;
+                }
+                const float sc = amax / 127.0f;
+                scale_out[(c * H + h) * K + k] = sc;
+                for (int64_t v = 0; v < V; ++v) {
+                    int q = 0;
+                    if (amax > 0.0f) {
+                        const float y = orc_load_f32(active, dtype, r * row_stride + (h * V + v) * K + k) / sc;
+                        const float rq = nearbyintf(y); /* default rounding: to nearest, ties to even */
+                        q = rq > 127.0f ? 127 : rq < -127.0f ? -127 : (int)rq;
+                    }
+                    qdata[((c * H + h) * V + v) * K + k] = (int8_t)q;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Dequantise checkpoint slots into active state rows: for each pair s with
+ * 0 <= src_slot[s] < n_slots and 0 <= dst_row[s] < n_rows,
+ *   active[dst][h][v][k] = to_dtype(code[src][h][v][k] * scale[src][h][k])
+ * (one fp32 multiply; bf16 rows round to nearest even).  Other rows and the
+ * gaps between rows are not touched. */
+int oracle_ckpt_load_int8(const int8_t *qdata, const float *scale, int64_t n_slots,
+                          const int64_t *src_slot, const int64_t *dst_row, int64_t count, void *active,
+                          int dtype, int64_t n_rows, int64_t row_stride, int64_t H, int64_t V, int64_t K)
+{
+    if (dtype != ORC_F32 && dtype != ORC_BF16) return -1;
+    if (n_rows <= 0 || H <= 0 || V <= 0 || K <= 0 || row_stride < H * V * K || count < 0) return -1;
+    for (int64_t s = 0; s < count; ++s) {
+        const int64_t c = src_slot[s], r = dst_row[s];
+        if (c < 0 || c >= n_slots || r < 0 || r >= n_rows) continue;
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t v = 0; v < V; ++v)
+                for (int64_t k = 0; k < K; ++k) {
+                    const float x = (float)qdata[((c * H + h) * V + v) * K + k] * scale[(c * H + h) * K + k];
+                    const int64_t e = r * row_stride + (h * V + v) * K + k;
+                    if (dtype == ORC_F32) ((float *)active)[e] = x;
+                    else ((uint16_t *)active)[e] = orc_f32_to_bf16(x);
+                }
     }
     return 0;
 }

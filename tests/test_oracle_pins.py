@@ -519,3 +519,88 @@ def test_checkpoint_interval_longer_than_every_sequence_records_nothing():
     q, k, v, g, beta, cu = rand_tokens(42, [10, 127], 1, 4, 4)
     _, _, ck = oracle.prefill_ckpt(q, k, v, g, beta, cu, 128)
     assert ck.shape[0] == 0
+
+
+# --------------------------------------------------------------------------
+# INT8 checkpoints
+# --------------------------------------------------------------------------
+
+def _golden_int8():
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "int8_ckpt_small.txt")):
+        if line.startswith("#") or ":" not in line:
+            continue
+        key, rest = line.split(":", 1)
+        vals[key.strip()] = [float(x) for x in rest.split()]
+    return vals
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_int8_checkpoint_golden(dtype):
+    gv = _golden_int8()
+    V, K = int(gv["V"][0]), int(gv["K"][0])
+    x = np.array(gv["state_v_major"], dtype=np.float32)
+    stride = V * K + 3  # a gap after the row
+    N = 2
+    act = np.full(N * stride, 99.0, dtype=np.float32)
+    act[stride:stride + V * K] = x  # row 1
+    if dtype == "bf16":
+        act = oracle.f32_to_bf16_bits(act)
+    q = np.full((3, 1, V, K), 55, dtype=np.int8)
+    sc = np.full((3, 1, K), -1.0, dtype=np.float32)
+    oracle.ckpt_store_int8(act, N, stride, 1, V, K, [1, -1, 0], [2, 0, 7], q, sc)
+    np.testing.assert_array_equal(q[2].reshape(-1), np.array(gv["codes_v_major"], dtype=np.int8))
+    np.testing.assert_array_equal(sc[2].reshape(-1), np.array(gv["scale"], dtype=np.float32))
+    assert np.all(q[:2] == 55) and np.all(sc[:2] == -1.0)  # invalid src (-1) and dst (7) pairs: skipped
+    back = np.full(N * stride, 99.0, dtype=np.float32)
+    if dtype == "bf16":
+        back = oracle.f32_to_bf16_bits(back)
+    oracle.ckpt_load_int8(q, sc, [2, 9], [0, 1], back, N, stride, 1, V, K)
+    row0 = back[:V * K]
+    if dtype == "bf16":
+        row0 = (row0.astype(np.uint32) << 16).view(np.float32)
+    np.testing.assert_array_equal(row0, np.array(gv["back_v_major"], dtype=np.float32))
+    rest = back[V * K:]
+    want = np.full(rest.shape, 99.0, dtype=np.float32)
+    if dtype == "bf16":
+        want = oracle.f32_to_bf16_bits(want)
+    np.testing.assert_array_equal(rest, want)  # gap, row 1 (invalid slot 9): untouched
+
+
+def test_int8_checkpoint_error_bound_and_extremes():
+    """|back - x| <= scale / 2 element-wise (plus fp32 rounding of the product); the
+    column's max-abs element maps to +-127; negating the state negates the codes."""
+    rng = np.random.default_rng(50)
+    H, V, K = 2, 16, 8
+    x = (rng.standard_normal((3, H, V, K)) * rng.uniform(0.01, 10, (3, H, 1, K))).astype(np.float32)
+    act = x.reshape(-1).copy()
+    stride = H * V * K
+    q = np.zeros((3, H, V, K), dtype=np.int8)
+    sc = np.zeros((3, H, K), dtype=np.float32)
+    oracle.ckpt_store_int8(act, 3, stride, H, V, K, [0, 1, 2], [0, 1, 2], q, sc)
+    amax = np.abs(x).max(axis=2)
+    np.testing.assert_allclose(sc, amax / 127, rtol=1e-6)
+    at_max = np.abs(x) == amax[:, :, None, :]
+    assert np.all(np.abs(q[at_max]) == 127)
+    back = np.zeros_like(act)
+    oracle.ckpt_load_int8(q, sc, [0, 1, 2], [0, 1, 2], back, 3, stride, H, V, K)
+    err = np.abs(back.reshape(x.shape) - x)
+    assert np.all(err <= sc[:, :, None, :] * (0.5 + 1e-5) + 1e-30)
+    qn = np.zeros_like(q)
+    scn = np.zeros_like(sc)
+    oracle.ckpt_store_int8((-x).reshape(-1).copy(), 3, stride, H, V, K, [0, 1, 2], [0, 1, 2], qn, scn)
+    np.testing.assert_array_equal(qn, -q)
+    np.testing.assert_array_equal(scn, sc)
+
+
+def test_int8_checkpoint_power_of_two_scaling_keeps_codes():
+    """Scaling a state by 2^m is exact in fp32: the scales scale by 2^m, the codes stay."""
+    rng = np.random.default_rng(51)
+    H, V, K = 1, 8, 4
+    x = rng.standard_normal((1, H, V, K)).astype(np.float32)
+    q1, s1 = np.zeros((1, H, V, K), np.int8), np.zeros((1, H, K), np.float32)
+    q2, s2 = np.zeros_like(q1), np.zeros_like(s1)
+    oracle.ckpt_store_int8(x.reshape(-1).copy(), 1, V * K, H, V, K, [0], [0], q1, s1)
+    oracle.ckpt_store_int8((x * 8).reshape(-1).copy(), 1, V * K, H, V, K, [0], [0], q2, s2)
+    np.testing.assert_array_equal(q1, q2)
+    np.testing.assert_array_equal(s2, s1 * 8)
