@@ -278,6 +278,38 @@ def cached_measure(P, steps: int, warmup: int, ckpt_every: int = 1024) -> dict:
     return res
 
 
+def ckpt_int8_measure(P, steps: int, warmup: int, pairs: int = 256) -> dict:
+    """INT8 checkpoint store (active fp32 rows -> int8 slots) and load (slots -> rows)
+    of `pairs` states of the step's cache [1024, 32, 128, 128]; median device time and
+    GB/s of the compulsory bytes (state rows, codes, scales)."""
+    import kimi_delta_attention_varlen_gb300 as kda
+    pc = P["cache3"]
+    N, H, V, K = pc.view.shape
+    dev = pc.view.device
+    rows = torch.randperm(N, generator=torch.Generator().manual_seed(21))[:pairs].to(torch.int32).to(dev)
+    slots = torch.arange(pairs, dtype=torch.int32, device=dev)
+    q = torch.empty(pairs, H, V, K, dtype=torch.int8, device=dev)
+    sc = torch.empty(pairs, H, K, dtype=torch.float32, device=dev)
+    state_b = pairs * H * V * K * pc.view.element_size()
+    code_b = pairs * H * V * K + pairs * H * K * 4
+    res = {"pairs": pairs, "cache": f"fp32 [{N},{H},{V},{K}]"}
+    for name, fn in (("store", lambda: kda.kda_ckpt_store_int8(pc.view, rows, slots, q, sc)),
+                     ("load", lambda: kda.kda_ckpt_load_int8(q, sc, slots, pc.view, rows))):
+        for _ in range(warmup):
+            fn()
+        times = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        res[name] = {"ms": ms, "gbs": (state_b + code_b) / (ms * 1e-3) / 1e9, "bytes": state_b + code_b}
+    return res
+
+
 def copy_measure(dev, steps: int, warmup: int) -> dict:
     import kimi_delta_attention_varlen_gb300 as kda
     from kimi_delta_attention_varlen_gb300 import workloads as wl
@@ -439,6 +471,7 @@ def native(args, ranks: Ranks) -> dict | None:
 
     copy = copy_measure(dev, max(5, args.steps), max(3, args.warmup))
     fused = cached_measure(P, max(5, args.steps), max(3, args.warmup))
+    ck8 = ckpt_int8_measure(P, max(5, args.steps), max(3, args.warmup))
     pk, pk_kind = peaks()
     nb = prefill_bytes(P)
     flops = prefill_flops(P)
@@ -480,6 +513,8 @@ def native(args, ranks: Ranks) -> dict | None:
                        "scatter_frac": copy["scatter"]["gbs"] / pk["hbm_gbs"]},
         "decode": {"ms": br["decode"], "requests_per_s": P["dw"].R / (br["decode"] * 1e-3)},
         "cached_prefill": {**fused, "unfused_ms": br["gather"] + prefill_ms + br["scatter"]},
+        "ckpt_int8": {**ck8, "store_frac": ck8["store"]["gbs"] / pk["hbm_gbs"],
+                      "load_frac": ck8["load"]["gbs"] / pk["hbm_gbs"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk,

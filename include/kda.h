@@ -294,6 +294,46 @@ int kda_prefill_varlen_noalloc(const void *q, const void *k, const void *v, int3
                                int32_t init_dtype, float *final_state, void *out, void *stream);
 
 /* ------------------------------------------------------------------------
+ * kda_ckpt_store_int8 / kda_ckpt_load_int8
+ *
+ * INT8 checkpoints of recurrent states, the Int8CheckpointStore of the
+ * "KDA's challenges for AI infra" page, section 6.6.2: inactive states are
+ * kept as symmetric int8 codes with one fp32 scale per (slot, head, key
+ * channel), taken from the max-abs along the value dimension; a cache hit
+ * dequantises once into an active slot, which then continues in full
+ * precision.  For one layer's pools:
+ *
+ *   qdata  [n_slots, h, v, k] device int8, contiguous, 16-byte aligned
+ *   scale  [n_slots, h, k]    device fp32, contiguous, 16-byte aligned
+ *   active the state cache (kda_cache; v == k in {32, 64, 128}; data and
+ *          row stride 16-byte aligned)
+ *
+ * store: for each pair s with 0 <= src_rows[s] < n_rows and
+ *   0 <= dst_slots[s] < n_slots, for each head h and key channel k of the
+ *   row's [h][v][k] block x (upcast to fp32):
+ *     amax = max_v |x[h][v][k]|,  scale[dst][h][k] = amax / 127,
+ *     qdata[dst][h][v][k] = round_half_even(x / scale) clamped to
+ *     [-127, 127] (0 when amax == 0),
+ *   each a correctly rounded fp32 operation.  Pairs with an invalid index
+ *   are skipped; other slots are not touched.
+ * load: for each pair s with 0 <= src_slots[s] < n_slots and
+ *   0 <= dst_rows[s] < n_rows:  active[dst][h][v][k] =
+ *   qdata[src][h][v][k] * scale[src][h][k] (one fp32 multiply), converted
+ *   to the cache dtype (bf16: round to nearest even).  Gaps and other rows
+ *   are not touched.
+ *   src_*, dst_*  [count] device, idx_type (int32 / int64).
+ *   count == 0 validates the metadata and launches nothing.
+ *   Preconditions (not checked, no host sync): valid destinations are
+ *   unique; the pools do not overlap the cache.
+ * ---------------------------------------------------------------------- */
+int kda_ckpt_store_int8(const kda_cache *active, const void *src_rows, const void *dst_slots,
+                        int32_t idx_type, int64_t count, int8_t *qdata, float *scale, int64_t n_slots,
+                        void *stream);
+int kda_ckpt_load_int8(const int8_t *qdata, const float *scale, int64_t n_slots,
+                       const void *src_slots, const void *dst_rows, int32_t idx_type, int64_t count,
+                       const kda_cache *active, void *stream);
+
+/* ------------------------------------------------------------------------
  * kda_decode_step
  *
  * For each request r and head: with row = idx[r],

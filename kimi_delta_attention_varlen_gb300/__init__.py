@@ -25,7 +25,8 @@ from ._abi import (EXPORTED, KDA_BF16, KDA_F32, KDA_I32, KDA_I64, LIB_PATH, KdaC
 
 __all__ = [
     "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
-    "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc", "kda_decode_step", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
+    "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc", "kda_decode_step",
+    "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
     "KdaError", "EXPORTED", "LIB_PATH",
 ]
 
@@ -213,6 +214,41 @@ def kda_prefill_varlen_cached(q, k, v, g, beta, cu_seqlens, out, workspace, cach
         _itype_code(idx_in), _ptr(final_state), _ptr(checkpoints), ck_code, int(ckpt_every), slots, _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "kda_prefill_varlen_cached")
+
+
+def _ckpt_pools(cache, qdata, scale):
+    _, H, V, K = cache.shape
+    _need(qdata.dtype == torch.int8 and qdata.dim() == 4 and tuple(qdata.shape[1:]) == (H, V, K) and
+          qdata.is_contiguous(), "qdata must be a contiguous int8 [slots, H, V, K] tensor")
+    _need(scale.dtype == torch.float32 and tuple(scale.shape) == (qdata.shape[0], H, K) and scale.is_contiguous(),
+          "scale must be a contiguous float32 [slots, H, K] tensor")
+
+
+def kda_ckpt_store_int8(cache, src_rows, dst_slots, qdata, scale, stream=None) -> None:
+    """Quantise active cache rows src_rows[s] into int8 checkpoint slots dst_slots[s]:
+    per (slot, head, k) scale = max_v |x| / 127, codes round(x / scale) in [-127, 127]."""
+    d = cache_descriptor(cache)
+    _index_vector(src_rows)
+    _index_vector(dst_slots)
+    _need(src_rows.numel() == dst_slots.numel() and src_rows.dtype == dst_slots.dtype,
+          "src_rows and dst_slots: same length and dtype")
+    _ckpt_pools(cache, qdata, scale)
+    rc = lib().kda_ckpt_store_int8(ctypes.byref(d), _ptr(src_rows), _ptr(dst_slots), _itype_code(src_rows),
+                                   src_rows.numel(), _ptr(qdata), _ptr(scale), qdata.shape[0], _stream(stream))
+    _check(rc, "kda_ckpt_store_int8")
+
+
+def kda_ckpt_load_int8(qdata, scale, src_slots, cache, dst_rows, stream=None) -> None:
+    """Dequantise int8 checkpoint slots src_slots[s] into active cache rows dst_rows[s]."""
+    d = cache_descriptor(cache)
+    _index_vector(src_slots)
+    _index_vector(dst_rows)
+    _need(src_slots.numel() == dst_rows.numel() and src_slots.dtype == dst_rows.dtype,
+          "src_slots and dst_rows: same length and dtype")
+    _ckpt_pools(cache, qdata, scale)
+    rc = lib().kda_ckpt_load_int8(_ptr(qdata), _ptr(scale), qdata.shape[0], _ptr(src_slots), _ptr(dst_rows),
+                                  _itype_code(src_slots), src_slots.numel(), ctypes.byref(d), _stream(stream))
+    _check(rc, "kda_ckpt_load_int8")
 
 
 def kda_decode_step(q, k, v, g, beta, cache, idx, out, *, scale: float | None = None,

@@ -31,6 +31,8 @@ EXPORTED = (
     "kda_prefill_varlen_noalloc",
     "kda_prefill_varlen_cached",
     "kda_prefill_checkpoint_count",
+    "kda_ckpt_store_int8",
+    "kda_ckpt_load_int8",
     "kda_decode_step",
     "kda_status_string",
     "kda_last_cuda_error_string",
@@ -96,6 +98,10 @@ def lib():
         L.kda_prefill_varlen_cached.restype = ctypes.c_int
         L.kda_prefill_checkpoint_count.argtypes = [ctypes.POINTER(ctypes.c_int32), i64, i32]
         L.kda_prefill_checkpoint_count.restype = i64
+        L.kda_ckpt_store_int8.argtypes = [cache_p, vp, vp, i32, i64, vp, vp, i64, vp]
+        L.kda_ckpt_store_int8.restype = ctypes.c_int
+        L.kda_ckpt_load_int8.argtypes = [vp, vp, i64, vp, vp, i32, i64, cache_p, vp]
+        L.kda_ckpt_load_int8.restype = ctypes.c_int
         L.kda_decode_step.argtypes = [vp, vp, vp, i32, vp, vp, i64, i32, i32, i32, f32, i32, cache_p, vp, i32,
                                       vp, vp]
         L.kda_decode_step.restype = ctypes.c_int

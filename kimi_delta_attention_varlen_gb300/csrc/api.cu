@@ -251,6 +251,49 @@ int kda_decode_step(const void *q, const void *k, const void *v, int32_t io_dtyp
     return cuda_status(kda::launch_decode_step(a, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// Shared checks of the INT8 checkpoint calls: a built head size, 16-byte rows,
+// aligned index arrays and checkpoint buffers.
+int check_ckpt_args(const kda_cache *active, kda::CacheDesc *c, const void *src, const void *dst,
+                    int32_t idx_type, int64_t count, const void *qdata, const void *scale, int64_t n_slots)
+{
+    int rc = check_cache(active, c);
+    if (rc != KDA_OK) return rc;
+    if (!valid_itype(idx_type)) return KDA_ERR_DTYPE;
+    if (count < 0 || n_slots < 0) return KDA_ERR_SHAPE;
+    if (!built_head_size(static_cast<int32_t>(c->k), static_cast<int32_t>(c->v))) return KDA_ERR_UNSUPPORTED;
+    if (c->h > 65535) return KDA_ERR_RANGE;
+    if (count == 0) return KDA_OK;
+    if (count * c->h >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
+    if ((rc = check_index_array(src, idx_type)) != KDA_OK) return rc;
+    if ((rc = check_index_array(dst, idx_type)) != KDA_OK) return rc;
+    if (qdata == nullptr || scale == nullptr) return KDA_ERR_NULL;
+    if (!aligned(qdata, 16) || !aligned(scale, 16) || !aligned(c->data, 16)) return KDA_ERR_ALIGN;
+    if ((c->row_stride * esize(c->dtype)) % 16 != 0) return KDA_ERR_ALIGN;
+    return KDA_OK;
+}
+}  // namespace
+
+int kda_ckpt_store_int8(const kda_cache *active, const void *src_rows, const void *dst_slots, int32_t idx_type,
+                        int64_t count, int8_t *qdata, float *scale, int64_t n_slots, void *stream)
+{
+    kda::CacheDesc c{};
+    const int rc = check_ckpt_args(active, &c, src_rows, dst_slots, idx_type, count, qdata, scale, n_slots);
+    if (rc != KDA_OK || count == 0) return rc;
+    return cuda_status(kda::launch_ckpt_store_int8(c, src_rows, dst_slots, idx_type, count, qdata, scale, n_slots,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+int kda_ckpt_load_int8(const int8_t *qdata, const float *scale, int64_t n_slots, const void *src_slots,
+                       const void *dst_rows, int32_t idx_type, int64_t count, const kda_cache *active, void *stream)
+{
+    kda::CacheDesc c{};
+    const int rc = check_ckpt_args(active, &c, src_slots, dst_rows, idx_type, count, qdata, scale, n_slots);
+    if (rc != KDA_OK || count == 0) return rc;
+    return cuda_status(kda::launch_ckpt_load_int8(c, qdata, scale, n_slots, src_slots, dst_rows, idx_type, count,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
 const char *kda_status_string(int32_t status)
 {
     switch (status) {

@@ -38,6 +38,12 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode_step(const DecodeArgs &a, cudaStream_t st);
 
+// INT8 checkpoints; the cache's head size k (== v) is 32, 64 or 128.
+cudaError_t launch_ckpt_store_int8(const CacheDesc &c, const void *src, const void *dst, int32_t idx_type,
+                                   int64_t count, int8_t *qdata, float *scale, int64_t n_slots, cudaStream_t st);
+cudaError_t launch_ckpt_load_int8(const CacheDesc &c, const int8_t *qdata, const float *scale, int64_t n_slots,
+                                  const void *src, const void *dst, int32_t idx_type, int64_t count, cudaStream_t st);
+
 // Prefill workspace: a header (status word), the chunk table, and one record
 // per (chunk, head) holding the chunk's W, Q~, K~, A_qk, gamma and U^T.
 struct PrefillLayout {

@@ -179,6 +179,27 @@ def test_checkpoint_count(L):
     assert kda.kda_prefill_checkpoint_count([0, 256, 320], 64) == 5
 
 
+def test_int8_checkpoint_rejections(L):
+    c = cache(dtype=1)
+    st = L.kda_ckpt_store_int8
+    ld = L.kda_ckpt_load_int8
+    assert st(None, A, A, 0, 4, A, A, 4, None) == NULL
+    assert st(ctypes.byref(c), A, A, 3, 4, A, A, 4, None) == DTYPE
+    assert st(ctypes.byref(c), A, A, 0, -1, A, A, 4, None) == SHAPE
+    assert st(ctypes.byref(c), A, A, 0, 4, A, A, -1, None) == SHAPE
+    assert st(ctypes.byref(cache(v=16, k=32)), A, A, 0, 4, A, A, 4, None) == UNSUPPORTED
+    assert st(ctypes.byref(c), None, None, 0, 0, None, None, 4, None) == OK  # empty: nothing launched
+    assert st(ctypes.byref(c), None, A, 0, 4, A, A, 4, None) == NULL
+    assert st(ctypes.byref(c), A, A, 0, 4, None, A, 4, None) == NULL
+    assert st(ctypes.byref(c), A, A, 0, 4, A + 8, A, 4, None) == ALIGN
+    assert st(ctypes.byref(c), A, A, 0, 4, A, A + 4, 4, None) == ALIGN
+    assert st(ctypes.byref(cache(dtype=1, stride=2 * 32 * 32 + 4)), A, A, 0, 4, A, A, 4, None) == ALIGN
+    assert ld(A, A, 4, A, A, 0, 4, None, None) == NULL
+    assert ld(A, A, 4, A + 2, A, 0, 4, ctypes.byref(c), None) == ALIGN
+    assert ld(None, A, 4, A, A, 0, 4, ctypes.byref(c), None) == NULL
+    assert ld(A, A, 4, A, A, 0, 0, ctypes.byref(c), None) == OK
+
+
 def decode(L, c, **kw):
     a = dict(q=A, k=A, v=A, io=1, g=A, beta=A, R=8, h=2, dk=32, dv=32, scale=0.1, l2=1, idx=A, it=0, out=A)
     a.update(kw)
