@@ -81,6 +81,13 @@ def _load():
                                                   ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                   ctypes.c_int64, ctypes.c_int64]
             lib.oracle_ckpt_load_int8.restype = ctypes.c_int
+            lib.oracle_conv1d_varlen.argtypes = [_D, _I64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _D,
+                                                 _D, ctypes.c_int, _D, _D, _D]
+            lib.oracle_conv1d_varlen.restype = ctypes.c_int
+            lib.oracle_conv1d_update.argtypes = [_D, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _D, _D,
+                                                 ctypes.c_int, _VP, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                 _I64, _D]
+            lib.oracle_conv1d_update.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [_D, _D, _D, _D, _D, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
                                           ctypes.c_int, ctypes.c_double, _VP, ctypes.c_int,
@@ -245,6 +252,52 @@ def ckpt_load_int8(qdata: np.ndarray, scale: np.ndarray, src, dst, active_flat: 
                                        _dtype_code(active_flat), n_rows, row_stride, H, V, K)
     if rc != 0:
         raise ValueError(f"oracle_ckpt_load_int8 failed ({rc})")
+
+
+ACT = {"none": 0, "silu": 1}
+
+
+def conv1d_varlen(x, cu_seqlens, weight, bias=None, activation="none", init=None):
+    """Depthwise causal convolution over a varlen batch.  x: [T, C]; weight: [C, W];
+    bias: [C] or None; init: [B, W-1, C] or None.  Returns (y [T, C], final [B, W-1, C])."""
+    x, w = _f64(x), _f64(weight)
+    cu = _i64(cu_seqlens).reshape(-1)
+    T, C = x.shape
+    W = w.shape[1]
+    B = cu.size - 1
+    assert w.shape == (C, W) and cu[0] == 0 and cu[-1] == T
+    b = None if bias is None else _f64(bias)
+    ini = None if init is None else _f64(init)
+    if ini is not None:
+        assert ini.shape == (B, W - 1, C)
+    y = np.zeros((T, C), dtype=np.float64)
+    final = np.zeros((B, max(W - 1, 0), C), dtype=np.float64)
+    rc = _load().oracle_conv1d_varlen(_ptr(x, _D), _ptr(cu, _I64), B, C, W, _ptr(w, _D),
+                                      None if b is None else _ptr(b, _D), ACT[activation],
+                                      None if ini is None else _ptr(ini, _D), _ptr(y, _D), _ptr(final, _D))
+    if rc != 0:
+        raise ValueError(f"oracle_conv1d_varlen failed ({rc})")
+    return y, final
+
+
+def conv1d_update(x, weight, cache_flat: np.ndarray, n_rows: int, row_stride: int, idx, bias=None,
+                  activation="none"):
+    """One token per request on conv-state cache rows ([W-1, C] each, float32 or bf16 bits),
+    in place.  Returns y [R, C]."""
+    x, w = _f64(x), _f64(weight)
+    R, C = x.shape
+    W = w.shape[1]
+    assert cache_flat.flags.c_contiguous
+    idx = _i64(idx).reshape(-1)
+    assert idx.size == R
+    b = None if bias is None else _f64(bias)
+    y = np.zeros((R, C), dtype=np.float64)
+    rc = _load().oracle_conv1d_update(_ptr(x, _D), R, C, W, _ptr(w, _D), None if b is None else _ptr(b, _D),
+                                      ACT[activation], cache_flat.ctypes.data, _dtype_code(cache_flat), n_rows,
+                                      row_stride, _ptr(idx, _I64), _ptr(y, _D))
+    if rc != 0:
+        raise ValueError(f"oracle_conv1d_update failed ({rc})")
+    return y
 
 
 def decode(q, k, v, g, beta, cache_flat: np.ndarray, n_rows: int, row_stride: int, idx,

@@ -34,6 +34,17 @@
  *                   (Int8CheckpointStore): per (slot, head, k) a scale from
  *                   the max-abs over d_v, symmetric codes in [-127, 127];
  *                   loading multiplies back into an active state row.
+ *   oracle_conv1d_varlen / oracle_conv1d_update
+ *                   the short causal convolution applied to q, k and v
+ *                   before the recurrence (infra page, sections 6.5 and
+ *                   8.2.3: causal_conv1d_fn for prefill, causal_conv1d_update
+ *                   for decode, with a convolution state per request).  The
+ *                   pages give no formula; the textbook depthwise causal
+ *                   convolution is taken: per channel c and width W,
+ *                   y_t = act(bias_c + sum_{i<W} w[c][i] x_{t-(W-1)+i}),
+ *                   inputs before a sequence start coming from its state
+ *                   (the last W-1 inputs seen, oldest first; zeros when
+ *                   absent), act = identity or SiLU (y * sigmoid(y)).
  *   oracle_decode   one token of the same recurrence per request, reading
  *                   the state from a cache row by index and writing it back
  *                   in the cache dtype (the decode route named on the state
@@ -228,6 +239,70 @@ int oracle_ckpt_load_int8(const int8_t *qdata, const float *scale, int64_t n_slo
                     else ((uint16_t *)active)[e] = orc_f32_to_bf16(x);
                 }
     }
+    return 0;
+}
+
+/* ------------------------- short causal convolution ------------------------ */
+
+static double orc_act(double y, int act) { return act == 1 ? y / (1.0 + exp(-y)) : y; }
+
+/* x: [T, C]; cu_seqlens: [B + 1]; weight: [C, W] (weight[c][W-1] multiplies the
+ * current token); bias: [C] or NULL; init: [B, W-1, C] or NULL (zeros);
+ * y: [T, C]; final_state: [B, W-1, C] = the last W-1 inputs of each sequence's
+ * window, oldest first (init's rows when the sequence is shorter). */
+int oracle_conv1d_varlen(const double *x, const int64_t *cu_seqlens, int64_t B, int64_t C, int64_t W,
+                         const double *weight, const double *bias, int act, const double *init,
+                         double *y, double *final_state)
+{
+    if (B < 0 || C <= 0 || W < 1 || (act != 0 && act != 1)) return -1;
+    double *win = (double *)malloc(sizeof(double) * (size_t)W);
+    if (!win) return -2;
+    for (int64_t b = 0; b < B; ++b) {
+        if (cu_seqlens[b + 1] < cu_seqlens[b]) { free(win); return -1; }
+        for (int64_t c = 0; c < C; ++c) {
+            /* window = (state oldest .. newest, current); the state part first */
+            for (int64_t i = 0; i + 1 < W; ++i) win[i] = init ? init[(b * (W - 1) + i) * C + c] : 0.0;
+            for (int64_t t = cu_seqlens[b]; t < cu_seqlens[b + 1]; ++t) {
+                win[W - 1] = x[t * C + c];
+                double acc = bias ? bias[c] : 0.0;
+                for (int64_t i = 0; i < W; ++i) acc += weight[c * W + i] * win[i];
+                y[t * C + c] = orc_act(acc, act);
+                for (int64_t i = 0; i + 1 < W; ++i) win[i] = win[i + 1]; /* slide by one token */
+            }
+            for (int64_t i = 0; i + 1 < W; ++i) final_state[(b * (W - 1) + i) * C + c] = win[i];
+        }
+    }
+    free(win);
+    return 0;
+}
+
+/* One token per request on conv-state cache rows, in place: row idx[r] holds
+ * [W-1, C] (oldest first) in the cache dtype; an invalid index starts from
+ * zeros and writes nothing back.  x: [R, C]; y: [R, C]. */
+int oracle_conv1d_update(const double *x, int64_t R, int64_t C, int64_t W, const double *weight,
+                         const double *bias, int act, void *cache, int cache_dtype, int64_t n_rows,
+                         int64_t row_stride, const int64_t *idx, double *y)
+{
+    if (R < 0 || C <= 0 || W < 2 || (act != 0 && act != 1)) return -1;
+    if (cache_dtype != ORC_F32 && cache_dtype != ORC_BF16) return -1;
+    double *win = (double *)malloc(sizeof(double) * (size_t)W);
+    if (!win) return -2;
+    for (int64_t r = 0; r < R; ++r) {
+        const int64_t row = idx[r];
+        const int valid = row >= 0 && row < n_rows;
+        for (int64_t c = 0; c < C; ++c) {
+            for (int64_t i = 0; i + 1 < W; ++i)
+                win[i] = valid ? orc_load(cache, cache_dtype, row * row_stride + i * C + c) : 0.0;
+            win[W - 1] = x[r * C + c];
+            double acc = bias ? bias[c] : 0.0;
+            for (int64_t i = 0; i < W; ++i) acc += weight[c * W + i] * win[i];
+            y[r * C + c] = orc_act(acc, act);
+            if (valid)
+                for (int64_t i = 0; i + 1 < W; ++i)
+                    orc_store(cache, cache_dtype, row * row_stride + i * C + c, win[i + 1]);
+        }
+    }
+    free(win);
     return 0;
 }
 

@@ -604,3 +604,93 @@ def test_int8_checkpoint_power_of_two_scaling_keeps_codes():
     oracle.ckpt_store_int8((x * 8).reshape(-1).copy(), 1, V * K, H, V, K, [0], [0], q2, s2)
     np.testing.assert_array_equal(q1, q2)
     np.testing.assert_array_equal(s2, s1 * 8)
+
+
+# --------------------------------------------------------------------------
+# Short causal convolution
+# --------------------------------------------------------------------------
+
+def test_conv1d_single_channel_is_numpy_convolve():
+    """Zero state, no bias, identity: channel c of y is the first T terms of the full
+    convolution of x with the reversed kernel (numpy's textbook routine)."""
+    rng = np.random.default_rng(60)
+    T, C, W = 37, 3, 4
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, W))
+    y, _ = oracle.conv1d_varlen(x, [0, T], w)
+    for c in range(C):
+        np.testing.assert_allclose(y[:, c], np.convolve(x[:, c], w[c, ::-1])[:T], rtol=1e-12, atol=1e-12)
+
+
+def test_conv1d_impulse_response_and_bias():
+    T, C, W = 10, 2, 3
+    w = np.array([[1.0, 2.0, 3.0], [-1.0, 0.5, 4.0]])
+    x = np.zeros((T, C))
+    x[4] = 1.0
+    y, final = oracle.conv1d_varlen(x, [0, T], w, bias=np.array([0.25, -1.0]))
+    want = np.tile(np.array([0.25, -1.0]), (T, 1))
+    want[4] += w[:, 2]  # current-token tap first, then the older ones
+    want[5] += w[:, 1]
+    want[6] += w[:, 0]
+    np.testing.assert_array_equal(y, want)
+    np.testing.assert_array_equal(final[0], x[T - 2:])  # the last W-1 inputs, oldest first
+
+
+def test_conv1d_split_sequence_continues_through_its_state():
+    """Running a sequence in two parts, the first part's final state as the second's
+    initial state, gives the outputs and final state of one run (the state is exactly
+    the window the convolution needs)."""
+    rng = np.random.default_rng(61)
+    T, C, W = 23, 5, 4
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, W))
+    b = rng.standard_normal(C)
+    init = rng.standard_normal((1, W - 1, C))
+    y, f = oracle.conv1d_varlen(x, [0, T], w, bias=b, activation="silu", init=init)
+    for cut in (0, 1, 2, 9, T):
+        y1, f1 = oracle.conv1d_varlen(x[:cut], [0, cut], w, bias=b, activation="silu", init=init)
+        y2, f2 = oracle.conv1d_varlen(x[cut:], [0, T - cut], w, bias=b, activation="silu", init=f1)
+        np.testing.assert_allclose(np.concatenate([y1, y2]), y, rtol=1e-14, atol=1e-14)
+        np.testing.assert_array_equal(f2, f)
+
+
+def test_conv1d_short_and_empty_sequences_keep_older_state_rows():
+    W, C = 4, 2
+    init = np.arange(2 * 3 * C, dtype=np.float64).reshape(2, 3, C)
+    x = np.array([[100.0, 200.0]])
+    _, f = oracle.conv1d_varlen(x, [0, 1, 1], np.ones((C, W)), init=init)
+    np.testing.assert_array_equal(f[0], np.concatenate([init[0, 1:], x]))  # one token shifts in
+    np.testing.assert_array_equal(f[1], init[1])                          # empty: unchanged
+
+
+def test_conv1d_silu_closed_form():
+    x = np.array([[0.0], [1.0], [-2.0], [30.0]])
+    y, _ = oracle.conv1d_varlen(x, [0, 4], np.array([[0.0, 1.0]]), activation="silu")
+    want = x[:, 0] / (1.0 + np.exp(-x[:, 0]))
+    np.testing.assert_allclose(y[:, 0], want, rtol=1e-15)
+    assert y[0, 0] == 0.0 and abs(y[3, 0] - 30.0) < 1e-11
+
+
+def test_conv1d_update_equals_one_token_prefill():
+    rng = np.random.default_rng(62)
+    R, C, W = 3, 6, 4
+    w = rng.standard_normal((C, W))
+    b = rng.standard_normal(C)
+    x = rng.standard_normal((R, C)).astype(np.float32).astype(np.float64)
+    N, stride = 4, (W - 1) * C + 2
+    cache = np.zeros(N * stride, dtype=np.float32)
+    st = rng.standard_normal((N, W - 1, C)).astype(np.float32)
+    for r in range(N):
+        cache[r * stride:r * stride + (W - 1) * C] = st[r].reshape(-1)
+    idx = [2, -1, 0]
+    before = cache.copy()
+    y = oracle.conv1d_update(x, w, cache, N, stride, idx, bias=b, activation="silu")
+    init = np.stack([st[2], np.zeros((W - 1, C)), st[0]]).astype(np.float64)
+    y_ref, f_ref = oracle.conv1d_varlen(x, [0, 1, 2, 3], w, bias=b, activation="silu", init=init)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-14, atol=1e-14)
+    for r, row in ((0, 2), (2, 0)):
+        got = cache[row * stride:row * stride + (W - 1) * C].reshape(W - 1, C)
+        np.testing.assert_array_equal(got, f_ref[r].astype(np.float32))
+    for row in (1, 3):  # rows not addressed (and the invalid index) are untouched
+        np.testing.assert_array_equal(cache[row * stride:(row + 1) * stride], before[row * stride:(row + 1) * stride])
+    np.testing.assert_array_equal(cache[(W - 1) * C:stride], before[(W - 1) * C:stride])  # gap
