@@ -310,6 +310,41 @@ def ckpt_int8_measure(P, steps: int, warmup: int, pairs: int = 256) -> dict:
     return res
 
 
+def conv1d_measure(P, steps: int, warmup: int, W: int = 4) -> dict:
+    """The short causal convolution (width 4, SiLU, bf16 states) over the step's tokens
+    for q, k and v as one [T, 3 H D] bf16 buffer, with initial and final states; median
+    device time and GB/s of the compulsory bytes (x in, y out, states in and out)."""
+    import kimi_delta_attention_varlen_gb300 as kda
+    w = P["w"]
+    T, B = P["cu_list"][-1], w.B
+    C = 3 * w.H * w.K
+    dev = P["out"].device
+    g = torch.Generator(device=dev).manual_seed(31)
+    x = torch.randn(T, C, generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    wt = torch.randn(C, W, generator=g, device=dev) * 0.5
+    bias = torch.randn(C, generator=g, device=dev) * 0.1
+    init = torch.randn(B, W - 1, C, generator=g, device=dev).to(torch.bfloat16)
+    fin = torch.empty_like(init)
+
+    def call():
+        kda.kda_conv1d_varlen(x, P["cu"], wt, y, bias=bias, activation="silu", init_state=init, final_state=fin)
+    for _ in range(warmup):
+        call()
+    times = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    nbytes = 2 * T * C * 2 + 2 * B * (W - 1) * C * 2 + C * (W + 1) * 4
+    return {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes, "tokens_per_s": T / (ms * 1e-3),
+            "shape": f"x [{T}, {C}] bf16, width {W}, SiLU, bf16 states"}
+
+
 def copy_measure(dev, steps: int, warmup: int) -> dict:
     import kimi_delta_attention_varlen_gb300 as kda
     from kimi_delta_attention_varlen_gb300 import workloads as wl
@@ -472,6 +507,7 @@ def native(args, ranks: Ranks) -> dict | None:
     copy = copy_measure(dev, max(5, args.steps), max(3, args.warmup))
     fused = cached_measure(P, max(5, args.steps), max(3, args.warmup))
     ck8 = ckpt_int8_measure(P, max(5, args.steps), max(3, args.warmup))
+    conv = conv1d_measure(P, max(5, args.steps), max(3, args.warmup))
     pk, pk_kind = peaks()
     nb = prefill_bytes(P)
     flops = prefill_flops(P)
@@ -513,6 +549,7 @@ def native(args, ranks: Ranks) -> dict | None:
                        "scatter_frac": copy["scatter"]["gbs"] / pk["hbm_gbs"]},
         "decode": {"ms": br["decode"], "requests_per_s": P["dw"].R / (br["decode"] * 1e-3)},
         "cached_prefill": {**fused, "unfused_ms": br["gather"] + prefill_ms + br["scatter"]},
+        "conv1d": {**conv, "frac": conv["gbs"] / pk["hbm_gbs"]},
         "ckpt_int8": {**ck8, "store_frac": ck8["store"]["gbs"] / pk["hbm_gbs"],
                       "load_frac": ck8["load"]["gbs"] / pk["hbm_gbs"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},

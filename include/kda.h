@@ -294,6 +294,52 @@ int kda_prefill_varlen_noalloc(const void *q, const void *k, const void *v, int3
                                int32_t init_dtype, float *final_state, void *out, void *stream);
 
 /* ------------------------------------------------------------------------
+ * kda_conv1d_varlen / kda_conv1d_update
+ *
+ * The short causal convolution that q, k and v pass before the recurrence,
+ * with a convolution state per request ("KDA's challenges for AI infra",
+ * sections 6.5 and 8.2.3: causal_conv1d_fn in prefill, causal_conv1d_update
+ * in decode; the pages give no formula, the textbook depthwise causal
+ * convolution is used).  For channel c of width W (2..4):
+ *   y_t[c] = act(bias[c] + sum_{i<W} weight[c][i] * x_{t-(W-1)+i}[c]),
+ *   act = identity (activation 0) or SiLU y * sigmoid(y) (activation 1),
+ * where inputs before a sequence's first token come from its state: the last
+ * W-1 inputs, oldest first (zeros when no state is given).  fp32 arithmetic.
+ *
+ * kda_conv1d_varlen: over a cu_seqlens varlen batch (the prefill layout).
+ *   x, y         [total_tokens, channels] device, io_dtype (fp32 / bf16);
+ *                q, k and v may be convolved in one call as one buffer.
+ *   cu_seqlens   [num_seqs + 1] device int32 (monotone; precondition).
+ *   weight       [channels, W] device fp32 (weight[c][W-1] multiplies the
+ *                current token);  bias [channels] device fp32 or NULL.
+ *   init_state   [num_seqs, W-1, channels] device, state_dtype, or NULL.
+ *   final_state  [num_seqs, W-1, channels] device, state_dtype, or NULL:
+ *                each sequence's last W-1 inputs (an empty sequence keeps
+ *                its initial state); bf16 rounds to nearest even.
+ *   A state cache row [W-1, channels] is a kda_cache with h = 1, v = W-1,
+ *   k = channels, so kda_state_gather / kda_state_scatter move conv states
+ *   between cache rows and these packed buffers, as for the recurrence.
+ * kda_conv1d_update: one token per request on cache rows in place (decode):
+ *   x, y [batch, channels]; conv_cache rows [W-1, channels] (h == 1,
+ *   v == W-1, k == channels); idx [batch] int32 / int64.  A valid row is
+ *   read as the state and replaced by the state after the token; an invalid
+ *   index uses zeros and writes nothing.  Valid rows must be unique.
+ * channels must be a multiple of 8; all arrays 16-byte aligned (cu_seqlens
+ * and indices: their element size).  Errors: KDA_ERR_UNSUPPORTED for W
+ * outside 2..4, KDA_ERR_SHAPE for channels % 8 != 0, an unknown activation
+ * or a conv cache that does not match W and channels; the others as for the
+ * calls above.  Nothing is launched on an error; batch == 0 launches nothing.
+ * ---------------------------------------------------------------------- */
+int kda_conv1d_varlen(const void *x, int32_t io_dtype, const int32_t *cu_seqlens, int64_t num_seqs,
+                      int64_t total_tokens, int64_t channels, int32_t width, const float *weight,
+                      const float *bias, int32_t activation, const void *init_state, void *final_state,
+                      int32_t state_dtype, void *y, void *stream);
+int kda_conv1d_update(const void *x, int32_t io_dtype, int64_t batch, int64_t channels, int32_t width,
+                      const float *weight, const float *bias, int32_t activation,
+                      const kda_cache *conv_cache, const void *idx, int32_t idx_type, void *y,
+                      void *stream);
+
+/* ------------------------------------------------------------------------
  * kda_ckpt_store_int8 / kda_ckpt_load_int8
  *
  * INT8 checkpoints of recurrent states, the Int8CheckpointStore of the

@@ -26,7 +26,7 @@ from ._abi import (EXPORTED, KDA_BF16, KDA_F32, KDA_I32, KDA_I64, LIB_PATH, KdaC
 __all__ = [
     "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
     "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc", "kda_decode_step",
-    "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
+    "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_conv1d_varlen", "kda_conv1d_update", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
     "KdaError", "EXPORTED", "LIB_PATH",
 ]
 
@@ -214,6 +214,58 @@ def kda_prefill_varlen_cached(q, k, v, g, beta, cu_seqlens, out, workspace, cach
         _itype_code(idx_in), _ptr(final_state), _ptr(checkpoints), ck_code, int(ckpt_every), slots, _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "kda_prefill_varlen_cached")
+
+
+_ACT = {"none": 0, "silu": 1}
+
+
+def _conv_weights(weight, bias, C):
+    _need(weight.dtype == torch.float32 and weight.dim() == 2 and weight.shape[0] == C and weight.is_contiguous(),
+          "weight must be a contiguous float32 [C, W] tensor")
+    if bias is not None:
+        _need(bias.dtype == torch.float32 and tuple(bias.shape) == (C,) and bias.is_contiguous(),
+              "bias must be a contiguous float32 [C] tensor")
+    return weight.shape[1]
+
+
+def kda_conv1d_varlen(x, cu_seqlens, weight, y, *, bias=None, activation: str = "none", init_state=None,
+                      final_state=None, stream=None) -> None:
+    """Depthwise causal convolution over a varlen batch: x, y [T, C] (bf16 / fp32);
+    weight [C, W] fp32; bias [C] fp32 or None; init/final states [B, W-1, C] (fp32 / bf16,
+    one dtype) or None."""
+    T, C = x.shape
+    B = cu_seqlens.numel() - 1
+    W = _conv_weights(weight, bias, C)
+    _need(tuple(y.shape) == (T, C) and y.dtype == x.dtype and x.is_contiguous() and y.is_contiguous(),
+          "x and y must be contiguous [T, C] tensors of one dtype")
+    _need(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous() and B >= 1,
+          "cu_seqlens must be a contiguous int32 tensor of B + 1 >= 2 offsets")
+    st_code = 0
+    for name, t in (("init_state", init_state), ("final_state", final_state)):
+        if t is not None:
+            _need(tuple(t.shape) == (B, W - 1, C) and t.is_contiguous(), f"{name} must be contiguous [B, W-1, C]")
+            st_code = _dtype_code(t)
+    if init_state is not None and final_state is not None:
+        _need(init_state.dtype == final_state.dtype, "init_state and final_state share a dtype")
+    rc = lib().kda_conv1d_varlen(_ptr(x), _dtype_code(x), _ptr(cu_seqlens), B, T, C, W, _ptr(weight), _ptr(bias),
+                                 _ACT[activation], _ptr(init_state), _ptr(final_state), st_code, _ptr(y),
+                                 _stream(stream))
+    _check(rc, "kda_conv1d_varlen")
+
+
+def kda_conv1d_update(x, weight, conv_cache, idx, y, *, bias=None, activation: str = "none", stream=None) -> None:
+    """One token per request on conv-state cache rows in place: x, y [R, C]; conv_cache a
+    [N, 1, W-1, C] view (rows of W-1 states, oldest first); idx [R] int32/int64."""
+    R, C = x.shape
+    W = _conv_weights(weight, bias, C)
+    _need(tuple(y.shape) == (R, C) and y.dtype == x.dtype and x.is_contiguous() and y.is_contiguous(),
+          "x and y must be contiguous [R, C] tensors of one dtype")
+    _index_vector(idx)
+    _need(idx.numel() == R, "idx must hold one index per request")
+    d = cache_descriptor(conv_cache)
+    rc = lib().kda_conv1d_update(_ptr(x), _dtype_code(x), R, C, W, _ptr(weight), _ptr(bias), _ACT[activation],
+                                 ctypes.byref(d), _ptr(idx), _itype_code(idx), _ptr(y), _stream(stream))
+    _check(rc, "kda_conv1d_update")
 
 
 def _ckpt_pools(cache, qdata, scale):

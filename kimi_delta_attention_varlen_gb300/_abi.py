@@ -31,6 +31,8 @@ EXPORTED = (
     "kda_prefill_varlen_noalloc",
     "kda_prefill_varlen_cached",
     "kda_prefill_checkpoint_count",
+    "kda_conv1d_varlen",
+    "kda_conv1d_update",
     "kda_ckpt_store_int8",
     "kda_ckpt_load_int8",
     "kda_decode_step",
@@ -98,6 +100,10 @@ def lib():
         L.kda_prefill_varlen_cached.restype = ctypes.c_int
         L.kda_prefill_checkpoint_count.argtypes = [ctypes.POINTER(ctypes.c_int32), i64, i32]
         L.kda_prefill_checkpoint_count.restype = i64
+        L.kda_conv1d_varlen.argtypes = [vp, i32, vp, i64, i64, i64, i32, vp, vp, i32, vp, vp, i32, vp, vp]
+        L.kda_conv1d_varlen.restype = ctypes.c_int
+        L.kda_conv1d_update.argtypes = [vp, i32, i64, i64, i32, vp, vp, i32, cache_p, vp, i32, vp, vp]
+        L.kda_conv1d_update.restype = ctypes.c_int
         L.kda_ckpt_store_int8.argtypes = [cache_p, vp, vp, i32, i64, vp, vp, i64, vp]
         L.kda_ckpt_store_int8.restype = ctypes.c_int
         L.kda_ckpt_load_int8.argtypes = [vp, vp, i64, vp, vp, i32, i64, cache_p, vp]

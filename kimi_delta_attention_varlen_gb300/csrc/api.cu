@@ -294,6 +294,65 @@ int kda_ckpt_load_int8(const int8_t *qdata, const float *scale, int64_t n_slots,
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+int check_conv_common(const void *x, int32_t io_dtype, int64_t channels, int32_t width, const float *weight,
+                      const float *bias, int32_t activation, const void *y)
+{
+    if (!valid_dtype(io_dtype)) return KDA_ERR_DTYPE;
+    if (width < 2 || width > 4 || channels < 1) return KDA_ERR_UNSUPPORTED;
+    if (channels % 8 != 0) return KDA_ERR_SHAPE;
+    if (activation != 0 && activation != 1) return KDA_ERR_SHAPE;
+    if (channels > (INT64_C(1) << 30)) return KDA_ERR_RANGE;
+    if (weight == nullptr) return KDA_ERR_NULL;
+    const void *vec16[] = {x, weight, bias, y};
+    for (const void *p : vec16)
+        if (p != nullptr && !aligned(p, 16)) return KDA_ERR_ALIGN;
+    return KDA_OK;
+}
+}  // namespace
+
+int kda_conv1d_varlen(const void *x, int32_t io_dtype, const int32_t *cu_seqlens, int64_t num_seqs,
+                      int64_t total_tokens, int64_t channels, int32_t width, const float *weight, const float *bias,
+                      int32_t activation, const void *init_state, void *final_state, int32_t state_dtype, void *y,
+                      void *stream)
+{
+    int rc = check_conv_common(x, io_dtype, channels, width, weight, bias, activation, y);
+    if (rc != KDA_OK) return rc;
+    if ((init_state != nullptr || final_state != nullptr) && !valid_dtype(state_dtype)) return KDA_ERR_DTYPE;
+    if (num_seqs < 1 || total_tokens < 0) return KDA_ERR_SHAPE;
+    if (num_seqs >= (INT64_C(1) << 30) || total_tokens >= (INT64_C(1) << 36)) return KDA_ERR_RANGE;
+    if ((total_tokens + 15) / 16 >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
+    if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+    if (total_tokens > 0 && (x == nullptr || y == nullptr)) return KDA_ERR_NULL;
+    if (!aligned(cu_seqlens, 4)) return KDA_ERR_ALIGN;
+    const void *st16[] = {init_state, final_state};
+    for (const void *p : st16)
+        if (p != nullptr && !aligned(p, 16)) return KDA_ERR_ALIGN;
+    kda::Conv1dArgs a{x, io_dtype, cu_seqlens, num_seqs, total_tokens, channels, width, weight, bias, activation,
+                      init_state, final_state, state_dtype, y};
+    return cuda_status(kda::launch_conv1d_varlen(a, static_cast<cudaStream_t>(stream)));
+}
+
+int kda_conv1d_update(const void *x, int32_t io_dtype, int64_t batch, int64_t channels, int32_t width,
+                      const float *weight, const float *bias, int32_t activation, const kda_cache *conv_cache,
+                      const void *idx, int32_t idx_type, void *y, void *stream)
+{
+    kda::CacheDesc c{};
+    int rc = check_cache(conv_cache, &c);
+    if (rc != KDA_OK) return rc;
+    if ((rc = check_conv_common(x, io_dtype, channels, width, weight, bias, activation, y)) != KDA_OK) return rc;
+    if (!valid_itype(idx_type)) return KDA_ERR_DTYPE;
+    if (c.h != 1 || c.v != width - 1 || c.k != channels) return KDA_ERR_SHAPE;
+    if (batch < 0) return KDA_ERR_SHAPE;
+    if (batch == 0) return KDA_OK;
+    if (batch >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
+    if ((rc = check_index_array(idx, idx_type)) != KDA_OK) return rc;
+    if (x == nullptr || y == nullptr) return KDA_ERR_NULL;
+    if (!aligned(c.data, 16) || (c.row_stride * esize(c.dtype)) % 16 != 0) return KDA_ERR_ALIGN;
+    kda::Conv1dUpdateArgs a{x, io_dtype, batch, channels, width, weight, bias, activation, c, idx, idx_type, y};
+    return cuda_status(kda::launch_conv1d_update(a, static_cast<cudaStream_t>(stream)));
+}
+
 const char *kda_status_string(int32_t status)
 {
     switch (status) {

@@ -38,6 +38,36 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode_step(const DecodeArgs &a, cudaStream_t st);
 
+// Short causal convolution (width 2..4, channels a multiple of 8).
+struct Conv1dArgs {
+    const void *x;
+    int32_t io_dtype;
+    const int32_t *cu_seqlens;
+    int64_t num_seqs, total_tokens, channels;
+    int32_t width;
+    const float *weight, *bias;
+    int32_t activation;
+    const void *init_state;
+    void *final_state;
+    int32_t state_dtype;
+    void *y;
+};
+cudaError_t launch_conv1d_varlen(const Conv1dArgs &a, cudaStream_t st);
+
+struct Conv1dUpdateArgs {
+    const void *x;
+    int32_t io_dtype;
+    int64_t batch, channels;
+    int32_t width;
+    const float *weight, *bias;
+    int32_t activation;
+    CacheDesc cache;
+    const void *idx;
+    int32_t idx_type;
+    void *y;
+};
+cudaError_t launch_conv1d_update(const Conv1dUpdateArgs &a, cudaStream_t st);
+
 // INT8 checkpoints; the cache's head size k (== v) is 32, 64 or 128.
 cudaError_t launch_ckpt_store_int8(const CacheDesc &c, const void *src, const void *dst, int32_t idx_type,
                                    int64_t count, int8_t *qdata, float *scale, int64_t n_slots, cudaStream_t st);
