@@ -88,6 +88,12 @@ def _load():
                                                  ctypes.c_int, _VP, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                                  _I64, _D]
             lib.oracle_conv1d_update.restype = ctypes.c_int
+            lib.oracle_target_verify.argtypes = [_D, _D, _D, _D, _D, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
+                                                 ctypes.c_int, ctypes.c_double, _VP, ctypes.c_int, ctypes.c_int64,
+                                                 ctypes.c_int64, _I64, _VP, ctypes.c_int, ctypes.c_int64,
+                                                 ctypes.c_int64, _I64, _D, ctypes.c_int]
+            lib.oracle_target_verify.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [_D, _D, _D, _D, _D, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
                                           ctypes.c_int, ctypes.c_double, _VP, ctypes.c_int,
@@ -298,6 +304,31 @@ def conv1d_update(x, weight, cache_flat: np.ndarray, n_rows: int, row_stride: in
     if rc != 0:
         raise ValueError(f"oracle_conv1d_update failed ({rc})")
     return y
+
+
+def target_verify(q, k, v, g, beta, cache_flat: np.ndarray, n_rows: int, row_stride: int, idx,
+                  pool_flat: np.ndarray, pool_rows: int, pool_stride: int, inter_idx, scale=1.0, l2norm=True,
+                  eps=EPS, nthreads=None):
+    """L draft tokens per request from cache row idx[r] (read only); the state after token t
+    of request r goes to pool row inter_idx[r, t] (float32 or bf16 bits; rows of pool_stride
+    elements holding [H, V, K]), in place.  q, k, g: [R, L, H, K]; v: [R, L, H, V];
+    beta: [R, L, H].  Returns out [R, L, H, V]."""
+    q, k, v, g, beta = (_f64(a) for a in (q, k, v, g, beta))
+    R, L, H, K = q.shape
+    V = v.shape[3]
+    assert cache_flat.flags.c_contiguous and pool_flat.flags.c_contiguous
+    idx = _i64(idx).reshape(-1)
+    ii = _i64(inter_idx).reshape(-1)
+    assert idx.size == R and ii.size == R * L
+    out = np.zeros((R, L, H, V), dtype=np.float64)
+    rc = _load().oracle_target_verify(_ptr(q, _D), _ptr(k, _D), _ptr(v, _D), _ptr(g, _D), _ptr(beta, _D), R, L,
+                                      H, K, V, float(scale), 1 if l2norm else 0, float(eps), cache_flat.ctypes.data,
+                                      _dtype_code(cache_flat), n_rows, row_stride, _ptr(idx, _I64),
+                                      pool_flat.ctypes.data, _dtype_code(pool_flat), pool_rows, pool_stride,
+                                      _ptr(ii, _I64), _ptr(out, _D), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_target_verify failed ({rc})")
+    return out
 
 
 def decode(q, k, v, g, beta, cache_flat: np.ndarray, n_rows: int, row_stride: int, idx,

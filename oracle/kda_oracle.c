@@ -45,6 +45,15 @@
  *                   inputs before a sequence start coming from its state
  *                   (the last W-1 inputs seen, oldest first; zeros when
  *                   absent), act = identity or SiLU (y * sigmoid(y)).
+ *   oracle_target_verify
+ *                   speculative target verification (infra page, section
+ *                   6.4, target_verify, and 6.5's verify intermediate state
+ *                   indices): L draft tokens per request run through the
+ *                   recurrence from the request's cached state, the output of
+ *                   every token is returned and the state after each token
+ *                   goes to its own slot of an intermediate-state pool; the
+ *                   cached state itself is not changed (a caller commits the
+ *                   accepted prefix by copying one intermediate slot).
  *   oracle_decode   one token of the same recurrence per request, reading
  *                   the state from a cache row by index and writing it back
  *                   in the cache dtype (the decode route named on the state
@@ -522,6 +531,75 @@ static void *orc_decode_worker(void *arg)
 /* One decode token per request on cache rows, in place.  q, k, g: [R, H, K];
  * v: [R, H, V]; beta: [R, H]; cache: n_rows rows of row_stride elements, each
  * holding [H, V, K]; idx: [R]; out: [R, H, V].  Valid indices must be unique. */
+typedef struct {
+    const double *q, *k, *v, *g, *beta;
+    int64_t R, L, H, K, V;
+    double scale, eps;
+    int l2norm;
+    const void *cache;
+    int cache_dtype;
+    int64_t n_rows, row_stride;
+    const int64_t *idx;
+    void *pool;
+    int pool_dtype;
+    int64_t pool_rows, pool_stride;
+    const int64_t *inter_idx; /* [R, L] */
+    double *out;              /* [R, L, H, V] */
+    int64_t n_items, next;
+} orc_verify_job;
+
+static void *orc_verify_worker(void *arg)
+{
+    orc_verify_job *a = (orc_verify_job *)arg;
+    const int64_t H = a->H, K = a->K, V = a->V, L = a->L;
+    double *S = (double *)malloc(sizeof(double) * (size_t)(K * V + 2 * K + V));
+    if (!S) return (void *)1;
+    double *qn = S + K * V, *kn = qn + K, *p = kn + K;
+    for (;;) {
+        const int64_t item = __atomic_fetch_add(&a->next, 1, __ATOMIC_RELAXED);
+        if (item >= a->n_items) break;
+        const int64_t r = item / H, h = item % H;
+        const int64_t row = a->idx[r];
+        const int valid = row >= 0 && row < a->n_rows;
+        for (int64_t j = 0; j < V; ++j)
+            for (int64_t c = 0; c < K; ++c)
+                S[c * V + j] = valid ? orc_load(a->cache, a->cache_dtype, row * a->row_stride + (h * V + j) * K + c)
+                                     : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t tok = r * L + t;
+            orc_token_step(S, K, V, a->q + (tok * H + h) * K, a->k + (tok * H + h) * K, a->v + (tok * H + h) * V,
+                           a->g + (tok * H + h) * K, a->beta[tok * H + h], a->scale, a->l2norm, a->eps,
+                           a->out + (tok * H + h) * V, qn, kn, p);
+            const int64_t slot = a->inter_idx[tok];
+            if (slot >= 0 && slot < a->pool_rows)
+                for (int64_t j = 0; j < V; ++j)
+                    for (int64_t c = 0; c < K; ++c)
+                        orc_store(a->pool, a->pool_dtype, slot * a->pool_stride + (h * V + j) * K + c, S[c * V + j]);
+        }
+    }
+    free(S);
+    return NULL;
+}
+
+/* L tokens per request from cache row idx[r] (zeros when invalid; the cache is
+ * only read).  q, k, g: [R, L, H, K]; v: [R, L, H, V]; beta: [R, L, H];
+ * inter_idx: [R, L] pool rows (invalid: not written); out: [R, L, H, V]. */
+int oracle_target_verify(const double *q, const double *k, const double *v, const double *g,
+                         const double *beta, int64_t R, int64_t L, int64_t H, int64_t K, int64_t V,
+                         double scale, int l2norm, double eps, const void *cache, int cache_dtype,
+                         int64_t n_rows, int64_t row_stride, const int64_t *idx, void *pool, int pool_dtype,
+                         int64_t pool_rows, int64_t pool_stride, const int64_t *inter_idx, double *out,
+                         int nthreads)
+{
+    if (R < 0 || L < 1 || H <= 0 || K <= 0 || V <= 0 || n_rows <= 0 || row_stride < H * V * K) return -1;
+    if (pool_rows < 0 || pool_stride < H * V * K) return -1;
+    if ((cache_dtype != ORC_F32 && cache_dtype != ORC_BF16) || (pool_dtype != ORC_F32 && pool_dtype != ORC_BF16))
+        return -1;
+    orc_verify_job a = {q, k, v, g, beta, R, L, H, K, V, scale, eps, l2norm, cache, cache_dtype, n_rows,
+                        row_stride, idx, pool, pool_dtype, pool_rows, pool_stride, inter_idx, out, R * H, 0};
+    return orc_run_threads(orc_verify_worker, &a, nthreads);
+}
+
 int oracle_decode(const double *q, const double *k, const double *v, const double *g,
                   const double *beta, int64_t R, int64_t H, int64_t K, int64_t V, double scale,
                   int l2norm, double eps, void *cache, int cache_dtype, int64_t n_rows,

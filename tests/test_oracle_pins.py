@@ -694,3 +694,42 @@ def test_conv1d_update_equals_one_token_prefill():
     for row in (1, 3):  # rows not addressed (and the invalid index) are untouched
         np.testing.assert_array_equal(cache[row * stride:(row + 1) * stride], before[row * stride:(row + 1) * stride])
     np.testing.assert_array_equal(cache[(W - 1) * C:stride], before[(W - 1) * C:stride])  # gap
+
+
+# --------------------------------------------------------------------------
+# Speculative target verification
+# --------------------------------------------------------------------------
+
+def test_target_verify_is_prefill_with_per_token_states():
+    """Verifying L tokens equals prefilling them from the cached state: the same outputs,
+    intermediate state t = the checkpoint after t + 1 tokens; the cache is left as it was."""
+    rng = np.random.default_rng(70)
+    R, L, H, K, V = 3, 5, 2, 6, 4
+    q, k, v, g, beta, _ = rand_tokens(71, [R * L], H, K, V)
+    N, stride = 4, H * V * K + 3
+    cache = rng.standard_normal(N * stride).astype(np.float32)
+    before = cache.copy()
+    idx = [2, -1, 0]
+    P, pstride = 20, H * V * K
+    pool = np.full(P * pstride, 7.0, dtype=np.float32)
+    inter = np.arange(R * L).reshape(R, L)
+    inter[1, 2] = -1      # an invalid slot: not written
+    inter[2, 4] = P + 3
+    sh = lambda a: a.reshape(R, L, *a.shape[1:])  # noqa: E731
+    out = oracle.target_verify(sh(q), sh(k), sh(v), sh(g), sh(beta), cache, N, stride, idx, pool, P, pstride,
+                               inter, scale=0.5)
+    np.testing.assert_array_equal(cache, before)
+    init = np.zeros((R, H, V, K))
+    for r, row in enumerate(idx):
+        if row >= 0:
+            init[r] = cache[row * stride:row * stride + H * V * K].reshape(H, V, K)
+    cu = np.arange(0, R * L + 1, L)
+    o_ref, _, ck = oracle.prefill_ckpt(q, k, v, g, beta, cu, 1, init=init, scale=0.5)
+    np.testing.assert_allclose(out.reshape(R * L, H, V), o_ref, rtol=1e-12, atol=1e-12)
+    for r in range(R):
+        for t in range(L):
+            s = inter[r, t]
+            if 0 <= s < P:
+                got = pool[s * pstride:(s + 1) * pstride].reshape(H, V, K)
+                np.testing.assert_array_equal(got, ck[r * L + t].astype(np.float32))
+    np.testing.assert_array_equal(pool[7 * pstride:8 * pstride], np.full(pstride, 7.0, np.float32))  # slot of (1, 2)
