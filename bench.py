@@ -345,6 +345,44 @@ def conv1d_measure(P, steps: int, warmup: int, W: int = 4) -> dict:
             "shape": f"x [{T}, {C}] bf16, width {W}, SiLU, bf16 states"}
 
 
+def verify_measure(P, steps: int, warmup: int, L: int = 4) -> dict:
+    """Speculative target verification of L draft tokens for the decode workload's
+    requests (bf16 cache [2048, 32, 128, 128], R = 512): every token's state to its own
+    bf16 pool slot.  Median device time; GB/s of the compulsory bytes (states read once,
+    L intermediate states written, token inputs and outputs)."""
+    import kimi_delta_attention_varlen_gb300 as kda
+    from kimi_delta_attention_varlen_gb300 import workloads as wl
+    dw, pc = P["dw"], P["cache5"]
+    R, H, K, V = dw.R, dw.H, dw.K, dw.V
+    dev = P["out"].device
+    t = wl.token_inputs(R * L, H, K, V, dw.io_dtype, seed=41, device=dev)
+    inp = {n: x.view(R, L, *x.shape[1:]) for n, x in t.items()}
+    pool = torch.empty(R * L, H, V, K, dtype=pc.view.dtype, device=dev)
+    inter = torch.arange(R * L, dtype=torch.int32, device=dev).view(R, L)
+    out = torch.empty(R, L, H, V, dtype=dw.io_dtype, device=dev)
+
+    def call():
+        kda.kda_target_verify(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], pc.view, P["didx"], pool, inter,
+                              out)
+    for _ in range(warmup):
+        call()
+    times = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    valid = int((dw.idx >= 0).sum())
+    st = H * V * K * pc.view.element_size()
+    io = R * L * H * (3 * K * 2 + K * 4 + 4 + V * 2)
+    nbytes = valid * st + R * L * st + io
+    return {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes, "draft_tokens": L, "requests": R,
+            "tokens_per_s": R * L / (ms * 1e-3)}
+
+
 def copy_measure(dev, steps: int, warmup: int) -> dict:
     import kimi_delta_attention_varlen_gb300 as kda
     from kimi_delta_attention_varlen_gb300 import workloads as wl
@@ -508,6 +546,7 @@ def native(args, ranks: Ranks) -> dict | None:
     fused = cached_measure(P, max(5, args.steps), max(3, args.warmup))
     ck8 = ckpt_int8_measure(P, max(5, args.steps), max(3, args.warmup))
     conv = conv1d_measure(P, max(5, args.steps), max(3, args.warmup))
+    ver = verify_measure(P, max(5, args.steps), max(3, args.warmup))
     pk, pk_kind = peaks()
     nb = prefill_bytes(P)
     flops = prefill_flops(P)
@@ -550,6 +589,7 @@ def native(args, ranks: Ranks) -> dict | None:
         "decode": {"ms": br["decode"], "requests_per_s": P["dw"].R / (br["decode"] * 1e-3)},
         "cached_prefill": {**fused, "unfused_ms": br["gather"] + prefill_ms + br["scatter"]},
         "conv1d": {**conv, "frac": conv["gbs"] / pk["hbm_gbs"]},
+        "target_verify": {**ver, "frac": ver["gbs"] / pk["hbm_gbs"]},
         "ckpt_int8": {**ck8, "store_frac": ck8["store"]["gbs"] / pk["hbm_gbs"],
                       "load_frac": ck8["load"]["gbs"] / pk["hbm_gbs"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},

@@ -294,6 +294,34 @@ int kda_prefill_varlen_noalloc(const void *q, const void *k, const void *v, int3
                                int32_t init_dtype, float *final_state, void *out, void *stream);
 
 /* ------------------------------------------------------------------------
+ * kda_target_verify
+ *
+ * Speculative target verification ("KDA's challenges for AI infra", section
+ * 6.4, target_verify, and 6.5, verify intermediate state indices): for each
+ * request r, L draft tokens run through the recurrence of kda_decode_step
+ * from S = cache row idx[r] (zeros for an invalid index); token t's output
+ * goes to out[r][t] and the state after token t to row inter_idx[r][t] of
+ * the intermediate-state pool (converted to the pool dtype; an invalid slot
+ * is not written).  The cache is only read: a caller commits the accepted
+ * prefix of n tokens by copying pool row inter_idx[r][n-1] into the cache
+ * (kda_state_gather / kda_state_scatter).
+ *
+ *   q, k, g     [batch, L, h, dk] device (q, k io_dtype; g fp32)
+ *   v, out      [batch, L, h, dv] device, io_dtype;  beta [batch, L, h] fp32
+ *   cache, pool state caches with ->h == h, ->v == dv, ->k == dk; data and
+ *               row strides 16-byte aligned; fp32 or bf16 each
+ *   idx         [batch];  inter_idx [batch, L];  idx_type int32 / int64
+ *   dk == dv in {32, 64, 128}.  Valid pool slots must be unique and must not
+ *   alias cache rows that are read (preconditions, not checked).
+ *   batch == 0 validates the metadata and launches nothing.
+ * ---------------------------------------------------------------------- */
+int kda_target_verify(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,
+                      const float *beta, int64_t batch, int32_t L, int32_t h, int32_t dk, int32_t dv,
+                      float scale, int32_t qk_l2norm, const kda_cache *cache, const void *idx,
+                      const kda_cache *pool, const void *inter_idx, int32_t idx_type, void *out,
+                      void *stream);
+
+/* ------------------------------------------------------------------------
  * kda_conv1d_varlen / kda_conv1d_update
  *
  * The short causal convolution that q, k and v pass before the recurrence,

@@ -26,7 +26,7 @@ from ._abi import (EXPORTED, KDA_BF16, KDA_F32, KDA_I32, KDA_I64, LIB_PATH, KdaC
 __all__ = [
     "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
     "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc", "kda_decode_step",
-    "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_conv1d_varlen", "kda_conv1d_update", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
+    "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_conv1d_varlen", "kda_conv1d_update", "kda_target_verify", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
     "KdaError", "EXPORTED", "LIB_PATH",
 ]
 
@@ -214,6 +214,31 @@ def kda_prefill_varlen_cached(q, k, v, g, beta, cu_seqlens, out, workspace, cach
         _itype_code(idx_in), _ptr(final_state), _ptr(checkpoints), ck_code, int(ckpt_every), slots, _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "kda_prefill_varlen_cached")
+
+
+def kda_target_verify(q, k, v, g, beta, cache, idx, pool, inter_idx, out, *, scale: float | None = None,
+                      qk_l2norm: bool = True, stream=None) -> None:
+    """L draft tokens per request from cache rows idx[r] (read only); outputs to out and the
+    state after token t of request r to pool row inter_idx[r, t].  q, k, g: [R, L, H, K];
+    v, out: [R, L, H, V]; beta: [R, L, H]; cache, pool: [N, H, V, K] views."""
+    R, L, H, K = q.shape
+    V = v.shape[3]
+    for name, t, shape in (("q", q, (R, L, H, K)), ("k", k, (R, L, H, K)), ("v", v, (R, L, H, V)),
+                           ("out", out, (R, L, H, V)), ("g", g, (R, L, H, K)), ("beta", beta, (R, L, H))):
+        _need(tuple(t.shape) == shape and t.is_contiguous(), f"{name} must be contiguous {shape}")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype and out.dtype == q.dtype, "q, k, v, out share a dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g and beta must be float32")
+    _index_vector(idx)
+    _need(idx.numel() == R, "idx must hold one index per request")
+    _need(inter_idx.is_contiguous() and tuple(inter_idx.shape) == (R, L) and inter_idx.dtype == idx.dtype,
+          "inter_idx must be a contiguous [R, L] tensor of idx's dtype")
+    dc, dp = cache_descriptor(cache), cache_descriptor(pool)
+    if scale is None:
+        scale = K ** -0.5
+    rc = lib().kda_target_verify(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g), _ptr(beta), R, L, H, K, V,
+                                 float(scale), 1 if qk_l2norm else 0, ctypes.byref(dc), _ptr(idx), ctypes.byref(dp),
+                                 _ptr(inter_idx), _itype_code(idx), _ptr(out), _stream(stream))
+    _check(rc, "kda_target_verify")
 
 
 _ACT = {"none": 0, "silu": 1}

@@ -31,6 +31,7 @@ EXPORTED = (
     "kda_prefill_varlen_noalloc",
     "kda_prefill_varlen_cached",
     "kda_prefill_checkpoint_count",
+    "kda_target_verify",
     "kda_conv1d_varlen",
     "kda_conv1d_update",
     "kda_ckpt_store_int8",
@@ -100,6 +101,9 @@ def lib():
         L.kda_prefill_varlen_cached.restype = ctypes.c_int
         L.kda_prefill_checkpoint_count.argtypes = [ctypes.POINTER(ctypes.c_int32), i64, i32]
         L.kda_prefill_checkpoint_count.restype = i64
+        L.kda_target_verify.argtypes = [vp, vp, vp, i32, vp, vp, i64, i32, i32, i32, i32, f32, i32, cache_p, vp,
+                                        cache_p, vp, i32, vp, vp]
+        L.kda_target_verify.restype = ctypes.c_int
         L.kda_conv1d_varlen.argtypes = [vp, i32, vp, i64, i64, i64, i32, vp, vp, i32, vp, vp, i32, vp, vp]
         L.kda_conv1d_varlen.restype = ctypes.c_int
         L.kda_conv1d_update.argtypes = [vp, i32, i64, i64, i32, vp, vp, i32, cache_p, vp, i32, vp, vp]

@@ -294,6 +294,36 @@ int kda_ckpt_load_int8(const int8_t *qdata, const float *scale, int64_t n_slots,
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int kda_target_verify(const void *q, const void *k, const void *v, int32_t io_dtype, const float *g,
+                      const float *beta, int64_t batch, int32_t L, int32_t h, int32_t dk, int32_t dv, float scale,
+                      int32_t qk_l2norm, const kda_cache *cache, const void *idx, const kda_cache *pool,
+                      const void *inter_idx, int32_t idx_type, void *out, void *stream)
+{
+    kda::CacheDesc c{}, pl{};
+    int rc = check_cache(cache, &c);
+    if (rc != KDA_OK) return rc;
+    if ((rc = check_cache(pool, &pl)) != KDA_OK) return rc;
+    if (!valid_dtype(io_dtype) || !valid_itype(idx_type)) return KDA_ERR_DTYPE;
+    if (batch < 0 || L < 1 || h < 1 || dk < 1 || dv < 1) return KDA_ERR_SHAPE;
+    if (!built_head_size(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    if (c.h != h || c.k != dk || c.v != dv || pl.h != h || pl.k != dk || pl.v != dv) return KDA_ERR_SHAPE;
+    if (batch == 0) return KDA_OK;
+    if (batch * static_cast<int64_t>(h) >= (INT64_C(1) << 31) || L > (1 << 20)) return KDA_ERR_RANGE;
+    if ((rc = check_index_array(idx, idx_type)) != KDA_OK) return rc;
+    if ((rc = check_index_array(inter_idx, idx_type)) != KDA_OK) return rc;
+    if (q == nullptr || k == nullptr || v == nullptr || g == nullptr || beta == nullptr || out == nullptr)
+        return KDA_ERR_NULL;
+    const void *vec16[] = {q, k, v, g, c.data, pl.data};
+    for (const void *p : vec16)
+        if (!aligned(p, 16)) return KDA_ERR_ALIGN;
+    if (!aligned(beta, 4) || !aligned(out, 4)) return KDA_ERR_ALIGN;
+    if ((c.row_stride * esize(c.dtype)) % 16 != 0 || (pl.row_stride * esize(pl.dtype)) % 16 != 0)
+        return KDA_ERR_ALIGN;
+    kda::VerifyArgs a{q, k, v, io_dtype, g, beta, batch, L, h, dk, scale, qk_l2norm ? 1 : 0, c, idx, pl, inter_idx,
+                      idx_type, out};
+    return cuda_status(kda::launch_target_verify(a, static_cast<cudaStream_t>(stream)));
+}
+
 namespace {
 int check_conv_common(const void *x, int32_t io_dtype, int64_t channels, int32_t width, const float *weight,
                       const float *bias, int32_t activation, const void *y)

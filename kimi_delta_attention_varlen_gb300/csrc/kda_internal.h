@@ -38,6 +38,24 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode_step(const DecodeArgs &a, cudaStream_t st);
 
+// Speculative target verification (head size d = dk = dv in {32, 64, 128}).
+struct VerifyArgs {
+    const void *q, *k, *v;
+    int32_t io_dtype;
+    const float *g, *beta;
+    int64_t batch;
+    int32_t L, h, d;
+    float scale;
+    int32_t l2norm;
+    CacheDesc cache;       // initial states, read only
+    const void *idx;       // [batch]
+    CacheDesc pool;        // intermediate states
+    const void *inter_idx; // [batch, L]
+    int32_t idx_type;
+    void *out;
+};
+cudaError_t launch_target_verify(const VerifyArgs &a, cudaStream_t st);
+
 // Short causal convolution (width 2..4, channels a multiple of 8).
 struct Conv1dArgs {
     const void *x;

@@ -1,0 +1,217 @@
+// Speculative target verification: L draft tokens per request run through
+// the recurrence from the request's cached state; every token's output is
+// returned and the state after each token is written to its own slot of an
+// intermediate-state pool ("KDA's challenges for AI infra", section 6.4,
+// target_verify, and 6.5, verify intermediate state indices).  The cached
+// state is only read; committing the accepted prefix is a copy of one slot
+// (kda_state_gather / kda_state_scatter).
+//
+// Per (request, head) and token, as in the decode step (column v of S, row v
+// of the cache block, evolves on its own):
+//   a_v = sum_k k_k e^{g_k} S[k][v],  b_v = sum_k q_k e^{g_k} S[k][v],
+//   u_v = beta (v_v - a_v),  S'[k][v] = e^{g_k} S[k][v] + k_k u_v,
+//   o_v = scale (b_v + (q.k) u_v).
+// GPU mapping: one CTA per (request, head); D/8 lanes share a state row, each
+// holding 8 channels of ROWS rows in registers for all L tokens, so the state
+// is read once and each intermediate state is one coalesced write.  The draft
+// tokens' inputs are staged in shared memory 8 tokens at a time (one memory
+// latency per group, in flight together with the state).
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+template <int D> __host__ __device__ constexpr int verify_threads() { return D * D / 8 < 256 ? D * D / 8 : 256; }
+
+template <int LPR> __device__ __forceinline__ float group_sum(float x)
+{
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ void load8(const void *base, int32_t dtype, int64_t e, float x[8])
+{
+    if (dtype == KDA_F32) {
+        const float4 a = *reinterpret_cast<const float4 *>(static_cast<const float *>(base) + e);
+        const float4 b = *(reinterpret_cast<const float4 *>(static_cast<const float *>(base) + e) + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + e);
+        x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+        x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+    }
+}
+
+__device__ __forceinline__ void store8_stream(void *base, int32_t dtype, int64_t e, const float x[8])
+{
+    if (dtype == KDA_F32) {
+        float *p = static_cast<float *>(base) + e;
+        st_cs_v4(p, make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                               __float_as_uint(x[3])));
+        st_cs_v4(p + 4, make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]), __float_as_uint(x[6]),
+                                   __float_as_uint(x[7])));
+    } else {
+        st_cs_v4(static_cast<uint16_t *>(base) + e,
+                 make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                            pack_bf16x2(x[6], x[7])));
+    }
+}
+
+constexpr int kVT = 8;  // draft tokens staged per group
+
+template <int D, typename IO> struct VerifyLayout {
+    static constexpr int ROW = D * static_cast<int>(sizeof(IO));
+    static constexpr int Q = 0;
+    static constexpr int K = Q + kVT * ROW;
+    static constexpr int V = K + kVT * ROW;
+    static constexpr int G = V + kVT * ROW;
+    static constexpr int BETA = G + kVT * D * 4;
+    static constexpr int BYTES = BETA + kVT * 4;
+};
+
+template <int D, typename IO, typename IdxT>
+__global__ void __launch_bounds__(verify_threads<D>())
+verify_kernel(VerifyArgs a)
+{
+    constexpr int LPR = D / 8;                    // lanes per state row
+    constexpr int THREADS = verify_threads<D>();
+    constexpr int RPP = THREADS / LPR;            // rows per pass
+    constexpr int ROWS = D / RPP;                 // rows per thread
+    const int tid = threadIdx.x;
+    const int c0 = 8 * (tid % LPR);               // this lane's channels
+    const int r0 = tid / LPR;                     // rows r0 + RPP j
+    const int64_t H = a.h;
+    const int64_t req = blockIdx.x / H;
+    const int h = static_cast<int>(blockIdx.x % H);
+    const int64_t row = static_cast<int64_t>(static_cast<const IdxT *>(a.idx)[req]);
+    const bool valid = row >= 0 && row < a.cache.n_rows;
+    const int64_t blk = (static_cast<int64_t>(h) * D) * D;  // head block within a cache / pool row
+
+    float s[ROWS][8];
+#pragma unroll
+    for (int j = 0; j < ROWS; ++j) {
+        if (valid) {
+            load8(a.cache.data, a.cache.dtype, row * a.cache.row_stride + blk + (r0 + RPP * j) * D + c0, s[j]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) s[j][c] = 0.f;
+        }
+    }
+    const IO *qg = static_cast<const IO *>(a.q);
+    const IO *kg = static_cast<const IO *>(a.k);
+    const IO *vg = static_cast<const IO *>(a.v);
+    IO *og = static_cast<IO *>(a.out);
+    const IdxT *inter = static_cast<const IdxT *>(a.inter_idx);
+    // token inputs, staged VT tokens at a time: q, k, v [VT][D] io, g [VT][D] fp32, beta [VT]
+    extern __shared__ __align__(16) char smem[];
+    using VL = VerifyLayout<D, IO>;
+    IO *sq = reinterpret_cast<IO *>(smem + VL::Q);
+    IO *sk = reinterpret_cast<IO *>(smem + VL::K);
+    IO *sv = reinterpret_cast<IO *>(smem + VL::V);
+    float *sg = reinterpret_cast<float *>(smem + VL::G);
+    float *sb = reinterpret_cast<float *>(smem + VL::BETA);
+    constexpr int IOCH = D * static_cast<int>(sizeof(IO)) / 16;  // 16-byte chunks of one io row
+    constexpr int GCH = D * 4 / 16;                               // ... of one g row
+    for (int t0 = 0; t0 < a.L; t0 += kVT) {
+        const int nt = a.L - t0 < kVT ? a.L - t0 : kVT;
+        __syncthreads();  // the previous group's inputs are consumed
+        for (int e = tid; e < nt * (3 * IOCH + GCH); e += THREADS) {
+            const int tt = e / (3 * IOCH + GCH), part = e % (3 * IOCH + GCH);
+            const int64_t base = ((req * a.L + t0 + tt) * H + h) * D;
+            if (part < 3 * IOCH) {
+                const int which = part / IOCH, ch = part % IOCH;
+                const IO *src = (which == 0 ? qg : which == 1 ? kg : vg) + base;
+                IO *dst = (which == 0 ? sq : which == 1 ? sk : sv) + tt * D;
+                cp_async16(smem_u32(reinterpret_cast<char *>(dst) + 16 * ch),
+                           reinterpret_cast<const char *>(src) + 16 * ch, 16u);
+            } else {
+                const int ch = part - 3 * IOCH;
+                cp_async16(smem_u32(reinterpret_cast<char *>(sg + tt * D) + 16 * ch),
+                           reinterpret_cast<const char *>(a.g + base) + 16 * ch, 16u);
+            }
+        }
+        if (tid < nt) sb[tid] = a.beta[(req * a.L + t0 + tid) * H + h];
+        cp_async_wait_all();
+        __syncthreads();
+        for (int tt = 0; tt < nt; ++tt) {
+            const int64_t tok = req * a.L + t0 + tt;
+            const int64_t base = (tok * H + h) * D;
+            float qv[8], kv[8], gv[8], vv[ROWS];
+            load8(sq + tt * D, sizeof(IO) == 4 ? KDA_F32 : KDA_BF16, c0, qv);
+            load8(sk + tt * D, sizeof(IO) == 4 ? KDA_F32 : KDA_BF16, c0, kv);
+            load8(sg + tt * D, KDA_F32, c0, gv);
+#pragma unroll
+            for (int j = 0; j < ROWS; ++j) vv[j] = load_as_f32(sv + tt * D + r0 + RPP * j);
+            const float bt = sb[tt];
+            float sqs = 0.f, sks = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                sqs = fmaf(qv[c], qv[c], sqs);
+                sks = fmaf(kv[c], kv[c], sks);
+            }
+            sqs = group_sum<LPR>(sqs);
+            sks = group_sum<LPR>(sks);
+            const float nq = a.l2norm ? rsqrtf(sqs + 1e-6f) : 1.f, nk = a.l2norm ? rsqrtf(sks + 1e-6f) : 1.f;
+            float qk = 0.f, e[8], ke[8], qe[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                qv[c] *= nq;
+                kv[c] *= nk;
+                qk = fmaf(qv[c], kv[c], qk);
+                e[c] = expf(gv[c]);
+                ke[c] = kv[c] * e[c];
+                qe[c] = qv[c] * e[c];
+            }
+            qk = group_sum<LPR>(qk);
+            const int64_t slot = static_cast<int64_t>(inter[tok]);
+            const bool keep = slot >= 0 && slot < a.pool.n_rows;
+#pragma unroll
+            for (int j = 0; j < ROWS; ++j) {
+                float ak = 0.f, bq = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    ak = fmaf(ke[c], s[j][c], ak);
+                    bq = fmaf(qe[c], s[j][c], bq);
+                }
+                ak = group_sum<LPR>(ak);
+                bq = group_sum<LPR>(bq);
+                const float u = bt * (vv[j] - ak);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) s[j][c] = fmaf(e[c], s[j][c], kv[c] * u);
+                if (tid % LPR == 0) og[base + r0 + RPP * j] = from_f32<IO>(a.scale * fmaf(qk, u, bq));
+                if (keep)
+                    store8_stream(a.pool.data, a.pool.dtype, slot * a.pool.row_stride + blk + (r0 + RPP * j) * D + c0,
+                                  s[j]);
+            }
+        }
+    }
+}
+
+template <int D, typename IO, typename IdxT> cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t st)
+{
+    verify_kernel<D, IO, IdxT>
+        <<<static_cast<unsigned>(a.batch * a.h), verify_threads<D>(), VerifyLayout<D, IO>::BYTES, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D> cudaError_t launch_d(const VerifyArgs &a, cudaStream_t st)
+{
+    const bool bf = a.io_dtype == KDA_BF16, i64 = a.idx_type == KDA_I64;
+    if (bf) return i64 ? launch_typed<D, __nv_bfloat16, int64_t>(a, st) : launch_typed<D, __nv_bfloat16, int32_t>(a, st);
+    return i64 ? launch_typed<D, float, int64_t>(a, st) : launch_typed<D, float, int32_t>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_target_verify(const VerifyArgs &a, cudaStream_t st)
+{
+    switch (a.d) {
+    case 32: return launch_d<32>(a, st);
+    case 64: return launch_d<64>(a, st);
+    default: return launch_d<128>(a, st);
+    }
+}
+
+}  // namespace kda

@@ -200,6 +200,31 @@ def test_int8_checkpoint_rejections(L):
     assert ld(A, A, 4, A, A, 0, 0, ctypes.byref(c), None) == OK
 
 
+def test_target_verify_rejections(L):
+    c = cache(dtype=1)
+    V = L.kda_target_verify
+
+    def call(cc=c, pool=c, **kw):
+        a = dict(q=A, k=A, v=A, io=1, g=A, beta=A, R=4, Lt=3, h=2, dk=32, dv=32, idx=A, inter=A, it=0, out=A)
+        a.update(kw)
+        return V(a["q"], a["k"], a["v"], a["io"], a["g"], a["beta"], a["R"], a["Lt"], a["h"], a["dk"], a["dv"], 0.1,
+                 1, ctypes.byref(cc) if cc is not None else None, a["idx"],
+                 ctypes.byref(pool) if pool is not None else None, a["inter"], a["it"], a["out"], None)
+    assert call(cc=None) == NULL
+    assert call(pool=None) == NULL
+    assert call(io=3) == DTYPE
+    assert call(Lt=0) == SHAPE
+    assert call(R=-1) == SHAPE
+    assert call(h=3) == SHAPE
+    assert call(pool=cache(dtype=0, h=2, v=64, k=64)) == SHAPE
+    assert call(dk=48, dv=48) == UNSUPPORTED
+    assert call(R=0, q=None) == OK
+    assert call(inter=None) == NULL
+    assert call(q=None) == NULL
+    assert call(g=A + 4) == ALIGN
+    assert call(pool=cache(dtype=1, stride=2 * 32 * 32 + 4)) == ALIGN
+
+
 def decode(L, c, **kw):
     a = dict(q=A, k=A, v=A, io=1, g=A, beta=A, R=8, h=2, dk=32, dv=32, scale=0.1, l2=1, idx=A, it=0, out=A)
     a.update(kw)
