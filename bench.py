@@ -345,7 +345,7 @@ def conv1d_measure(P, steps: int, warmup: int, W: int = 4) -> dict:
             "shape": f"x [{T}, {C}] bf16, width {W}, SiLU, bf16 states"}
 
 
-def verify_measure(P, steps: int, warmup: int, L: int = 4) -> dict:
+def verify_measure(P, steps: int, warmup: int, L: int = 4, requests: int | None = None) -> dict:
     """Speculative target verification of L draft tokens for the decode workload's
     requests (bf16 cache [2048, 32, 128, 128], R = 512): every token's state to its own
     bf16 pool slot.  Median device time; GB/s of the compulsory bytes (states read once,
@@ -353,7 +353,8 @@ def verify_measure(P, steps: int, warmup: int, L: int = 4) -> dict:
     import kimi_delta_attention_varlen_gb300 as kda
     from kimi_delta_attention_varlen_gb300 import workloads as wl
     dw, pc = P["dw"], P["cache5"]
-    R, H, K, V = dw.R, dw.H, dw.K, dw.V
+    R, H, K, V = (requests or dw.R), dw.H, dw.K, dw.V
+    didx = P["didx"][:R]
     dev = P["out"].device
     t = wl.token_inputs(R * L, H, K, V, dw.io_dtype, seed=41, device=dev)
     inp = {n: x.view(R, L, *x.shape[1:]) for n, x in t.items()}
@@ -362,8 +363,7 @@ def verify_measure(P, steps: int, warmup: int, L: int = 4) -> dict:
     out = torch.empty(R, L, H, V, dtype=dw.io_dtype, device=dev)
 
     def call():
-        kda.kda_target_verify(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], pc.view, P["didx"], pool, inter,
-                              out)
+        kda.kda_target_verify(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], pc.view, didx, pool, inter, out)
     for _ in range(warmup):
         call()
     times = []
@@ -375,7 +375,7 @@ def verify_measure(P, steps: int, warmup: int, L: int = 4) -> dict:
         b.synchronize()
         times.append(a.elapsed_time(b))
     ms = statistics.median(times)
-    valid = int((dw.idx >= 0).sum())
+    valid = int((dw.idx[:R] >= 0).sum())
     st = H * V * K * pc.view.element_size()
     io = R * L * H * (3 * K * 2 + K * 4 + 4 + V * 2)
     nbytes = valid * st + R * L * st + io
@@ -504,9 +504,13 @@ def native(args, ranks: Ranks) -> dict | None:
 
     br = {"gather": med("g0", "p0"), "chunk_table": med("p0", "p1"), "chunk_prep": med("p1", "p2"),
           "state_pass": med("p2", "p3"), "scatter": med("p3", "s1"), "decode": med("s1", "d1")}
-    if args.workload == "small":  # reduced batch for profiler captures: the step only
+    if args.workload == "small":  # reduced sizes for profiler captures: the step, then one call of each next-row leg
+        legs = {"cached_prefill": cached_measure(P, 1, 1),
+                "ckpt_int8": ckpt_int8_measure(P, 1, 1, pairs=64),
+                "conv1d": conv1d_measure(P, 1, 1),
+                "target_verify": verify_measure(P, 1, 1, requests=128)}
         return {"metric": METRIC, "value": value, "unit": UNIT, "workload": P["w"].name, "tokens": T,
-                "breakdown_ms": br} if ranks.rank == 0 else None
+                "breakdown_ms": br, "legs": legs} if ranks.rank == 0 else None
 
     # end to end through the public API: pinned host inputs -> device, step, results -> host
     inp = P["inp"]
@@ -645,7 +649,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=["full", "small"], default="full",
-                    help="small: 4-sequence varlen batch, step timing only (for profiler captures)")
+                    help="small: 4-sequence varlen batch, step timing plus one call of each next-row leg "
+                         "at reduced sizes (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
