@@ -314,6 +314,44 @@ chunk_prep_kernel(PrepParams p)
     }
 
     // ---- 2. row pass: normalise q, k; operand tiles in shared memory; Q~, K~ to the record ----
+    // norms of the warp's 8 rows: 16 partial sums per lane reduced by a transposed butterfly
+    // (lane L ends with the total of value L >> 1), one rsqrt per lane, then broadcast
+    float nqs[ROWS], nks[ROWS];
+    if constexpr (kStage) {
+        float vsum[2 * ROWS];
+#pragma unroll
+        for (int j = 0; j < ROWS; ++j) {
+            const uint32_t o = tile_off<D, C>(r0 + j, cb);
+            float qv[CPL], kv[CPL];
+            load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::QP + o), qv);
+            load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::KP + o), kv);
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                sq += qv[c] * qv[c];
+                sk += kv[c] * kv[c];
+            }
+            vsum[2 * j] = sq;
+            vsum[2 * j + 1] = sk;
+        }
+#pragma unroll
+        for (int mask = 16, half = ROWS; mask >= 2; mask >>= 1, half >>= 1) {
+            const bool up = (lane & mask) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float send = up ? vsum[i] : vsum[i + half];
+                const float keep = up ? vsum[i + half] : vsum[i];
+                vsum[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+            }
+        }
+        const float tot = vsum[0] + __shfl_xor_sync(0xffffffffu, vsum[0], 1);
+        const float rn = p.l2norm ? rsqrtf(tot + 1e-6f) : 1.f;
+#pragma unroll
+        for (int j = 0; j < ROWS; ++j) {
+            nqs[j] = __shfl_sync(0xffffffffu, rn, 4 * j);
+            nks[j] = __shfl_sync(0xffffffffu, rn, 4 * j + 2);
+        }
+    }
 #pragma unroll
     for (int j0 = 0; j0 < ROWS; j0 += PRE) {
         if (!kStage && j0 > 0) load_rows(j0);
@@ -330,19 +368,25 @@ chunk_prep_kernel(PrepParams p)
                 rk[j].get(kv);
                 rv[j].get(vv);
             }
-            float sq = 0.f, sk = 0.f;
+            float nq, nk;
+            if constexpr (kStage) {
+                nq = nqs[j0 + j];
+                nk = nks[j0 + j];
+            } else {
+                float sq = 0.f, sk = 0.f;
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                sq += qv[c] * qv[c];
-                sk += kv[c] * kv[c];
-            }
+                for (int c = 0; c < CPL; ++c) {
+                    sq += qv[c] * qv[c];
+                    sk += kv[c] * kv[c];
+                }
 #pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o2);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o2);
+                for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                    sq += __shfl_xor_sync(0xffffffffu, sq, o2);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, o2);
+                }
+                nq = p.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
+                nk = p.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
             }
-            const float nq = p.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
-            const float nk = p.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
             float kp[CPL], qp[CPL], kr[CPL], qt[CPL], kt[CPL];
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
