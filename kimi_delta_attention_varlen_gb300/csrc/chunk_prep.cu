@@ -54,8 +54,8 @@ template <int D> struct PrepSmem {
     static constexpr int QP = KP + TILE; // q P: Gram A operand -> U^T staging [D][64]
     static constexpr int KR = QP + TILE; // k R: Gram B operand
     static constexpr int VS = KR + TILE; // v (bf16): U right-hand side -> U
-    static constexpr int TAB = VS + TILE;                  // L[4][D] fp32, F[7][D] bf16 (row 6: ones)
-    static constexpr int BETA = TAB + 4 * D * 4 + 7 * D * 2;  // beta [64]
+    static constexpr int TAB = VS + TILE;                  // L[4][D] fp32, F[6][D] bf16
+    static constexpr int BETA = TAB + 4 * D * 4 + 6 * D * 2;  // beta [64]
     static constexpr int BYTES = BETA + C * 4;
 };
 
@@ -129,9 +129,8 @@ __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float f0, float f1)
     return pack_bf16x2(bf16_lo(u) * f0, bf16_hi(u) * f1);
 }
 
-// Slot of the factor F_IJ (J < I) in the F table; slot kOnes holds ones.
+// Slot of the factor F_IJ (J < I) in the F table.
 __device__ __forceinline__ int fslot(int I, int J) { return I * (I - 1) / 2 + J; }
-constexpr int kOnes = 6;
 
 // N consecutive fp32 values from global memory (N = 1, 2, 4; aligned to N floats).
 template <int N> __device__ __forceinline__ void ldg_f32(const float *p, float x[N])
@@ -186,7 +185,7 @@ chunk_prep_kernel(PrepParams p)
 
     float *sSum = reinterpret_cast<float *>(smem + SM::SUMS);
     float *sL = reinterpret_cast<float *>(smem + SM::TAB);
-    uint16_t *sFb = reinterpret_cast<uint16_t *>(sL + 4 * D);  // F_IJ as bf16 [6][D], then a row of ones
+    uint16_t *sFb = reinterpret_cast<uint16_t *>(sL + 4 * D);  // F_IJ as bf16 [6][D]
     float *sBeta = reinterpret_cast<float *>(smem + SM::BETA);
 
     // ---- 1. issue every load of the chunk ----
@@ -282,8 +281,8 @@ chunk_prep_kernel(PrepParams p)
 #pragma unroll
         for (int c = 0; c < CPL; ++c) gr[j][c] += off[c];
 
-    // per-channel factors: F_IJ (warps 0-5, one (I, J) each; warp 6 the row of
-    // ones), L_I = e^{G_mI} (even warps), gamma = e^{G_last} (warp 7, to the record)
+    // per-channel factors: F_IJ (warps 0-5, one (I, J) each), L_I = e^{G_mI}
+    // (even warps), gamma = e^{G_last} (warp 7, to the record)
     float gmi[CPL], lI[CPL], ls[CPL], zz[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
@@ -301,12 +300,7 @@ chunk_prep_kernel(PrepParams p)
             f[c] = exp2f(pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], fI) -
                          pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], fJ));
         store_bf16<CPL>(reinterpret_cast<char *>(sFb + warp * D), static_cast<uint32_t>(cb * 2), f);
-    } else if (warp == 6) {
-        float one[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) one[c] = 1.f;
-        store_bf16<CPL>(reinterpret_cast<char *>(sFb + kOnes * D), static_cast<uint32_t>(cb * 2), one);
-    } else {
+    } else if (warp == 7) {
         float gam[CPL];
 #pragma unroll
         for (int c = 0; c < CPL; ++c) gam[c] = exp2f(glast[c]);
@@ -422,45 +416,55 @@ chunk_prep_kernel(PrepParams p)
     // diagonal blocks in fp32 for their inverses; A_qk (x scale, causal) -> the record.
     float *sAd = reinterpret_cast<float *>(smem + SM::AD);  // [4][16][17] fp32
     {
-        constexpr int MAXP = (20 + kWarps - 1) / kWarps;  // pairs per warp (3)
-        const int npairs = (20 - warp + kWarps - 1) / kWarps;
+        // Pairs by slot: u = 0 an off-diagonal pair (warp w: the w-th of 12), u = 1 a diagonal
+        // pair (the w-th of 8), u = 2 (warps 0-3) the off-diagonal pair 8 + w.  Off-diagonal
+        // pairs scale by F_IJ; diagonal ones need no factor.  The first six of each kind are A_kk.
+        constexpr int MAXP = 3;
+        const int npairs = warp < 4 ? 3 : 2;
         int pI[MAXP], pJ[MAXP];
         bool pqk[MAXP];
 #pragma unroll
         for (int u = 0; u < MAXP; ++u) {
-            const int pr = warp + kWarps * u;
-            const int li = pr % 10;                        // lower-triangle block index
-            pqk[u] = pr >= 10;
-            pI[u] = li >= 6 ? 3 : li >= 3 ? 2 : li >= 1 ? 1 : 0;
-            pJ[u] = li - pI[u] * (pI[u] + 1) / 2;
+            if (u == 1) {  // diagonal: index w in 0..7
+                pqk[u] = warp >= 4;
+                pI[u] = pJ[u] = warp & 3;
+            } else {       // off-diagonal: index w or 8 + w in 0..11
+                const int o = u == 0 ? warp : 8 + warp;
+                const int sl = o % 6;  // F slot (I, J), J < I
+                pqk[u] = o >= 6;
+                pI[u] = sl < 1 ? 1 : sl < 3 ? 2 : 3;
+                pJ[u] = sl - pI[u] * (pI[u] - 1) / 2;
+            }
         }
         float acc[MAXP][2][4] = {};
-        // One k-step of pair u: a <- a * F_IJ on the fragment's four channels (bf16x2
-        // products; the all-ones row for diagonal pairs keeps the code branch-free).
-        auto step = [&](int u, int ks) {
+        // One k-step of pair u; off-diagonal pairs: a <- a * F_IJ on the fragment's four
+        // channels (bf16x2 products).
+        auto step = [&](int u, int ks, auto scaled) {
             const int I = pI[u], J = pJ[u];
             uint32_t a[4], b[4];
             ldmatrix_x4(a, smem_u32(smem + (pqk[u] ? SM::QP : SM::KP) +
                                     tile_off<D, C>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
-            const uint16_t *f = sFb + (J < I ? fslot(I, J) : kOnes) * D + 16 * ks + 2 * tig;
-            const uint32_t f01 = *reinterpret_cast<const uint32_t *>(f);
-            const uint32_t f23 = *reinterpret_cast<const uint32_t *>(f + 8);
-            a[0] = mul_bf16x2(a[0], f01);
-            a[1] = mul_bf16x2(a[1], f01);
-            a[2] = mul_bf16x2(a[2], f23);
-            a[3] = mul_bf16x2(a[3], f23);
+            if constexpr (decltype(scaled)::value) {
+                const uint16_t *f = sFb + fslot(I, J) * D + 16 * ks + 2 * tig;
+                const uint32_t f01 = *reinterpret_cast<const uint32_t *>(f);
+                const uint32_t f23 = *reinterpret_cast<const uint32_t *>(f + 8);
+                a[0] = mul_bf16x2(a[0], f01);
+                a[1] = mul_bf16x2(a[1], f01);
+                a[2] = mul_bf16x2(a[2], f23);
+                a[3] = mul_bf16x2(a[3], f23);
+            }
             ldmatrix_x4(b, smem_u32(smem + SM::KR + tile_off<D, C>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
             mma_bf16(acc[u][0], a, b[0], b[1]);
             mma_bf16(acc[u][1], a, b[2], b[3]);
         };
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // every warp: pairs warp, warp + 8 (independent chains)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) step(u, ks);
+        for (int ks = 0; ks < D / 16; ++ks) {  // every warp: an off-diagonal and a diagonal pair
+            step(0, ks, std::true_type{});
+            step(1, ks, std::false_type{});
         }
-        if (npairs > 2) {  // warps 0-3: pair warp + 16
+        if (npairs > 2) {  // warps 0-3: one more off-diagonal pair
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) step(2, ks);
+            for (int ks = 0; ks < D / 16; ++ks) step(2, ks, std::true_type{});
         }
         // Epilogue of pair u (one branch per pair on its kind, none per element).
         auto epilogue = [&](int u) {
