@@ -86,6 +86,23 @@ __device__ __forceinline__ float activate(float y, int32_t act)
     return act == 1 ? __fdividef(y, 1.f + __expf(-y)) : y;
 }
 
+__device__ __forceinline__ float tanh_approx(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// SiLU for bf16 outputs: y * sigmoid(y) with sigmoid(y) = (1 + tanh(y / 2)) / 2
+// from one hardware tanh (relative error about 2^-11 on the sigmoid, below half a
+// bf16 step of the output, which is rounded to 2^-9 anyway).
+__device__ __forceinline__ float activate_bf16(float y, int32_t act)
+{
+    if (act != 1) return y;
+    const float h = 0.5f * y;
+    return fmaf(h, tanh_approx(h), h);
+}
+
 struct ConvArgs {
     const void *x;
     int32_t io_dtype;
@@ -124,7 +141,7 @@ template <int W> __device__ __forceinline__ void load_taps(const ConvArgs &a, in
 
 // Tokens [t0, t0 + TT) x channels [c0, c0 + 8) per thread.
 template <int W, typename IO, int TT>
-__global__ void __launch_bounds__(kConvThreads, 4)
+__global__ void __launch_bounds__(kConvThreads, 3)
 conv_varlen_kernel(ConvArgs a)
 {
     const int64_t c0 = (static_cast<int64_t>(blockIdx.y) * kConvThreads + threadIdx.x) * kVec;
@@ -167,6 +184,32 @@ conv_varlen_kernel(ConvArgs a)
         }
     }
     IO *y = static_cast<IO *>(a.y);
+    if (t0 + TT <= end) {  // the whole tile inside one sequence (the common case): no branches
+        IO *yp = y + t0 * C + c0;
+#pragma unroll
+        for (int jt = 0; jt < TT; ++jt) {
+            float xt[8], out[8];
+            xr[jt].get(xt);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float acc = bias[j];
+#pragma unroll
+                for (int i = 0; i < W - 1; ++i) acc = fmaf(w[j][i], win[(jt + i) % (W - 1)][j], acc);
+                acc = fmaf(w[j][W - 1], xt[j], acc);
+                out[j] = sizeof(IO) == 2 ? activate_bf16(acc, a.act) : activate(acc, a.act);
+            }
+            store8(yp, a.io_dtype, 0, out);
+            yp += C;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) win[jt % (W - 1)][j] = xt[j];  // ring: the oldest entry is replaced
+        }
+        if (t0 + TT == end && a.final_state != nullptr) {  // the tile ends the sequence: its final state
+#pragma unroll
+            for (int i = 0; i < W - 1; ++i)
+                store8(a.final_state, a.state_dtype, (b * (W - 1) + i) * C + c0, win[(TT + i) % (W - 1)]);
+        }
+        return;
+    }
 #pragma unroll
     for (int jt = 0; jt < TT; ++jt) {
         const int64_t t = t0 + jt;
@@ -195,7 +238,7 @@ conv_varlen_kernel(ConvArgs a)
 #pragma unroll
             for (int i = 0; i < W - 1; ++i) acc = fmaf(w[j][i], win[i][j], acc);
             acc = fmaf(w[j][W - 1], xt[j], acc);
-            out[j] = activate(acc, a.act);
+            out[j] = sizeof(IO) == 2 ? activate_bf16(acc, a.act) : activate(acc, a.act);
         }
         store8(y, a.io_dtype, t * C + c0, out);
 #pragma unroll
