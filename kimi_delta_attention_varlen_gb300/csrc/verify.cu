@@ -167,23 +167,66 @@ verify_kernel(VerifyArgs a)
             qk = group_sum<LPR>(qk);
             const int64_t slot = static_cast<int64_t>(inter[tok]);
             const bool keep = slot >= 0 && slot < a.pool.n_rows;
+            if constexpr (2 * ROWS == LPR) {
+                // the 2 ROWS dot products of this thread's rows, reduced over the row's LPR
+                // lanes by a transposed butterfly: lane g of the group ends with value g
+                // (a of row g / 2 for even g, b for odd g)
+                float vals[2 * ROWS];
 #pragma unroll
-            for (int j = 0; j < ROWS; ++j) {
-                float ak = 0.f, bq = 0.f;
+                for (int j = 0; j < ROWS; ++j) {
+                    float ak = 0.f, bq = 0.f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    ak = fmaf(ke[c], s[j][c], ak);
-                    bq = fmaf(qe[c], s[j][c], bq);
+                    for (int c = 0; c < 8; ++c) {
+                        ak = fmaf(ke[c], s[j][c], ak);
+                        bq = fmaf(qe[c], s[j][c], bq);
+                    }
+                    vals[2 * j] = ak;
+                    vals[2 * j + 1] = bq;
                 }
-                ak = group_sum<LPR>(ak);
-                bq = group_sum<LPR>(bq);
-                const float u = bt * (vv[j] - ak);
+                const int lane = tid & 31;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) s[j][c] = fmaf(e[c], s[j][c], kv[c] * u);
-                if (tid % LPR == 0) og[base + r0 + RPP * j] = from_f32<IO>(a.scale * fmaf(qk, u, bq));
-                if (keep)
-                    store8_stream(a.pool.data, a.pool.dtype, slot * a.pool.row_stride + blk + (r0 + RPP * j) * D + c0,
-                                  s[j]);
+                for (int mask = LPR / 2, half = ROWS; mask >= 1; mask >>= 1, half >>= 1) {
+                    const bool up = (lane & mask) != 0;
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        const float send = up ? vals[i] : vals[i + half];
+                        const float kept = up ? vals[i + half] : vals[i];
+                        vals[i] = kept + __shfl_xor_sync(0xffffffffu, send, mask);
+                    }
+                }
+                const int g = tid % LPR, jr = g >> 1;
+                const float u_even = bt * (load_as_f32(sv + tt * D + r0 + RPP * jr) - vals[0]);  // even lanes: u
+                const float u_pair = __shfl_sync(0xffffffffu, u_even, lane & ~1);
+                if (g & 1) og[base + r0 + RPP * jr] = from_f32<IO>(a.scale * fmaf(qk, u_pair, vals[0]));
+                const int gbase = lane & ~(LPR - 1);
+#pragma unroll
+                for (int j = 0; j < ROWS; ++j) {
+                    const float u = __shfl_sync(0xffffffffu, u_even, gbase + 2 * j);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) s[j][c] = fmaf(e[c], s[j][c], kv[c] * u);
+                    if (keep)
+                        store8_stream(a.pool.data, a.pool.dtype,
+                                      slot * a.pool.row_stride + blk + (r0 + RPP * j) * D + c0, s[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < ROWS; ++j) {
+                    float ak = 0.f, bq = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        ak = fmaf(ke[c], s[j][c], ak);
+                        bq = fmaf(qe[c], s[j][c], bq);
+                    }
+                    ak = group_sum<LPR>(ak);
+                    bq = group_sum<LPR>(bq);
+                    const float u = bt * (vv[j] - ak);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) s[j][c] = fmaf(e[c], s[j][c], kv[c] * u);
+                    if (tid % LPR == 0) og[base + r0 + RPP * j] = from_f32<IO>(a.scale * fmaf(qk, u, bq));
+                    if (keep)
+                        store8_stream(a.pool.data, a.pool.dtype,
+                                      slot * a.pool.row_stride + blk + (r0 + RPP * j) * D + c0, s[j]);
+                }
             }
         }
     }
