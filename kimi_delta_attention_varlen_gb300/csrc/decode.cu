@@ -144,7 +144,7 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
         for (int c = 0; c < 8; ++c) {
             const float qh = cur.q[c] * rq;
             kh[c] = cur.k[c] * rk;
-            eg[c] = expf(cur.g[c]);
+            eg[c] = ex2_approx(cur.g[c] * 1.4426950408889634f);  // e^g
             ke[c] = kh[c] * eg[c];
             qe[c] = qh * eg[c];
             qk += qh * kh[c];
@@ -152,6 +152,77 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
         qk = group_sum<LPR>(qk);
         const bool valid = cur.row >= 0;
         CT *dst = cache + (valid ? cur.row : 0) * row_stride + static_cast<int64_t>(it % H) * D * D;
+        if constexpr (2 * ROWS == LPR) {
+            // the 2 ROWS dot products reduced over the LPR lanes of a row by a transposed
+            // butterfly: lane g of the group ends with value g (a of row g / 2 for even g, b for
+            // odd g); u of each row is broadcast from its lane; the state slices are read from
+            // shared memory again for the update instead of being held across the reduction
+            auto slice = [&](int j, float st[8]) {
+                if (valid) {
+                    if constexpr (V16 == 1) {
+                        const uint4 a = slots[((s * ROWS + j) * V16) * THREADS + tid];
+                        st[0] = bf16_lo(a.x); st[1] = bf16_hi(a.x); st[2] = bf16_lo(a.y); st[3] = bf16_hi(a.y);
+                        st[4] = bf16_lo(a.z); st[5] = bf16_hi(a.z); st[6] = bf16_lo(a.w); st[7] = bf16_hi(a.w);
+                    } else {
+                        const uint4 a = slots[((s * ROWS + j) * V16) * THREADS + tid];
+                        const uint4 b = slots[((s * ROWS + j) * V16 + 1) * THREADS + tid];
+                        st[0] = __uint_as_float(a.x); st[1] = __uint_as_float(a.y);
+                        st[2] = __uint_as_float(a.z); st[3] = __uint_as_float(a.w);
+                        st[4] = __uint_as_float(b.x); st[5] = __uint_as_float(b.y);
+                        st[6] = __uint_as_float(b.z); st[7] = __uint_as_float(b.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) st[c] = 0.f;
+                }
+            };
+            float vals[2 * ROWS];
+#pragma unroll
+            for (int j = 0; j < ROWS; ++j) {
+                float st[8], a = 0.f, b = 0.f;
+                slice(j, st);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    a = fmaf(ke[c], st[c], a);
+                    b = fmaf(qe[c], st[c], b);
+                }
+                vals[2 * j] = a;
+                vals[2 * j + 1] = b;
+            }
+            const int lane = tid & 31;
+#pragma unroll
+            for (int mask = LPR / 2, half = ROWS; mask >= 1; mask >>= 1, half >>= 1) {
+                const bool up = (lane & mask) != 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float send = up ? vals[i] : vals[i + half];
+                    const float kept = up ? vals[i + half] : vals[i];
+                    vals[i] = kept + __shfl_xor_sync(0xffffffffu, send, mask);
+                }
+            }
+            const int jr = lr >> 1;
+            // cur.v[jr] with jr varying by lane: select from the registers without local memory
+            float vj = cur.v[0];
+#pragma unroll
+            for (int j = 1; j < ROWS; ++j) vj = jr == j ? cur.v[j] : vj;
+            const float u_even = cur.beta * (vj - vals[0]);
+            const float u_pair = __shfl_sync(0xffffffffu, u_even, lane & ~1);
+            if (lr & 1) out[it * D + jr * RPP + rip] = from_f32<IO>(scale * fmaf(qk, u_pair, vals[0]));
+            const int gbase = lane & ~(LPR - 1);
+#pragma unroll
+            for (int j = 0; j < ROWS; ++j) {
+                const float u = __shfl_sync(0xffffffffu, u_even, gbase + 2 * j);
+                if (valid) {
+                    float st[8], sn[8];
+                    slice(j, st);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) sn[c] = fmaf(eg[c], st[c], kh[c] * u);
+                    store8(dst + (j * RPP + rip) * D + c0, sn);
+                }
+            }
+            cur = nxt;
+            continue;
+        }
 #pragma unroll
         for (int j = 0; j < ROWS; ++j) {
             const int vi = j * RPP + rip;
