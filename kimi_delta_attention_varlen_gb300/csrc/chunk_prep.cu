@@ -287,9 +287,9 @@ chunk_prep_kernel(PrepParams p)
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
         gmi[c] = pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], I);
-        lI[c] = exp2f(gmi[c]);             // e^{G_mI}           <= 1
+        lI[c] = ex2_approx(gmi[c]);             // e^{G_mI}          <= 1
         ls[c] = lI[c] * p.scale;
-        zz[c] = exp2f(glast[c] - gmi[c]);  // e^{G_last - G_mI}  <= 1
+        zz[c] = ex2_approx(glast[c] - gmi[c]);  // e^{G_last - G_mI}  <= 1
     }
     if (!(warp & 1)) st_f32<CPL>(sL + I * D + cb, lI);
     if (warp < 6) {
@@ -297,13 +297,13 @@ chunk_prep_kernel(PrepParams p)
         float f[CPL];
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
-            f[c] = exp2f(pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], fI) -
-                         pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], fJ));
+            f[c] = ex2_approx(pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], fI) -
+                              pick4(gm[0][c], gm[1][c], gm[2][c], gm[3][c], fJ));
         store_bf16<CPL>(reinterpret_cast<char *>(sFb + warp * D), static_cast<uint32_t>(cb * 2), f);
     } else if (warp == 7) {
         float gam[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) gam[c] = exp2f(glast[c]);
+        for (int c = 0; c < CPL; ++c) gam[c] = ex2_approx(glast[c]);
         st_f32<CPL>(reinterpret_cast<float *>(rec + R::GAMMA) + cb, gam);
     }
 
