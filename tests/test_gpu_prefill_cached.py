@@ -166,3 +166,96 @@ def test_checkpoint_slots_past_capacity_are_not_written():
     torch.cuda.synchronize()
     assert not torch.isnan(ck[:n - 2]).any()
     assert torch.isnan(ck[n - 2:]).all()
+
+
+def test_full_varlen_workload_fused_equals_unfused():
+    """At the benchmark's size (16 sequences U[512, 8192], H = 32, D = 128, fp32 cache
+    [1024, 32, 128, 128]): the fused call is bit-identical with gather -> prefill ->
+    scatter, outputs and every cache byte."""
+    w = wl.varlen()
+    H, D = w.H, w.K
+    cu = cu_of(w.lengths)
+    T, B = cu[-1], w.B
+    pc = wl.paged_cache(w.cache_rows, H, D, D, w.cache_dtype, w.cache_stride, seed=w.seed, device=DEV)
+    inp = wl.token_inputs(T, H, D, D, w.io_dtype, seed=w.seed, device=DEV)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    gidx, gflags, sidx = w.gather_idx.to(DEV), w.gather_flags.to(DEV), w.scatter_idx.to(DEV)
+    backing_a = pc.backing.clone()
+    view_a = backing_a.as_strided(pc.view.shape, pc.view.stride(), pc.front)
+    packed = torch.empty(B, H, D, D, dtype=pc.view.dtype, device=DEV)
+    kda_state_gather(view_a, gidx, packed, gflags)
+    out_a = torch.empty(T, H, D, dtype=w.io_dtype, device=DEV)
+    fin = torch.empty(B, H, D, D, dtype=torch.float32, device=DEV)
+    ws = workspace(T, B, H, D)
+    kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, out_a, ws, init_state=packed,
+                       final_state=fin)
+    kda_state_scatter(view_a, sidx, fin)
+    out_b = torch.empty_like(out_a)
+    kda_prefill_varlen_cached(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, out_b, ws, pc.view, gidx,
+                              flags=gflags, idx_out=sidx)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a.view(torch.uint8), out_b.view(torch.uint8))
+    assert torch.equal(backing_a.view(torch.uint8), pc.backing.view(torch.uint8))
+    del backing_a, view_a
+    torch.cuda.empty_cache()
+
+
+def test_next_rows_capture_into_a_cuda_graph():
+    """The fused prefill, INT8 store, conv1d and verify calls allocate nothing and take the
+    stream per call: captured once, a replay on new input values gives the eager results."""
+    from kimi_delta_attention_varlen_gb300 import (kda_ckpt_store_int8, kda_conv1d_varlen, kda_target_verify)
+    lengths, H, D = [130, 64, 7], 2, 64
+    cu = cu_of(lengths)
+    T, B = cu[-1], len(lengths)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    pc = wl.paged_cache(8, H, D, D, torch.float32, None, seed=1, device=DEV)
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=2, device=DEV)
+    idx = torch.tensor([3, 5, -1], dtype=torch.int32, device=DEV)
+    x = torch.randn(T, 3 * H * D, device=DEV).to(torch.bfloat16)
+    wt = torch.randn(3 * H * D, 4, device=DEV)
+    R, L = 2, 3
+    vin = {n: a.view(R, L, *a.shape[1:]) for n, a in wl.token_inputs(R * L, H, D, D, torch.bfloat16, seed=4,
+                                                                     device=DEV).items()}
+    ridx = torch.tensor([1, 6], dtype=torch.int32, device=DEV)
+    inter = torch.arange(R * L, dtype=torch.int32, device=DEV).view(R, L)
+
+    def make_outputs():
+        return dict(out=torch.empty(T, H, D, dtype=torch.bfloat16, device=DEV),
+                    q8=torch.empty(2, H, D, D, dtype=torch.int8, device=DEV),
+                    sc=torch.empty(2, H, D, dtype=torch.float32, device=DEV),
+                    y=torch.empty_like(x),
+                    pool=torch.empty(R * L, H, D, D, dtype=torch.float32, device=DEV),
+                    vout=torch.empty(R, L, H, D, dtype=torch.bfloat16, device=DEV))
+
+    ws = workspace(T, B, H, D)
+
+    def calls(o, cache):
+        kda_prefill_varlen_cached(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, o["out"], ws, cache,
+                                  idx, idx_out=idx)
+        kda_ckpt_store_int8(cache, idx[:2].contiguous(), torch.arange(2, dtype=torch.int32, device=DEV), o["q8"],
+                            o["sc"])
+        kda_conv1d_varlen(x, cu_t, wt, o["y"], activation="silu")
+        kda_target_verify(vin["q"], vin["k"], vin["v"], vin["g"], vin["beta"], cache, ridx, o["pool"], inter,
+                          o["vout"])
+
+    g_out = make_outputs()
+    start = pc.backing.clone()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        calls(g_out, pc.view)
+    # new values in the captured input buffers, the cache restored, then replay
+    for t in (inp["q"], inp["v"], x):
+        t.copy_(torch.randn(t.shape, device=DEV).to(t.dtype))
+    pc.backing.copy_(start)
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed_cache = pc.backing.clone()
+    pc.backing.copy_(start)
+    e_out = make_outputs()
+    calls(e_out, pc.view)
+    torch.cuda.synchronize()
+    for k in e_out:
+        assert torch.equal(g_out[k].view(torch.uint8), e_out[k].view(torch.uint8)), k
+    assert torch.equal(replayed_cache.view(torch.uint8), pc.backing.view(torch.uint8))
