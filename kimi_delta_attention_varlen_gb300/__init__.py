@@ -26,7 +26,8 @@ from ._abi import (EXPORTED, KDA_BF16, KDA_F32, KDA_I32, KDA_I64, LIB_PATH, KdaC
 __all__ = [
     "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
     "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc", "kda_decode_step",
-    "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_conv1d_varlen", "kda_conv1d_update", "kda_target_verify", "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
+    "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_conv1d_varlen", "kda_conv1d_update", "kda_target_verify",
+    "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
     "KdaError", "EXPORTED", "LIB_PATH",
 ]
 

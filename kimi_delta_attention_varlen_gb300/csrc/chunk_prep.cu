@@ -124,10 +124,6 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
     return *reinterpret_cast<uint32_t *>(&x);
 }
 
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float f0, float f1)
-{
-    return pack_bf16x2(bf16_lo(u) * f0, bf16_hi(u) * f1);
-}
 
 // Slot of the factor F_IJ (J < I) in the F table.
 __device__ __forceinline__ int fslot(int I, int J) { return I * (I - 1) / 2 + J; }
@@ -409,7 +405,8 @@ chunk_prep_kernel(PrepParams p)
         const int b = e >> 5, r = (e >> 1) & 15, ch = e & 1;
         const int I = b < 3 ? 0 : b < 5 ? 1 : 2;        // upper blocks (I, J), J > I
         const int J = b < 3 ? b + 1 : b < 5 ? b - 1 : 3;
-        *reinterpret_cast<uint4 *>(rec + R::AQK + swz_off<128>(16 * I + r, 16 * J + 8 * ch)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(rec + R::AQK + swz_off<128>(16 * I + r, 16 * J + 8 * ch)) =
+            make_uint4(0u, 0u, 0u, 0u);
     }
     // ---- 3. gated Gram products, 20 (matrix, I, J) block pairs over 8 warps ----
     // A_kk (x beta_i, strictly lower) -> bf16 tile for the substitution products, and its
@@ -453,7 +450,8 @@ chunk_prep_kernel(PrepParams p)
                 a[2] = mul_bf16x2(a[2], f23);
                 a[3] = mul_bf16x2(a[3], f23);
             }
-            ldmatrix_x4(b, smem_u32(smem + SM::KR + tile_off<D, C>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
+            ldmatrix_x4(b, smem_u32(smem + SM::KR +
+                                    tile_off<D, C>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
             mma_bf16(acc[u][0], a, b[0], b[1]);
             mma_bf16(acc[u][1], a, b[2], b[3]);
         };
@@ -519,7 +517,8 @@ chunk_prep_kernel(PrepParams p)
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            *reinterpret_cast<uint16_t *>(smem + SM::TD + swz_off<128>(16 * I + i, 16 * I + j)) = f32_to_bf16_bits(tcol[i]);
+            *reinterpret_cast<uint16_t *>(smem + SM::TD + swz_off<128>(16 * I + i, 16 * I + j)) =
+                f32_to_bf16_bits(tcol[i]);
     }
     __syncthreads();
 
@@ -556,7 +555,8 @@ chunk_prep_kernel(PrepParams p)
 #pragma unroll
                     for (int K = 0; K < I; ++K) {
                         uint32_t a[4];
-                        ldmatrix_x4(a, smem_u32(smem + SM::AB + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * K + 8 * (mi >> 1))));
+                        ldmatrix_x4(a, smem_u32(smem + SM::AB +
+                                                swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * K + 8 * (mi >> 1))));
 #pragma unroll
                         for (int np = 0; np < NP; ++np) {
                             uint32_t b[4];
@@ -590,11 +590,13 @@ chunk_prep_kernel(PrepParams p)
                 {
                     float acc[2 * NP][4] = {};
                     uint32_t a[4];
-                    ldmatrix_x4(a, smem_u32(smem + SM::TD + swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * I + 8 * (mi >> 1))));
+                    ldmatrix_x4(a, smem_u32(smem + SM::TD +
+                                            swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * I + 8 * (mi >> 1))));
 #pragma unroll
                     for (int np = 0; np < NP; ++np) {
                         uint32_t b[4];
-                        ldmatrix_x4_trans(b, smem_u32(xtile + tile_off<D, 16>(ri + 8 * (mi & 1), c0 + 16 * np + 8 * (mi >> 1))));
+                        ldmatrix_x4_trans(b, smem_u32(xtile + tile_off<D, 16>(ri + 8 * (mi & 1),
+                                                                              c0 + 16 * np + 8 * (mi >> 1))));
                         mma_bf16(acc[2 * np], a, b[0], b[1]);
                         mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
                     }
@@ -652,9 +654,13 @@ cudaError_t launch_chunk_prep(int d, int32_t io_dtype, const PrepParams &p, int6
 {
     const bool bf = io_dtype == KDA_BF16;
     switch (d) {
-    case 32: return bf ? launch_typed<32, __nv_bfloat16>(p, n_chunk_max, h, st) : launch_typed<32, float>(p, n_chunk_max, h, st);
-    case 64: return bf ? launch_typed<64, __nv_bfloat16>(p, n_chunk_max, h, st) : launch_typed<64, float>(p, n_chunk_max, h, st);
-    default: return bf ? launch_typed<128, __nv_bfloat16>(p, n_chunk_max, h, st) : launch_typed<128, float>(p, n_chunk_max, h, st);
+    case 32:
+        return bf ? launch_typed<32, __nv_bfloat16>(p, n_chunk_max, h, st) : launch_typed<32, float>(p, n_chunk_max, h, st);
+    case 64:
+        return bf ? launch_typed<64, __nv_bfloat16>(p, n_chunk_max, h, st) : launch_typed<64, float>(p, n_chunk_max, h, st);
+    default:
+        return bf ? launch_typed<128, __nv_bfloat16>(p, n_chunk_max, h, st)
+                  : launch_typed<128, float>(p, n_chunk_max, h, st);
     }
 }
 

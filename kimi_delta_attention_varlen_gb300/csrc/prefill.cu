@@ -17,14 +17,20 @@
 //
 // Kernels (all on the caller's stream):
 //   1. chunk_table_kernel   one CTA: chunk offsets per sequence (prefix sum of
-//                           ceil(len/64)) and a longest-first sequence order.
+//                           ceil(len/64)), a per-chunk table (first token,
+//                           length), checkpoint offsets and a longest-first
+//                           sequence order.
 //   2. chunk_prep_kernel    one CTA per (chunk, head), fully parallel: every
 //                           quantity above that does not depend on S, written
-//                           to the workspace as one record per (chunk, head).
-//   3. state_pass_kernel    one CTA per (sequence, head, value slice): walks the
-//                           sequence's chunks in order with S in registers
-//                           (fp32 accumulators), double-buffering the records
-//                           into shared memory with bulk async copies.
+//                           to the workspace as one record per (chunk, head)
+//                           (chunk_prep.cu).
+//   3. the state pass, which walks each sequence's chunks in order:
+//      state_pass_tc_kernel one CTA per (sequence, head), S in tensor memory
+//                           (state_pass_tc.cu; head size 128, bf16 output,
+//                           enough pairs to fill the GPU), or
+//      state_pass_kernel    one CTA per (sequence, head, value slice), S in
+//                           registers (fp32 accumulators), double-buffering
+//                           the records into shared memory with bulk copies.
 // All products run on the tensor cores (bf16 operands, fp32 accumulation).
 //
 // Exponent ranges.  Factors e^{G_i - G_j} are split through a reference row:
@@ -260,7 +266,8 @@ state_pass_kernel(PassParams p)
 #pragma unroll
             for (int n = 0; n < 8; ++n) {
                 const uint32_t u0 = *reinterpret_cast<const uint32_t *>(ut + swz_off<128>(vl0 + gid, 8 * n + 2 * tig));
-                const uint32_t u1 = *reinterpret_cast<const uint32_t *>(ut + swz_off<128>(vl0 + gid + 8, 8 * n + 2 * tig));
+                const uint32_t u1 =
+                    *reinterpret_cast<const uint32_t *>(ut + swz_off<128>(vl0 + gid + 8, 8 * n + 2 * tig));
                 x[n][0] = bf16_lo(u0) - x[n][0];
                 x[n][1] = bf16_hi(u0) - x[n][1];
                 x[n][2] = bf16_lo(u1) - x[n][2];
@@ -281,7 +288,8 @@ state_pass_kernel(PassParams p)
             for (int ks = 0; ks < 4; ++ks) {
                 if (ks <= tp) {
                     uint32_t ba[4];
-                    ldmatrix_x4(ba, smem_u32(sb + R::AQK + swz_off<128>(16 * tp + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
+                    ldmatrix_x4(ba, smem_u32(sb + R::AQK +
+                                             swz_off<128>(16 * tp + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
                     mma_bf16(y[2 * tp], va[ks], ba[0], ba[1]);
                     mma_bf16(y[2 * tp + 1], va[ks], ba[2], ba[3]);
                 }
@@ -326,7 +334,8 @@ state_pass_kernel(PassParams p)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     uint32_t bk[4];
-                    ldmatrix_x4_trans(bk, smem_u32(sb + R::KT + tile_off<D, C>(16 * ks + ri + 8 * (mi & 1), 16 * np + 8 * (mi >> 1))));
+                    ldmatrix_x4_trans(bk, smem_u32(sb + R::KT + tile_off<D, C>(16 * ks + ri + 8 * (mi & 1),
+                                                                                 16 * np + 8 * (mi >> 1))));
                     mma_bf16(s[2 * np], va[ks], bk[0], bk[1]);
                     mma_bf16(s[2 * np + 1], va[ks], bk[2], bk[3]);
                 }

@@ -242,7 +242,8 @@ template <int D, typename IO, typename IdxT> cudaError_t launch_typed(const Veri
 template <int D> cudaError_t launch_d(const VerifyArgs &a, cudaStream_t st)
 {
     const bool bf = a.io_dtype == KDA_BF16, i64 = a.idx_type == KDA_I64;
-    if (bf) return i64 ? launch_typed<D, __nv_bfloat16, int64_t>(a, st) : launch_typed<D, __nv_bfloat16, int32_t>(a, st);
+    if (bf)
+        return i64 ? launch_typed<D, __nv_bfloat16, int64_t>(a, st) : launch_typed<D, __nv_bfloat16, int32_t>(a, st);
     return i64 ? launch_typed<D, float, int64_t>(a, st) : launch_typed<D, float, int32_t>(a, st);
 }
 

@@ -5,7 +5,8 @@ Outputs: |d| <= 1e-5 * S (+ half a bf16 step of |y| for bf16 outputs), S = |bias
 sum |w x| the magnitude of the terms (fp32 accumulation of at most five terms, the
 SiLU's slope is below 1.1, and its fast exponential and division add a few ulps of
 |y|, far below 1e-5 S; for bf16 outputs the sigmoid comes from one hardware tanh,
-relative error about 2^-11, i.e. |y| 2^-12, inside the half bf16 step allowed).  States hold inputs: bit for bit (bf16 states of fp32
+relative error about 2^-11, i.e. |y| 2^-12, inside the half bf16 step allowed).
+States hold inputs: bit for bit (bf16 states of fp32
 inputs round to nearest even, as the oracle's cast)."""
 import numpy as np
 import pytest
