@@ -9,11 +9,13 @@
 // plus the state-pass operands Q~ = scale q e^G, K~ = k e^{G_last - G} and
 // gamma = e^{G_last}.
 //
-// GPU mapping: one CTA (8 warps) per (chunk, head), two CTAs per SM.  All
-// global loads of the chunk are issued up front: q/k/v rows by cp.async into
-// their operand tiles, each warp's 8 consecutive g rows into registers, where
-// the in-chunk cumulative sum runs (warp totals are exchanged once through
-// shared memory).  The gated Gram products and W, U run on the tensor cores
+// GPU mapping: one CTA (8 warps) per (chunk, head), three CTAs per SM for
+// bf16 inputs (two for fp32, whose row pass holds more registers).  All
+// global loads of the chunk are issued up front: q/k rows by cp.async into
+// their operand tiles, v rows into L2 only (they move to shared memory after
+// the Gram products, into the k R tile), and each warp's 8 consecutive g rows
+// into registers, where the in-chunk cumulative sum runs (warp totals are
+// exchanged once through shared memory).  The gated Gram products and W, U run on the tensor cores
 // (bf16 operands, fp32 accumulate); W and U come from block forward
 // substitution on (I + A_kk), computed in place over their right-hand sides:
 // only the four 16x16 diagonal inverses are formed (fp32), every product is an
@@ -39,12 +41,13 @@ constexpr int kWarps = kThreads / 32;
 template <int D> struct PrepSmem {
     static constexpr int TILE = C * D * 2;                 // bf16 [64][D]
     static constexpr int XT = 16 * D * 2;                  // bf16 [16][D]
-    // Matrix region: A_kk bf16, T_diag bf16, the diagonal blocks of A_kk in fp32
-    // and the two substitution tiles X_W, X_U.  Before the Gram products it holds
-    // the cumulative-sum exchange (warp totals and first rows, fp32 [12][D]).
-    static constexpr int AB = 0;                           // A_kk bf16 [64][64]
-    static constexpr int TD = AB + C * C * 2;              // diag(T_00..T_33) bf16 [64][64]
-    static constexpr int AD = TD + C * C * 2;              // A_II fp32 [4][16][17]
+    // Matrix region: the six off-diagonal blocks of A_kk (bf16), the four diagonal
+    // blocks of T (bf16), the diagonal blocks of A_kk in fp32 and the two substitution
+    // tiles X_W, X_U.  Before the Gram products it holds the cumulative-sum exchange
+    // (warp totals and first rows, fp32 [12][D]).
+    static constexpr int AB = 0;                           // A_IK (K < I) bf16 [6][16][16]
+    static constexpr int TD = AB + 6 * 512;                // T_II bf16 [4][16][16]
+    static constexpr int AD = TD + 4 * 512;                // A_II fp32 [4][16][17]
     static constexpr int XW = (AD + 4 * 16 * 17 * 4 + 127) / 128 * 128;
     static constexpr int XU = XW + XT;
     static constexpr int SUMS = 0;                         // fp32 [8][D] warp totals, [4][D] first rows
@@ -52,12 +55,18 @@ template <int D> struct PrepSmem {
     static constexpr int MREG = (MREG0 + 127) / 128 * 128;
     static constexpr int KP = MREG;      // k P: Gram A operand, W right-hand side -> W
     static constexpr int QP = KP + TILE; // q P: Gram A operand -> U^T staging [D][64]
-    static constexpr int KR = QP + TILE; // k R: Gram B operand
-    static constexpr int VS = KR + TILE; // v (bf16): U right-hand side -> U
-    static constexpr int TAB = VS + TILE;                  // L[4][D] fp32, F[6][D] bf16
+    static constexpr int KR = QP + TILE; // k R: Gram B operand -> v (bf16), the U right-hand side -> U
+    static constexpr int TAB = KR + TILE;                  // L[4][D] fp32, F[6][D] bf16
     static constexpr int BETA = TAB + 4 * D * 4 + 6 * D * 2;  // beta [64]
     static constexpr int BYTES = BETA + C * 4;
 };
+
+// Byte offset of element (r, c) (0..15) of 16x16 bf16 block `blk`: 32-byte rows, the two
+// 16-byte halves swapped on every other group of four rows (conflict-free ldmatrix).
+__device__ __forceinline__ uint32_t blk_off(int blk, int r, int c)
+{
+    return static_cast<uint32_t>(blk * 512 + r * 32 + ((((c >> 3) ^ (r >> 2)) & 1) << 4) + ((c & 7) << 1));
+}
 
 // CPL io elements of one row, kept packed in registers until used.
 template <typename IO, int N> struct Slice {
@@ -157,7 +166,7 @@ __device__ __forceinline__ float pick4(const float v0, const float v1, const flo
 }
 
 template <int D, typename IO>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, sizeof(IO) == 2 ? 3 : 2)  // bf16: 3 CTAs per SM (≈69 KB smem each)
 chunk_prep_kernel(PrepParams p)
 {
     using SM = PrepSmem<D>;
@@ -192,7 +201,7 @@ chunk_prep_kernel(PrepParams p)
     const int I = warp >> 1;
     const int cb = lane * CPL;
     constexpr bool kStage = sizeof(IO) == 2;  // bf16 rows are staged into their swizzled tiles
-    Slice<IO, CPL> rq[kStage ? 1 : PRE], rk[kStage ? 1 : PRE], rv[kStage ? 1 : PRE];
+    Slice<IO, CPL> rq[kStage ? 1 : PRE], rk[kStage ? 1 : PRE];
     auto load_rows = [&](int j0) {
 #pragma unroll
         for (int j = 0; j < PRE; ++j) {
@@ -201,15 +210,13 @@ chunk_prep_kernel(PrepParams p)
                 const int64_t off = ((t0 + i) * H + h) * D + cb;
                 rq[j].load(qg + off);
                 rk[j].load(kg + off);
-                rv[j].load(vg + off);
             } else {
                 rq[j].zero();
                 rk[j].zero();
-                rv[j].zero();
             }
         }
     };
-    if constexpr (kStage) {  // q -> QP, k -> KP, v -> VS tiles, 16-byte chunks, zeros past the end
+    if constexpr (kStage) {  // q -> QP, k -> KP tiles, 16-byte chunks, zeros past the end
         constexpr int CH = D / 8;    // 16-byte chunks per row
 #pragma unroll
         for (int e = tid; e < C * CH; e += kThreads) {
@@ -220,7 +227,6 @@ chunk_prep_kernel(PrepParams p)
             const uint32_t nb = i < len ? 16u : 0u;
             cp_async16(smem_u32(smem + SM::QP + so), qg + off, nb);
             cp_async16(smem_u32(smem + SM::KP + so), kg + off, nb);
-            cp_async16(smem_u32(smem + SM::VS + so), vg + off, nb);
         }
     } else {
         load_rows(0);
@@ -236,6 +242,7 @@ chunk_prep_kernel(PrepParams p)
         }
     }
     if (tid < C) sBeta[tid] = tid < len ? p.beta[(t0 + tid) * H + h] : 0.f;
+    if (tid < len) prefetch_l2(vg + ((t0 + tid) * H + h) * D, D * sizeof(IO));  // v is staged after the Gram
 
     // in-chunk cumulative sum of g per channel, in log2 units: inside the warp's
     // rows in registers, then across warps through their totals
@@ -349,14 +356,13 @@ chunk_prep_kernel(PrepParams p)
         for (int j = 0; j < PRE; ++j) {
             const int i = r0 + j0 + j;
             const uint32_t o = tile_off<D, C>(i, cb);
-            float qv[CPL], kv[CPL], vv[CPL];
+            float qv[CPL], kv[CPL];
             if constexpr (kStage) {
                 load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::QP + o), qv);
                 load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::KP + o), kv);
             } else {
                 rq[j].get(qv);
                 rk[j].get(kv);
-                rv[j].get(vv);
             }
             float nq, nk;
             if constexpr (kStage) {
@@ -393,7 +399,6 @@ chunk_prep_kernel(PrepParams p)
             store_bf16<CPL>(smem + SM::KP, o, kp);  // each lane rewrites exactly the bytes it read
             store_bf16<CPL>(smem + SM::QP, o, qp);
             store_bf16<CPL>(smem + SM::KR, o, kr);
-            if constexpr (!kStage) store_bf16<CPL>(smem + SM::VS, o, vv);
             store_bf16<CPL>(rec + R::QT, o, qt);
             store_bf16<CPL>(rec + R::KT, o, kt);
         }
@@ -477,7 +482,9 @@ chunk_prep_kernel(PrepParams p)
                         const float bi = sBeta[i];
                         const float y0 = j < i ? acc[u][nt][2 * hr] * bi : 0.f;
                         const float y1 = j + 1 < i ? acc[u][nt][2 * hr + 1] * bi : 0.f;
-                        *reinterpret_cast<uint32_t *>(smem + SM::AB + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
+                        if (I != J)
+                            *reinterpret_cast<uint32_t *>(smem + SM::AB + blk_off(fslot(I, J), i - 16 * I, j - 16 * J)) =
+                                pack_bf16x2(y0, y1);
                         if (d) {  // rows of 17 floats: scalar stores (odd rows are not 8-byte aligned)
                             d[(i - 16 * I) * 17 + (j - 16 * J)] = y0;
                             d[(i - 16 * I) * 17 + (j - 16 * J) + 1] = y1;
@@ -503,6 +510,26 @@ chunk_prep_kernel(PrepParams p)
     }
     __syncthreads();
 
+    // v -> the k R tile (free after the Gram products), bf16, zeros past the end; its
+    // latency overlaps the diagonal inverses (the rows were prefetched into L2)
+    if constexpr (kStage) {
+        constexpr int CH = D / 8;
+#pragma unroll
+        for (int e = tid; e < C * CH; e += kThreads) {
+            const int i = e / CH, ch = e % CH;
+            const int ii = i < len ? i : 0;
+            cp_async16(smem_u32(smem + SM::KR + tile_off<D, C>(i, 8 * ch)), vg + ((t0 + ii) * H + h) * D + 8 * ch,
+                       i < len ? 16u : 0u);
+        }
+    } else {
+#pragma unroll
+        for (int e = tid; e < C * (D / 4); e += kThreads) {
+            const int i = e / (D / 4), c4 = 4 * (e % (D / 4));
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            if (i < len) load_slice<IO, 4>(vg + ((t0 + i) * H + h) * D + c4, x);
+            store_bf16<4>(smem + SM::KR, tile_off<D, C>(i, c4), x);
+        }
+    }
     // ---- 4. inverses of the diagonal blocks, T_II = (I + A_II)^-1, fp32 forward substitution ----
     if (warp < 4 && lane < 16) {  // one column per lane
         const int I = warp, j = lane;
@@ -517,9 +544,9 @@ chunk_prep_kernel(PrepParams p)
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            *reinterpret_cast<uint16_t *>(smem + SM::TD + swz_off<128>(16 * I + i, 16 * I + j)) =
-                f32_to_bf16_bits(tcol[i]);
+            *reinterpret_cast<uint16_t *>(smem + SM::TD + blk_off(I, i, j)) = f32_to_bf16_bits(tcol[i]);
     }
+    cp_async_wait_all();  // v has landed (each thread its own copies; the barrier publishes them)
     __syncthreads();
 
     // ---- 5. W = (I + A)^-1 diag(beta) K e^G and U = (I + A)^-1 diag(beta) V, by block
@@ -545,7 +572,7 @@ chunk_prep_kernel(PrepParams p)
         // per-element branches on the matrix kind).
         auto substitute = [&](auto is_u_tag) {
             constexpr bool kU = decltype(is_u_tag)::value;
-            char *ytile = smem + (kU ? SM::VS : SM::KP);  // base rows in, Y = U or W rows out, [64][D] bf16
+            char *ytile = smem + (kU ? SM::KR : SM::KP);  // base rows in, Y = U or W rows out, [64][D] bf16
             char *xtile = smem + (kU ? SM::XU : SM::XW);  // X_I, [16][D] bf16
             char *utile = smem + SM::QP;                  // U^T [D][64] bf16, 128-byte swizzled rows
 #pragma unroll
@@ -555,8 +582,7 @@ chunk_prep_kernel(PrepParams p)
 #pragma unroll
                     for (int K = 0; K < I; ++K) {
                         uint32_t a[4];
-                        ldmatrix_x4(a, smem_u32(smem + SM::AB +
-                                                swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * K + 8 * (mi >> 1))));
+                        ldmatrix_x4(a, smem_u32(smem + SM::AB + blk_off(fslot(I, K), ri + 8 * (mi & 1), 8 * (mi >> 1))));
 #pragma unroll
                         for (int np = 0; np < NP; ++np) {
                             uint32_t b[4];
@@ -590,8 +616,7 @@ chunk_prep_kernel(PrepParams p)
                 {
                     float acc[2 * NP][4] = {};
                     uint32_t a[4];
-                    ldmatrix_x4(a, smem_u32(smem + SM::TD +
-                                            swz_off<128>(16 * I + ri + 8 * (mi & 1), 16 * I + 8 * (mi >> 1))));
+                    ldmatrix_x4(a, smem_u32(smem + SM::TD + blk_off(I, ri + 8 * (mi & 1), 8 * (mi >> 1))));
 #pragma unroll
                     for (int np = 0; np < NP; ++np) {
                         uint32_t b[4];

@@ -220,46 +220,45 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
                     store8(dst + (j * RPP + rip) * D + c0, sn);
                 }
             }
-            cur = nxt;
-            continue;
-        }
+        } else {
 #pragma unroll
-        for (int j = 0; j < ROWS; ++j) {
-            const int vi = j * RPP + rip;
-            float st[8];
-            if (valid) {
-                if constexpr (V16 == 1) {
-                    const uint4 a = slots[((s * ROWS + j) * V16) * THREADS + tid];
-                    st[0] = bf16_lo(a.x); st[1] = bf16_hi(a.x); st[2] = bf16_lo(a.y); st[3] = bf16_hi(a.y);
-                    st[4] = bf16_lo(a.z); st[5] = bf16_hi(a.z); st[6] = bf16_lo(a.w); st[7] = bf16_hi(a.w);
+            for (int j = 0; j < ROWS; ++j) {
+                const int vi = j * RPP + rip;
+                float st[8];
+                if (valid) {
+                    if constexpr (V16 == 1) {
+                        const uint4 a = slots[((s * ROWS + j) * V16) * THREADS + tid];
+                        st[0] = bf16_lo(a.x); st[1] = bf16_hi(a.x); st[2] = bf16_lo(a.y); st[3] = bf16_hi(a.y);
+                        st[4] = bf16_lo(a.z); st[5] = bf16_hi(a.z); st[6] = bf16_lo(a.w); st[7] = bf16_hi(a.w);
+                    } else {
+                        const uint4 a = slots[((s * ROWS + j) * V16) * THREADS + tid];
+                        const uint4 b = slots[((s * ROWS + j) * V16 + 1) * THREADS + tid];
+                        st[0] = __uint_as_float(a.x); st[1] = __uint_as_float(a.y);
+                        st[2] = __uint_as_float(a.z); st[3] = __uint_as_float(a.w);
+                        st[4] = __uint_as_float(b.x); st[5] = __uint_as_float(b.y);
+                        st[6] = __uint_as_float(b.z); st[7] = __uint_as_float(b.w);
+                    }
                 } else {
-                    const uint4 a = slots[((s * ROWS + j) * V16) * THREADS + tid];
-                    const uint4 b = slots[((s * ROWS + j) * V16 + 1) * THREADS + tid];
-                    st[0] = __uint_as_float(a.x); st[1] = __uint_as_float(a.y);
-                    st[2] = __uint_as_float(a.z); st[3] = __uint_as_float(a.w);
-                    st[4] = __uint_as_float(b.x); st[5] = __uint_as_float(b.y);
-                    st[6] = __uint_as_float(b.z); st[7] = __uint_as_float(b.w);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) st[c] = 0.f;
                 }
-            } else {
+                float a = 0.f, b = 0.f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) st[c] = 0.f;
-            }
-            float a = 0.f, b = 0.f;
+                for (int c = 0; c < 8; ++c) {
+                    a += ke[c] * st[c];
+                    b += qe[c] * st[c];
+                }
+                a = group_sum<LPR>(a);
+                b = group_sum<LPR>(b);
+                const float u = cur.beta * (cur.v[j] - a);
+                if (valid) {
+                    float sn[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                a += ke[c] * st[c];
-                b += qe[c] * st[c];
+                    for (int c = 0; c < 8; ++c) sn[c] = eg[c] * st[c] + kh[c] * u;
+                    store8(dst + vi * D + c0, sn);
+                }
+                if (lr == 0) out[it * D + vi] = from_f32<IO>(scale * (b + qk * u));
             }
-            a = group_sum<LPR>(a);
-            b = group_sum<LPR>(b);
-            const float u = cur.beta * (cur.v[j] - a);
-            if (valid) {
-                float sn[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) sn[c] = eg[c] * st[c] + kh[c] * u;
-                store8(dst + vi * D + c0, sn);
-            }
-            if (lr == 0) out[it * D + vi] = from_f32<IO>(scale * (b + qk * u));
         }
         cur = nxt;
     }
