@@ -15,18 +15,20 @@
 // their operand tiles, v rows into L2 only (they move to shared memory after
 // the Gram products, into the k R tile), and each warp's 8 consecutive g rows
 // into registers, where the in-chunk cumulative sum runs (warp totals are
-// exchanged once through shared memory).  The gated Gram products and W, U run on the tensor cores
-// (bf16 operands, fp32 accumulate); W and U come from block forward
-// substitution on (I + A_kk), computed in place over their right-hand sides:
-// only the four 16x16 diagonal inverses are formed (fp32), every product is an
-// MMA.  W and U^T leave through two bulk copies.
+// exchanged once through shared memory).  The gated Gram products and W, U
+// run on the tensor cores (bf16 operands, fp32 accumulate).  T' = (I + A_kk)^-1
+// diag(beta) is formed blockwise: the four 16x16 diagonal inverses by fp32
+// forward substitution, the six blocks below them by MMAs (T'_IJ = -T_II
+// sum_K A_IK T'_KJ); then W = T' (K e^G) and U = T' V are plain block
+// products, written in place over their right-hand sides.  W and U^T leave
+// through two bulk copies.
 //
 // Exponents: e^{G_i - G_j} = P_i F_IJ R_j with P_i = e^{G_i - G_mI},
 // R_j = e^{G_mJ - G_j} (m = midpoint of the 16-row block) and F_IJ =
 // e^{G_mI - G_mJ} <= 1 applied to the A fragments; P and R each span at most 8
-// tokens of decay.  beta is folded into the substitution's right-hand sides and
-// e^G = P L_I (L_I = e^{G_mI}), so neither beta V nor beta k e^G needs a tile
-// of its own.
+// tokens of decay.  beta is folded into the columns of T' and e^G = P L_K
+// (L_K = e^{G_mK}) into the fragments of the k P tile, so neither beta V nor
+// beta k e^G needs a tile of its own.
 #include <type_traits>
 
 #include "prefill_common.cuh"
@@ -40,18 +42,20 @@ constexpr int kWarps = kThreads / 32;
 
 template <int D> struct PrepSmem {
     static constexpr int TILE = C * D * 2;                 // bf16 [64][D]
-    static constexpr int XT = 16 * D * 2;                  // bf16 [16][D]
-    // Matrix region: the six off-diagonal blocks of A_kk (bf16), the four diagonal
-    // blocks of T (bf16), the diagonal blocks of A_kk in fp32 and the two substitution
-    // tiles X_W, X_U.  Before the Gram products it holds the cumulative-sum exchange
-    // (warp totals and first rows, fp32 [12][D]).
+    // Matrix region: the six off-diagonal blocks of A_kk (bf16), the diagonal blocks of
+    // T (bf16, as they are and column-scaled by beta), the six blocks of T' below them,
+    // three 16x16 scratch blocks and the diagonal blocks of A_kk in fp32.  Before the
+    // Gram products it holds the cumulative-sum exchange (warp totals and first rows,
+    // fp32 [12][D]).
     static constexpr int AB = 0;                           // A_IK (K < I) bf16 [6][16][16]
     static constexpr int TD = AB + 6 * 512;                // T_II bf16 [4][16][16]
-    static constexpr int AD = TD + 4 * 512;                // A_II fp32 [4][16][17]
-    static constexpr int XW = (AD + 4 * 16 * 17 * 4 + 127) / 128 * 128;
-    static constexpr int XU = XW + XT;
+    static constexpr int TS = TD + 4 * 512;                // T_II diag(beta_I) bf16 [4][16][16]
+    static constexpr int TO = TS + 4 * 512;                // T'_IJ (J < I) bf16 [6][16][16]
+    static constexpr int SCR = TO + 6 * 512;               // per-warp 16x16 bf16 scratch [3]
+    static constexpr int AD = SCR + 3 * 512;               // A_II fp32 [4][16][17]
+    static constexpr int MEND = AD + 4 * 16 * 17 * 4;
     static constexpr int SUMS = 0;                         // fp32 [8][D] warp totals, [4][D] first rows
-    static constexpr int MREG0 = XU + XT > 12 * D * 4 ? XU + XT : 12 * D * 4;
+    static constexpr int MREG0 = MEND > 12 * D * 4 ? MEND : 12 * D * 4;
     static constexpr int MREG = (MREG0 + 127) / 128 * 128;
     static constexpr int KP = MREG;      // k P: Gram A operand, W right-hand side -> W
     static constexpr int QP = KP + TILE; // q P: Gram A operand -> U^T staging [D][64]
@@ -530,7 +534,8 @@ chunk_prep_kernel(PrepParams p)
             store_bf16<4>(smem + SM::KR, tile_off<D, C>(i, c4), x);
         }
     }
-    // ---- 4. inverses of the diagonal blocks, T_II = (I + A_II)^-1, fp32 forward substitution ----
+    // ---- 4. inverses of the diagonal blocks, T_II = (I + A_II)^-1, fp32 forward substitution;
+    //         stored as they are (TD) and with their columns scaled by beta (TS) ----
     if (warp < 4 && lane < 16) {  // one column per lane
         const int I = warp, j = lane;
         const float *A = sAd + I * 16 * 17;
@@ -542,111 +547,131 @@ chunk_prep_kernel(PrepParams p)
             for (int kk = 0; kk < i; ++kk) acc -= A[i * 17 + kk] * tcol[kk];
             tcol[i] = acc;
         }
+        const float bj = sBeta[16 * I + j];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 16; ++i) {
             *reinterpret_cast<uint16_t *>(smem + SM::TD + blk_off(I, i, j)) = f32_to_bf16_bits(tcol[i]);
+            *reinterpret_cast<uint16_t *>(smem + SM::TS + blk_off(I, i, j)) = f32_to_bf16_bits(tcol[i] * bj);
+        }
+    }
+    __syncthreads();
+
+    // ---- 5. the off-diagonal blocks of T' = (I + A_kk)^-1 diag(beta):
+    //         T'_IJ = -T_II sum_{J<=K<I} A_IK T'_KJ.  Warp 0 forms (1,0), (2,0), (3,0), warp 1
+    //         (2,1), (3,1), warp 2 (3,2): each block needs only the diagonal blocks and the
+    //         warp's own earlier results. ----
+    if (warp < 3) {
+        char *scr = smem + SM::SCR + warp * 512;
+        auto tblock = [&](int I, int J) {
+            float x[2][4] = {};
+            for (int K = J; K < I; ++K) {
+                uint32_t a[4], b[4];
+                ldmatrix_x4(a, smem_u32(smem + SM::AB + blk_off(fslot(I, K), ri + 8 * (mi & 1), 8 * (mi >> 1))));
+                const int tb = K == J ? SM::TS + J * 512 : SM::TO + fslot(K, J) * 512;
+                ldmatrix_x4_trans(b, smem_u32(smem + tb + blk_off(0, ri + 8 * (mi & 1), 8 * (mi >> 1))));
+                mma_bf16(x[0], a, b[0], b[1]);
+                mma_bf16(x[1], a, b[2], b[3]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+                    *reinterpret_cast<uint32_t *>(scr + blk_off(0, gid + 8 * hr, 8 * nt + 2 * tig)) =
+                        pack_bf16x2(x[nt][2 * hr], x[nt][2 * hr + 1]);
+            __syncwarp();
+            float y[2][4] = {};
+            uint32_t a[4], b[4];
+            ldmatrix_x4(a, smem_u32(smem + SM::TD + blk_off(I, ri + 8 * (mi & 1), 8 * (mi >> 1))));
+            ldmatrix_x4_trans(b, smem_u32(scr + blk_off(0, ri + 8 * (mi & 1), 8 * (mi >> 1))));
+            mma_bf16(y[0], a, b[0], b[1]);
+            mma_bf16(y[1], a, b[2], b[3]);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+                    *reinterpret_cast<uint32_t *>(smem + SM::TO + blk_off(fslot(I, J), gid + 8 * hr, 8 * nt + 2 * tig)) =
+                        pack_bf16x2(-y[nt][2 * hr], -y[nt][2 * hr + 1]);
+            __syncwarp();  // the block is read by this warp's next block; scr is rewritten
+        };
+        if (warp == 0) {
+            tblock(1, 0);
+            tblock(2, 0);
+            tblock(3, 0);
+        } else if (warp == 1) {
+            tblock(2, 1);
+            tblock(3, 1);
+        } else {
+            tblock(3, 2);
+        }
     }
     cp_async_wait_all();  // v has landed (each thread its own copies; the barrier publishes them)
     __syncthreads();
 
-    // ---- 5. W = (I + A)^-1 diag(beta) K e^G and U = (I + A)^-1 diag(beta) V, by block
-    //         forward substitution: X_I = base_I - sum_{K<I} A_IK Y_K, Y_I = T_II X_I.
-    //         Warps 0-3: W, warps 4-7: U; each warp owns D / NW columns and, since
-    //         every product keeps columns apart, needs no other warp's results.
-    //         Y_I replaces base_I in its tile (k P -> W, v -> U); U^T is staged in
-    //         the q P tile in the record's layout. ----
+    // ---- 6. W = T' (K e^G) and U = T' V, block row I from blocks K <= I: warps 0-3 W,
+    //         warps 4-7 U, each warp D / NW columns.  The right-hand sides are read into
+    //         registers once (k P tile with e^G = P L_K applied to the fragments, or v), so
+    //         Y_I overwrites them in place; U^T is staged in the q P tile in the record's
+    //         layout. ----
     {
         constexpr int NW = D / 16 < 4 ? D / 16 : 4;  // warps per matrix with work
         constexpr int COLS = D / NW, NP = COLS / 16;
         const int q4 = warp & 3;
         const int c0 = q4 * COLS;
-        // Swizzled byte offset of column c0 + 8n + 2tig within any row r with r % 8 == gid.
-        // (64-row tiles and the 16-row X tile differ only in their slab stride.)
-        uint32_t colo[2 * NP], colx[2 * NP];
-#pragma unroll
-        for (int n = 0; n < 2 * NP; ++n) {
-            colo[n] = tile_off<D, C>(gid, c0 + 8 * n + 2 * tig) - gid * ROWB;
-            colx[n] = tile_off<D, 16>(gid, c0 + 8 * n + 2 * tig) - gid * ROWB;
-        }
-        // The whole substitution of one matrix, specialised at compile time (no
-        // per-element branches on the matrix kind).
-        auto substitute = [&](auto is_u_tag) {
+        auto product = [&](auto is_u_tag) {
             constexpr bool kU = decltype(is_u_tag)::value;
-            char *ytile = smem + (kU ? SM::KR : SM::KP);  // base rows in, Y = U or W rows out, [64][D] bf16
-            char *xtile = smem + (kU ? SM::XU : SM::XW);  // X_I, [16][D] bf16
+            char *ytile = smem + (kU ? SM::KR : SM::KP);  // right-hand sides in, Y = U or W rows out
             char *utile = smem + SM::QP;                  // U^T [D][64] bf16, 128-byte swizzled rows
+            uint32_t b[4][NP][4];
+#pragma unroll
+            for (int K = 0; K < 4; ++K)
+#pragma unroll
+                for (int np = 0; np < NP; ++np) {
+                    ldmatrix_x4_trans(b[K][np], smem_u32(ytile + tile_off<D, C>(16 * K + ri + 8 * (mi & 1),
+                                                                              c0 + 16 * np + 8 * (mi >> 1))));
+                    if constexpr (!kU) {  // row k of block K times L_K = e^{G_mK}, column gid of each n8 tile
+                        const float l0 = sL[K * D + c0 + 16 * np + gid], l1 = sL[K * D + c0 + 16 * np + 8 + gid];
+                        const uint32_t f0 = pack_bf16x2(l0, l0), f1 = pack_bf16x2(l1, l1);
+                        b[K][np][0] = mul_bf16x2(b[K][np][0], f0);
+                        b[K][np][1] = mul_bf16x2(b[K][np][1], f0);
+                        b[K][np][2] = mul_bf16x2(b[K][np][2], f1);
+                        b[K][np][3] = mul_bf16x2(b[K][np][3], f1);
+                    }
+                }
+            __syncwarp();  // every lane holds its fragments before Y overwrites the tile
 #pragma unroll
             for (int I = 0; I < 4; ++I) {
-                {
-                    float acc[2 * NP][4] = {};
+                float acc[2 * NP][4] = {};
 #pragma unroll
-                    for (int K = 0; K < I; ++K) {
-                        uint32_t a[4];
-                        ldmatrix_x4(a, smem_u32(smem + SM::AB + blk_off(fslot(I, K), ri + 8 * (mi & 1), 8 * (mi >> 1))));
-#pragma unroll
-                        for (int np = 0; np < NP; ++np) {
-                            uint32_t b[4];
-                            ldmatrix_x4_trans(b, smem_u32(ytile + tile_off<D, C>(16 * K + ri + 8 * (mi & 1),
-                                                                                 c0 + 16 * np + 8 * (mi >> 1))));
-                            mma_bf16(acc[2 * np], a, b[0], b[1]);
-                            mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
-                        }
-                    }
-                    const float bi[2] = {sBeta[16 * I + gid], sBeta[16 * I + gid + 8]};
-#pragma unroll
-                    for (int n = 0; n < 2 * NP; ++n) {
-                        float2 lf = make_float2(1.f, 1.f);
-                        if constexpr (!kU) lf = *reinterpret_cast<const float2 *>(sL + I * D + c0 + 8 * n + 2 * tig);
-#pragma unroll
-                        for (int hr = 0; hr < 2; ++hr) {
-                            const uint32_t rx = static_cast<uint32_t>(gid + 8 * hr) * ROWB;  // row within block I
-                            const uint32_t base = *reinterpret_cast<const uint32_t *>(
-                                ytile + static_cast<uint32_t>(16 * I) * ROWB + rx + colo[n]);
-                            float b0 = bi[hr] * bf16_lo(base), b1 = bi[hr] * bf16_hi(base);  // beta_i v_i or
-                            if constexpr (!kU) {                                                // beta_i k_i e^{G_i}
-                                b0 *= lf.x;
-                                b1 *= lf.y;
-                            }
-                            *reinterpret_cast<uint32_t *>(xtile + rx + colx[n]) =
-                                pack_bf16x2(b0 - acc[n][2 * hr], b1 - acc[n][2 * hr + 1]);
-                        }
-                    }
-                }
-                __syncwarp();  // X_I columns of this warp are complete (no other warp reads them)
-                {
-                    float acc[2 * NP][4] = {};
+                for (int K = 0; K <= I; ++K) {
                     uint32_t a[4];
-                    ldmatrix_x4(a, smem_u32(smem + SM::TD + blk_off(I, ri + 8 * (mi & 1), 8 * (mi >> 1))));
+                    const int tb = K == I ? SM::TS + I * 512 : SM::TO + fslot(I, K) * 512;
+                    ldmatrix_x4(a, smem_u32(smem + tb + blk_off(0, ri + 8 * (mi & 1), 8 * (mi >> 1))));
 #pragma unroll
                     for (int np = 0; np < NP; ++np) {
-                        uint32_t b[4];
-                        ldmatrix_x4_trans(b, smem_u32(xtile + tile_off<D, 16>(ri + 8 * (mi & 1),
-                                                                              c0 + 16 * np + 8 * (mi >> 1))));
-                        mma_bf16(acc[2 * np], a, b[0], b[1]);
-                        mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+                        mma_bf16(acc[2 * np], a, b[K][np][0], b[K][np][1]);
+                        mma_bf16(acc[2 * np + 1], a, b[K][np][2], b[K][np][3]);
                     }
+                }
 #pragma unroll
-                    for (int n = 0; n < 2 * NP; ++n) {
+                for (int n = 0; n < 2 * NP; ++n) {
+                    const uint32_t co = tile_off<D, C>(gid, c0 + 8 * n + 2 * tig) - gid * ROWB;
 #pragma unroll
-                        for (int hr = 0; hr < 2; ++hr) {
-                            const int i = 16 * I + gid + 8 * hr;
-                            const float y0 = acc[n][2 * hr], y1 = acc[n][2 * hr + 1];
-                            *reinterpret_cast<uint32_t *>(ytile + static_cast<uint32_t>(i) * ROWB + colo[n]) =
-                                pack_bf16x2(y0, y1);
-                            if constexpr (kU) {
-                                const int c = c0 + 8 * n + 2 * tig;
-                                *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
-                                *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);
-                            }
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int i = 16 * I + gid + 8 * hr;
+                        const float y0 = acc[n][2 * hr], y1 = acc[n][2 * hr + 1];
+                        *reinterpret_cast<uint32_t *>(ytile + static_cast<uint32_t>(i) * ROWB + co) = pack_bf16x2(y0, y1);
+                        if constexpr (kU) {
+                            const int c = c0 + 8 * n + 2 * tig;
+                            *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
+                            *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);
                         }
                     }
                 }
-                __syncwarp();  // Y_I columns of this warp are complete
             }
         };
         if (q4 < NW) {
-            if (warp >= 4) substitute(std::true_type{});
-            else substitute(std::false_type{});
+            if (warp >= 4) product(std::true_type{});
+            else product(std::false_type{});
         }
     }
     fence_proxy_async_smem();  // the W and U^T tiles are read by the bulk copies below
