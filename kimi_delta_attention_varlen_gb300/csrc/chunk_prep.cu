@@ -251,9 +251,20 @@ chunk_prep_kernel(PrepParams p)
     // in-chunk cumulative sum of g per channel, in log2 units: inside the warp's
     // rows in registers, then across warps through their totals
 #pragma unroll
-    for (int j = 0; j < ROWS; ++j)
+    for (int j = 0; j < ROWS; ++j) {
+        if constexpr (CPL % 2 == 0) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) gr[j][c] = j == 0 ? gr[0][c] * kLog2e : fmaf(gr[j][c], kLog2e, gr[j - 1][c]);
+            for (int c = 0; c < CPL; c += 2) {
+                const float2 x = make_float2(gr[j][c], gr[j][c + 1]), l2 = make_float2(kLog2e, kLog2e);
+                const float2 y = j == 0 ? mul2(x, l2) : fma2(x, l2, make_float2(gr[j - 1][c], gr[j - 1][c + 1]));
+                gr[j][c] = y.x;
+                gr[j][c + 1] = y.y;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) gr[j][c] = j == 0 ? gr[0][c] * kLog2e : fmaf(gr[j][c], kLog2e, gr[j - 1][c]);
+        }
+    }
     st_f32<CPL>(sSum + warp * D + cb, gr[ROWS - 1]);
     if (warp & 1) st_f32<CPL>(sSum + (kWarps + I) * D + cb, gr[0]);  // row 16 I + 8: the block midpoint
     cp_async_wait_all();
@@ -284,9 +295,19 @@ chunk_prep_kernel(PrepParams p)
         for (int c = 0; c < CPL; ++c) glast[c] = run[c];
     }
 #pragma unroll
-    for (int j = 0; j < ROWS; ++j)
+    for (int j = 0; j < ROWS; ++j) {
+        if constexpr (CPL % 2 == 0) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) gr[j][c] += off[c];
+            for (int c = 0; c < CPL; c += 2) {
+                const float2 x = add2(make_float2(gr[j][c], gr[j][c + 1]), make_float2(off[c], off[c + 1]));
+                gr[j][c] = x.x;
+                gr[j][c + 1] = x.y;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) gr[j][c] += off[c];
+        }
+    }
 
     // per-channel factors: F_IJ (warps 0-5, one (I, J) each), L_I = e^{G_mI}
     // (even warps), gamma = e^{G_last} (warp 7, to the record)
@@ -326,14 +347,26 @@ chunk_prep_kernel(PrepParams p)
             float qv[CPL], kv[CPL];
             load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::QP + o), qv);
             load_slice<__nv_bfloat16, CPL>(reinterpret_cast<const __nv_bfloat16 *>(smem + SM::KP + o), kv);
-            float sq = 0.f, sk = 0.f;
+            if constexpr (CPL % 2 == 0) {
+                float2 sq = make_float2(0.f, 0.f), sk = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                sq += qv[c] * qv[c];
-                sk += kv[c] * kv[c];
+                for (int c = 0; c < CPL; c += 2) {
+                    const float2 q2 = make_float2(qv[c], qv[c + 1]), k2 = make_float2(kv[c], kv[c + 1]);
+                    sq = fma2(q2, q2, sq);
+                    sk = fma2(k2, k2, sk);
+                }
+                vsum[2 * j] = sq.x + sq.y;
+                vsum[2 * j + 1] = sk.x + sk.y;
+            } else {
+                float sq = 0.f, sk = 0.f;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    sq += qv[c] * qv[c];
+                    sk += kv[c] * kv[c];
+                }
+                vsum[2 * j] = sq;
+                vsum[2 * j + 1] = sk;
             }
-            vsum[2 * j] = sq;
-            vsum[2 * j + 1] = sk;
         }
 #pragma unroll
         for (int mask = 16, half = ROWS; mask >= 2; mask >>= 1, half >>= 1) {
@@ -388,17 +421,36 @@ chunk_prep_kernel(PrepParams p)
                 nk = p.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
             }
             float kp[CPL], qp[CPL], kr[CPL], qt[CPL], kt[CPL];
+            if constexpr (CPL % 2 == 0) {  // channel pairs through the packed fp32x2 instructions
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                const float gi = gr[j0 + j][c];
-                const float P = ex2_approx(gi - gmi[c]);   // e^{G_i - G_m}
-                const float Rr = ex2_approx(gmi[c] - gi);  // e^{G_m - G_i}
-                const float qh = qv[c] * nq, kh = kv[c] * nk;
-                kp[c] = kh * P;
-                qp[c] = qh * P;
-                kr[c] = kh * Rr;
-                qt[c] = qp[c] * ls[c];
-                kt[c] = kr[c] * zz[c];
+                for (int c = 0; c < CPL; c += 2) {
+                    const float d0 = gr[j0 + j][c] - gmi[c], d1 = gr[j0 + j][c + 1] - gmi[c + 1];
+                    const float2 P = make_float2(ex2_approx(d0), ex2_approx(d1));     // e^{G_i - G_m}
+                    const float2 Rr = make_float2(ex2_approx(-d0), ex2_approx(-d1));  // e^{G_m - G_i}
+                    const float2 qh = mul2(make_float2(qv[c], qv[c + 1]), make_float2(nq, nq));
+                    const float2 kh = mul2(make_float2(kv[c], kv[c + 1]), make_float2(nk, nk));
+                    const float2 kp2 = mul2(kh, P), qp2 = mul2(qh, P), kr2 = mul2(kh, Rr);
+                    const float2 qt2 = mul2(qp2, make_float2(ls[c], ls[c + 1]));
+                    const float2 kt2 = mul2(kr2, make_float2(zz[c], zz[c + 1]));
+                    kp[c] = kp2.x; kp[c + 1] = kp2.y;
+                    qp[c] = qp2.x; qp[c + 1] = qp2.y;
+                    kr[c] = kr2.x; kr[c + 1] = kr2.y;
+                    qt[c] = qt2.x; qt[c + 1] = qt2.y;
+                    kt[c] = kt2.x; kt[c + 1] = kt2.y;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    const float gi = gr[j0 + j][c];
+                    const float P = ex2_approx(gi - gmi[c]);   // e^{G_i - G_m}
+                    const float Rr = ex2_approx(gmi[c] - gi);  // e^{G_m - G_i}
+                    const float qh = qv[c] * nq, kh = kv[c] * nk;
+                    kp[c] = kh * P;
+                    qp[c] = qh * P;
+                    kr[c] = kh * Rr;
+                    qt[c] = qp[c] * ls[c];
+                    kt[c] = kr[c] * zz[c];
+                }
             }
             store_bf16<CPL>(smem + SM::KP, o, kp);  // each lane rewrites exactly the bytes it read
             store_bf16<CPL>(smem + SM::QP, o, qp);
@@ -539,14 +591,16 @@ chunk_prep_kernel(PrepParams p)
     if (warp < 4 && lane < 16) {  // one column per lane
         const int I = warp, j = lane;
         const float *A = sAd + I * 16 * 17;
+        // Right-looking: once tcol[k] is final it is subtracted from every later row, so
+        // row i still accumulates its terms in the order k = 0, 1, .., i - 1 but the
+        // dependent chain is one step per row instead of one per term.
         float tcol[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = i == j ? 1.f : 0.f;
+        for (int i = 0; i < 16; ++i) tcol[i] = i == j ? 1.f : 0.f;
 #pragma unroll
-            for (int kk = 0; kk < i; ++kk) acc -= A[i * 17 + kk] * tcol[kk];
-            tcol[i] = acc;
-        }
+        for (int kk = 0; kk < 15; ++kk)
+#pragma unroll
+            for (int i = kk + 1; i < 16; ++i) tcol[i] -= A[i * 17 + kk] * tcol[kk];
         const float bj = sBeta[16 * I + j];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {

@@ -8,11 +8,12 @@
 // code * scale in the active row's dtype.  Codes are decided with correctly
 // rounded fp32 division and a round-to-nearest-even conversion.
 //
-// Both kernels are HBM-bound copies: one CTA per (pair, head) moves one
-// [V][K] state block (fp32 64 KB or bf16 32 KB at V = K = 128) and its
-// 16 KB of codes.  Store stages the block in shared memory with 16-byte
-// asynchronous copies (one HBM read) for the column max and the codes; load
-// streams codes in and rows out with coalesced accesses.
+// Both kernels are HBM-bound copies of [V][K] state blocks (fp32 64 KB or
+// bf16 32 KB at V = K = 128) and their 16 KB of codes.  Store: one CTA per
+// (pair, head, key-column slice) stages its slice in shared memory with
+// 16-byte asynchronous copies (one HBM read) for the column max and the codes.
+// Load: one CTA per (pair, head) streams codes in and rows out with coalesced
+// accesses.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -25,8 +26,6 @@ template <typename IdxT> __device__ __forceinline__ int64_t idx_at(const void *p
 {
     return static_cast<int64_t>(static_cast<const IdxT *>(p)[s]);
 }
-
-constexpr int kStoreThreads = 256;
 
 // round_half_even(x / sc) clamped to [-127, 127], with x / sc the correctly
 // rounded fp32 quotient.  x * (1 / sc) lies within a few ulps (< 1e-4 for
@@ -42,43 +41,63 @@ __device__ __forceinline__ int quantize(float x, float sc, float rc)
     return q > 127 ? 127 : (q < -127 ? -127 : q);
 }
 
-template <int D, int THREADS> struct Geo {
-    static constexpr int K4 = D / 4;                                 // 4-column groups per row
-    static constexpr int RPP = THREADS / K4 < D ? THREADS / K4 : D;  // rows per pass of the CTA
-    static constexpr int NR = D / RPP;                               // rows per thread
-    static constexpr int ACTIVE = RPP * K4;                          // threads holding rows
-    static_assert(NR * RPP == D && K4 <= 32 && ACTIVE % 32 == 0, "geometry");
+// Store geometry: a [ROWS][COLS] slice of a state block, THREADS threads, each
+// holding 4 consecutive columns of NR rows spaced RPP apart.
+template <int ROWS, int COLS, int THREADS> struct Geo {
+    static constexpr int K4 = COLS / 4;                                    // 4-column groups per row
+    static constexpr int RPP = THREADS / K4 < ROWS ? THREADS / K4 : ROWS;  // rows per pass of the CTA
+    static constexpr int NR = ROWS / RPP;                                  // rows per thread
+    static constexpr int ACTIVE = RPP * K4;                                // threads holding rows
+    static_assert(NR * RPP == ROWS && K4 <= 32 && ACTIVE % 32 == 0, "geometry");
 };
 
-// One CTA per (pair, head): the block streams into shared memory (16-byte
-// asynchronous copies; one HBM read, three CTAs per SM at fp32 D = 128), then
-// the column max-abs and the codes are computed from there.
+// Column slices per block and threads per CTA of the store.  The max-abs runs over
+// the value rows of each key column, so column slices are independent: a CTA takes
+// one [V][K / NS] slice, which keeps more, smaller slices in flight per SM (fp32
+// blocks at K = 128: two 32 KB halves, six CTAs per SM; bf16 blocks stay whole).
+template <int D, typename ElemT> struct StoreCfg {
+    static constexpr int NS = D >= 128 && sizeof(ElemT) == 4 ? 2 : 1;
+    static constexpr int THREADS = 256;
+};
+
+// One CTA per (pair, head, column slice): the slice streams into shared memory
+// (16-byte asynchronous copies; one HBM read), then the column max-abs and the
+// codes are computed from there.
 template <int D, typename ElemT, typename IdxT>
-__global__ void __launch_bounds__(kStoreThreads)
+__global__ void __launch_bounds__(StoreCfg<D, ElemT>::THREADS)
 ckpt_store_kernel(const ElemT *__restrict__ active, int64_t n_rows, int64_t row_stride, int32_t H,
                   const void *__restrict__ src, const void *__restrict__ dst, int64_t n_slots,
                   int8_t *__restrict__ qdata, float *__restrict__ scale)
 {
-    using G = Geo<D, kStoreThreads>;
-    constexpr int BLK = D * D * static_cast<int>(sizeof(ElemT));  // bytes of one [V][K] block
+    constexpr int NS = StoreCfg<D, ElemT>::NS, THREADS = StoreCfg<D, ElemT>::THREADS, DS = D / NS;
+    constexpr int ES = static_cast<int>(sizeof(ElemT));
+    using G = Geo<D, DS, THREADS>;
+    constexpr int RB = DS * ES;        // bytes of one slice row
+    constexpr int BLK = D * RB;        // bytes of one [V][DS] slice
     extern __shared__ __align__(16) char smem[];
-    float(*part)[D] = reinterpret_cast<float(*)[D]>(smem + BLK);  // [warps][D] column maxima
+    float(*part)[DS] = reinterpret_cast<float(*)[DS]>(smem + BLK);  // [warps][DS] column maxima
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t pair = blockIdx.x / H;
-    const int h = static_cast<int>(blockIdx.x % H);
+    const int sl = static_cast<int>(blockIdx.x % NS);
+    const int64_t ph = blockIdx.x / NS;
+    const int64_t pair = ph / H;
+    const int h = static_cast<int>(ph % H);
     const int64_t r = idx_at<IdxT>(src, pair), c = idx_at<IdxT>(dst, pair);
     if (r < 0 || r >= n_rows || c < 0 || c >= n_slots) return;  // uniform over the CTA
-    const char *blk = reinterpret_cast<const char *>(active + r * row_stride + static_cast<int64_t>(h) * D * D);
+    const char *blk = reinterpret_cast<const char *>(active + r * row_stride + static_cast<int64_t>(h) * D * D +
+                                                     sl * DS);
 #pragma unroll 4
-    for (int e = tid; e < BLK / 16; e += kStoreThreads) cp_async16(smem_u32(smem + 16 * e), blk + 16 * e, 16u);
+    for (int e = tid; e < BLK / 16; e += THREADS) {
+        const int v = e / (RB / 16), ch = e % (RB / 16);
+        cp_async16(smem_u32(smem + v * RB + 16 * ch), blk + static_cast<int64_t>(v) * D * ES + 16 * ch, 16u);
+    }
     cp_async_wait_all();
     __syncthreads();
 
     const int cg = tid % G::K4, r0 = tid / G::K4;
     const bool act = tid < G::ACTIVE;  // (all threads unless the block has fewer rows)
     auto load4 = [&](int v, float x[4]) {
-        const char *p = smem + (v * D + 4 * cg) * static_cast<int>(sizeof(ElemT));
-        if constexpr (sizeof(ElemT) == 4) {
+        const char *p = smem + v * RB + 4 * cg * ES;
+        if constexpr (ES == 4) {
             const float4 a = *reinterpret_cast<const float4 *>(p);
             x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         } else {
@@ -104,7 +123,7 @@ ckpt_store_kernel(const ElemT *__restrict__ active, int64_t n_rows, int64_t row_
     if (lane < G::K4) *reinterpret_cast<float4 *>(&part[warp][4 * cg]) = make_float4(m[0], m[1], m[2], m[3]);
     __syncthreads();
 #pragma unroll
-    for (int w = 0; w < kStoreThreads / 32; ++w) {
+    for (int w = 0; w < THREADS / 32; ++w) {
         const float4 a = *reinterpret_cast<const float4 *>(&part[w][4 * cg]);
         m[0] = fmaxf(m[0], a.x); m[1] = fmaxf(m[1], a.y); m[2] = fmaxf(m[2], a.z); m[3] = fmaxf(m[3], a.w);
     }
@@ -115,7 +134,8 @@ ckpt_store_kernel(const ElemT *__restrict__ active, int64_t n_rows, int64_t row_
         rc[e] = __frcp_rn(sc[e]);
     }
     const int64_t sbase = (c * H + h) * static_cast<int64_t>(D);
-    if (r0 == 0) *reinterpret_cast<float4 *>(scale + sbase + 4 * cg) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+    const int col = sl * DS + 4 * cg;  // first key column of this thread
+    if (r0 == 0) *reinterpret_cast<float4 *>(scale + sbase + col) = make_float4(sc[0], sc[1], sc[2], sc[3]);
     if (!act) return;
     int8_t *qb = qdata + sbase * D;
 #pragma unroll
@@ -129,7 +149,7 @@ ckpt_store_kernel(const ElemT *__restrict__ active, int64_t n_rows, int64_t row_
             const int q = m[e] > 0.f ? quantize(x[e], sc[e], rc[e]) : 0;
             packed |= (static_cast<uint32_t>(q) & 0xffu) << (8 * e);
         }
-        *reinterpret_cast<uint32_t *>(qb + static_cast<int64_t>(v) * D + 4 * cg) = packed;
+        *reinterpret_cast<uint32_t *>(qb + static_cast<int64_t>(v) * D + col) = packed;
     }
 }
 
@@ -171,12 +191,13 @@ template <int D, typename ElemT, typename IdxT>
 cudaError_t store_typed(const CacheDesc &c, const void *src, const void *dst, int64_t count, int8_t *qdata,
                         float *scale, int64_t n_slots, cudaStream_t st)
 {
-    const int64_t blocks = count * c.h;
-    constexpr int smem = D * D * static_cast<int>(sizeof(ElemT)) + (kStoreThreads / 32) * D * 4;
+    using Cfg = StoreCfg<D, ElemT>;
+    const int64_t blocks = count * c.h * Cfg::NS;
+    constexpr int smem = D * (D / Cfg::NS) * static_cast<int>(sizeof(ElemT)) + (Cfg::THREADS / 32) * (D / Cfg::NS) * 4;
     auto kern = ckpt_store_kernel<D, ElemT, IdxT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(blocks), kStoreThreads, smem, st>>>(
+    kern<<<static_cast<unsigned>(blocks), Cfg::THREADS, smem, st>>>(
         static_cast<const ElemT *>(c.data), c.n_rows, c.row_stride, static_cast<int32_t>(c.h), src, dst, n_slots,
         qdata, scale);
     return cudaGetLastError();

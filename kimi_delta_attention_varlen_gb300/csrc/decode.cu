@@ -178,16 +178,18 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
             };
             float vals[2 * ROWS];
 #pragma unroll
-            for (int j = 0; j < ROWS; ++j) {
-                float st[8], a = 0.f, b = 0.f;
+            for (int j = 0; j < ROWS; ++j) {  // channel pairs through the packed fp32x2 instructions
+                float st[8];
+                float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
                 slice(j, st);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    a = fmaf(ke[c], st[c], a);
-                    b = fmaf(qe[c], st[c], b);
+                for (int c = 0; c < 8; c += 2) {
+                    const float2 s2 = make_float2(st[c], st[c + 1]);
+                    a = fma2(make_float2(ke[c], ke[c + 1]), s2, a);
+                    b = fma2(make_float2(qe[c], qe[c + 1]), s2, b);
                 }
-                vals[2 * j] = a;
-                vals[2 * j + 1] = b;
+                vals[2 * j] = a.x + a.y;
+                vals[2 * j + 1] = b.x + b.y;
             }
             const int lane = tid & 31;
 #pragma unroll
@@ -216,7 +218,12 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
                     float st[8], sn[8];
                     slice(j, st);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) sn[c] = fmaf(eg[c], st[c], kh[c] * u);
+                    for (int c = 0; c < 8; c += 2) {  // e^g S + k u: k u rounded, then one fma, per element
+                        const float2 r = fma2(make_float2(eg[c], eg[c + 1]), make_float2(st[c], st[c + 1]),
+                                              mul2(make_float2(kh[c], kh[c + 1]), make_float2(u, u)));
+                        sn[c] = r.x;
+                        sn[c + 1] = r.y;
+                    }
                     store8(dst + (j * RPP + rip) * D + c0, sn);
                 }
             }

@@ -61,6 +61,18 @@ __device__ __forceinline__ void store8_stream(void *base, int32_t dtype, int64_t
 
 constexpr int kVT = 8;  // draft tokens staged per group
 
+// S'[k][v] = e^{g_k} S[k][v] + k_k u_v on a lane's 8 channels of one row, as channel
+// pairs: k u rounded, then one fused multiply-add, per element as the scalar form.
+__device__ __forceinline__ void update_row(float s[8], const float2 e[4], const float2 kn[4], float u)
+{
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float2 r = fma2(e[c], make_float2(s[2 * c], s[2 * c + 1]), mul2(kn[c], make_float2(u, u)));
+        s[2 * c] = r.x;
+        s[2 * c + 1] = r.y;
+    }
+}
+
 template <int D, typename IO> struct VerifyLayout {
     static constexpr int ROW = D * static_cast<int>(sizeof(IO));
     static constexpr int Q = 0;
@@ -145,26 +157,29 @@ verify_kernel(VerifyArgs a)
 #pragma unroll
             for (int j = 0; j < ROWS; ++j) vv[j] = load_as_f32(sv + tt * D + r0 + RPP * j);
             const float bt = sb[tt];
-            float sqs = 0.f, sks = 0.f;
+            // channel pairs (c, c + 1) go through the packed fp32x2 instructions
+            float2 sq2 = make_float2(0.f, 0.f), sk2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                sqs = fmaf(qv[c], qv[c], sqs);
-                sks = fmaf(kv[c], kv[c], sks);
+            for (int c = 0; c < 8; c += 2) {
+                const float2 q2 = make_float2(qv[c], qv[c + 1]), k2 = make_float2(kv[c], kv[c + 1]);
+                sq2 = fma2(q2, q2, sq2);
+                sk2 = fma2(k2, k2, sk2);
             }
-            sqs = group_sum<LPR>(sqs);
-            sks = group_sum<LPR>(sks);
+            const float sqs = group_sum<LPR>(sq2.x + sq2.y);
+            const float sks = group_sum<LPR>(sk2.x + sk2.y);
             const float nq = a.l2norm ? rsqrtf(sqs + 1e-6f) : 1.f, nk = a.l2norm ? rsqrtf(sks + 1e-6f) : 1.f;
-            float qk = 0.f, e[8], ke[8], qe[8];
+            float2 qk2 = make_float2(0.f, 0.f), e[4], ke[4], qe[4], kn[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                qv[c] *= nq;
-                kv[c] *= nk;
-                qk = fmaf(qv[c], kv[c], qk);
-                e[c] = expf(gv[c]);
-                ke[c] = kv[c] * e[c];
-                qe[c] = qv[c] * e[c];
+            for (int c = 0; c < 4; ++c) {
+                const float2 q2 = mul2(make_float2(qv[2 * c], qv[2 * c + 1]), make_float2(nq, nq));
+                kn[c] = mul2(make_float2(kv[2 * c], kv[2 * c + 1]), make_float2(nk, nk));
+                qk2 = fma2(q2, kn[c], qk2);
+                e[c] = make_float2(ex2_approx(gv[2 * c] * 1.4426950408889634f),  // e^g
+                                   ex2_approx(gv[2 * c + 1] * 1.4426950408889634f));
+                ke[c] = mul2(kn[c], e[c]);
+                qe[c] = mul2(q2, e[c]);
             }
-            qk = group_sum<LPR>(qk);
+            const float qk = group_sum<LPR>(qk2.x + qk2.y);
             const int64_t slot = static_cast<int64_t>(inter[tok]);
             const bool keep = slot >= 0 && slot < a.pool.n_rows;
             if constexpr (2 * ROWS == LPR) {
@@ -174,14 +189,15 @@ verify_kernel(VerifyArgs a)
                 float vals[2 * ROWS];
 #pragma unroll
                 for (int j = 0; j < ROWS; ++j) {
-                    float ak = 0.f, bq = 0.f;
+                    float2 ak = make_float2(0.f, 0.f), bq = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        ak = fmaf(ke[c], s[j][c], ak);
-                        bq = fmaf(qe[c], s[j][c], bq);
+                    for (int c = 0; c < 4; ++c) {
+                        const float2 s2 = make_float2(s[j][2 * c], s[j][2 * c + 1]);
+                        ak = fma2(ke[c], s2, ak);
+                        bq = fma2(qe[c], s2, bq);
                     }
-                    vals[2 * j] = ak;
-                    vals[2 * j + 1] = bq;
+                    vals[2 * j] = ak.x + ak.y;
+                    vals[2 * j + 1] = bq.x + bq.y;
                 }
                 const int lane = tid & 31;
 #pragma unroll
@@ -202,8 +218,7 @@ verify_kernel(VerifyArgs a)
 #pragma unroll
                 for (int j = 0; j < ROWS; ++j) {
                     const float u = __shfl_sync(0xffffffffu, u_even, gbase + 2 * j);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) s[j][c] = fmaf(e[c], s[j][c], kv[c] * u);
+                    update_row(s[j], e, kn, u);
                     if (keep)
                         store8_stream(a.pool.data, a.pool.dtype,
                                       slot * a.pool.row_stride + blk + (r0 + RPP * j) * D + c0, s[j]);
@@ -211,17 +226,17 @@ verify_kernel(VerifyArgs a)
             } else {
 #pragma unroll
                 for (int j = 0; j < ROWS; ++j) {
-                    float ak = 0.f, bq = 0.f;
+                    float2 ak2 = make_float2(0.f, 0.f), bq2 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        ak = fmaf(ke[c], s[j][c], ak);
-                        bq = fmaf(qe[c], s[j][c], bq);
+                    for (int c = 0; c < 4; ++c) {
+                        const float2 s2 = make_float2(s[j][2 * c], s[j][2 * c + 1]);
+                        ak2 = fma2(ke[c], s2, ak2);
+                        bq2 = fma2(qe[c], s2, bq2);
                     }
-                    ak = group_sum<LPR>(ak);
-                    bq = group_sum<LPR>(bq);
+                    const float ak = group_sum<LPR>(ak2.x + ak2.y);
+                    const float bq = group_sum<LPR>(bq2.x + bq2.y);
                     const float u = bt * (vv[j] - ak);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) s[j][c] = fmaf(e[c], s[j][c], kv[c] * u);
+                    update_row(s[j], e, kn, u);
                     if (tid % LPR == 0) og[base + r0 + RPP * j] = from_f32<IO>(a.scale * fmaf(qk, u, bq));
                     if (keep)
                         store8_stream(a.pool.data, a.pool.dtype,
