@@ -1,5 +1,5 @@
 // Inter-chunk state pass on the 5th-generation tensor cores (tcgen05, TMEM),
-// for head size 128 with bf16 output: one CTA of 128 threads per (sequence,
+// for head size 128 with bf16 output: one CTA of 256 threads per (sequence,
 // head), walking the sequence's chunks in order.
 //
 // Per chunk, with S the K x V state and the chunk's record (W, Q~, K~, A_qk,
@@ -18,9 +18,12 @@
 // V_new^T written by the threads each chunk, W, Q~, A_qk (K-major) and K~
 // (MN-major) straight from the bulk-copied record.  One thread issues the MMAs;
 // an mbarrier signals their completion.  Records are double-buffered (the
-// copy of chunk i + 2 starts when chunk i is done), and the outputs of chunk
-// i - 1 are written while the first MMA group of chunk i runs.  Every wait is bounded; an expired wait sets the
-// workspace status word and the CTA stops waiting (and still frees its TMEM).
+// copy of chunk i + 2 starts when chunk i is done).  The outputs of chunk
+// i - 1 move from tensor memory to a staging tile while the first MMA group of
+// chunk i runs and from there to global memory while the second group runs, so
+// neither half waits on a barrier of its own.  Every wait is bounded; an
+// expired wait sets the workspace status word and the CTA stops waiting (and
+// still frees its TMEM).
 #include "prefill_common.cuh"
 #include "tcgen05.cuh"
 
@@ -140,24 +143,25 @@ state_pass_tc_kernel(PassParams p)
     };
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 
-    // Outputs of chunk c (O^T in Y buffer c & 1): staging [t][v], then whole output rows.
-    auto write_outputs = [&](int32_t c) {
-        const int64_t t0 = tok_begin + static_cast<int64_t>(c) * C;
-        const int len = static_cast<int>(tok_end - t0 < C ? tok_end - t0 : C);
-        __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(smem + kOS);
+    // Outputs of chunk c (O^T in Y buffer c & 1): TMEM -> staging [t][v] (stage_outputs), then,
+    // after a CTA barrier, whole output rows from the staging to global memory (store_outputs).
+    __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(smem + kOS);
+    auto stage_outputs = [&](int32_t c) {
         uint32_t y[32];
         tc::ld32(tl + kColY + 64 * (c & 1) + 32 * half, y);
         tc::wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) os[(32 * half + e) * kTcD + v] = __float2bfloat16_rn(__uint_as_float(y[e]));
-        __syncthreads();
+    };
+    auto store_outputs = [&](int32_t c) {
+        const int64_t t0 = tok_begin + static_cast<int64_t>(c) * C;
+        const int len = static_cast<int>(tok_end - t0 < C ? tok_end - t0 : C);
         const uint4 *src = reinterpret_cast<const uint4 *>(os);
 #pragma unroll
         for (int e = tid; e < C * (kTcD * 2 / 16); e += kTcThreads) {
             const int t = e >> 4, part = e & 15;
             if (t < len) reinterpret_cast<uint4 *>(out + ((t0 + t) * H + h) * kTcD)[part] = src[e];
         }
-        __syncthreads();
     };
 
     for (int32_t i = 0; i < n_chunks; ++i) {
@@ -192,12 +196,16 @@ state_pass_tc_kernel(PassParams p)
             for (int q = 0; q < 4; ++q)
                 *reinterpret_cast<uint4 *>(smem + kSA + op_off(128, v, c0 + 8 * q)) = pack8(r + 8 * q);
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
+            for (int e = 0; e < 32; e += 4) {  // channel pairs through the packed fp32x2 multiply
                 const float4 gv = gam4[(c0 + e) >> 2];
-                r[e] = __float_as_uint(__uint_as_float(r[e]) * gv.x);
-                r[e + 1] = __float_as_uint(__uint_as_float(r[e + 1]) * gv.y);
-                r[e + 2] = __float_as_uint(__uint_as_float(r[e + 2]) * gv.z);
-                r[e + 3] = __float_as_uint(__uint_as_float(r[e + 3]) * gv.w);
+                const float2 a = mul2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                      make_float2(gv.x, gv.y));
+                const float2 b2 = mul2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])),
+                                       make_float2(gv.z, gv.w));
+                r[e] = __float_as_uint(a.x);
+                r[e + 1] = __float_as_uint(a.y);
+                r[e + 2] = __float_as_uint(b2.x);
+                r[e + 3] = __float_as_uint(b2.y);
             }
             tc::st32(tl + kColS + c0, r);
         }
@@ -219,7 +227,7 @@ state_pass_tc_kernel(PassParams p)
             }
             tc::commit(&bars[2]);
         }
-        if (i > 0) write_outputs(i - 1);  // the previous chunk's outputs, while these MMAs run
+        if (i > 0) stage_outputs(i - 1);  // the previous chunk's outputs into the staging, while these MMAs run
         wait_bar(&bars[2], mma_phase);
         mma_phase ^= 1u;
         tc::fence_after_sync();
@@ -259,6 +267,7 @@ state_pass_tc_kernel(PassParams p)
             }
             tc::commit(&bars[2]);
         }
+        if (i > 0) store_outputs(i - 1);  // staged before the barrier above; stored while these MMAs run
         wait_bar(&bars[2], mma_phase);
         mma_phase ^= 1u;
         tc::fence_after_sync();
@@ -266,7 +275,11 @@ state_pass_tc_kernel(PassParams p)
         // the MMAs have completed): refill it with chunk i + 2.
         if (tid == 0 && i + 2 < n_chunks) issue(i + 2, st);
     }
-    if (n_chunks > 0) write_outputs(n_chunks - 1);
+    if (n_chunks > 0) {
+        stage_outputs(n_chunks - 1);
+        __syncthreads();
+        store_outputs(n_chunks - 1);
+    }
 
     // final state -> packed fp32, the cache row out_idx[b], and the last checkpoint if it ends there
     {
