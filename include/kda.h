@@ -441,9 +441,24 @@ const char *kda_status_string(int32_t status);
 const char *kda_last_cuda_error_string(void);
 
 /* Reads the device-side status word a prefill call leaves in its workspace:
- * 0 when every internal wait completed, otherwise a non-zero code.  This is
- * the one call that synchronises: it copies 4 bytes on `stream` and waits. */
+ * 0 when every internal wait completed, otherwise a non-zero code (1: a
+ * record copy awaited by the register state pass did not complete within its
+ * bound; 2: a record copy or MMA awaited by the tensor-memory state pass did
+ * not).  A kernel whose wait expires stops waiting, finishes without touching
+ * memory it has not been given and releases its tensor memory, so the context
+ * stays usable.  This is the one call that synchronises: it copies 4 bytes on
+ * `stream` and waits. */
 int kda_prefill_workspace_status(const void *workspace, int32_t *status_out, void *stream);
+
+/* Diagnostic of the bounded waits above (infra-level failure detection: a
+ * hang is reported, never left on the GPU).  Launches one CTA on `stream`
+ * that waits, with the same bounded mbarrier wait as the prefill kernels
+ * (at most `polls` polls, > 0), on a barrier that receives its arrival
+ * (arrive != 0) or never does (arrive == 0), and writes to the device int32
+ * *status_dev: 0 when the wait completed, 1 when it expired.  Errors:
+ * KDA_ERR_NULL (status_dev NULL), KDA_ERR_RANGE (polls == 0), KDA_ERR_CUDA
+ * (launch failure).  Asynchronous; nothing is allocated. */
+int kda_selftest_bounded_wait(int32_t *status_dev, uint32_t polls, int32_t arrive, void *stream);
 
 #ifdef __cplusplus
 }

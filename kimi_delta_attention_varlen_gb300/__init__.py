@@ -27,7 +27,7 @@ __all__ = [
     "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
     "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc", "kda_decode_step",
     "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_conv1d_varlen", "kda_conv1d_update", "kda_target_verify",
-    "kda_status_string", "kda_prefill_workspace_status", "cache_descriptor",
+    "kda_status_string", "kda_prefill_workspace_status", "kda_selftest_bounded_wait", "cache_descriptor",
     "KdaError", "EXPORTED", "LIB_PATH",
 ]
 
@@ -364,6 +364,16 @@ def kda_prefill_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     _check(lib().kda_prefill_workspace_status(_ptr(workspace), ctypes.byref(out), _stream(stream)),
            "kda_prefill_workspace_status")
     return int(out.value)
+
+
+def kda_selftest_bounded_wait(status: torch.Tensor, polls: int, arrive: bool, stream=None) -> None:
+    """One CTA waits, with the kernels' bounded mbarrier wait (at most `polls` polls), on a
+    barrier that gets its arrival (`arrive`) or never does; writes 0 (completed) or 1
+    (expired) to the device int32 tensor `status`.  Asynchronous."""
+    if status.dtype != torch.int32 or status.numel() < 1:
+        raise ValueError("status must be a device int32 tensor")
+    _check(lib().kda_selftest_bounded_wait(_ptr(status), int(polls), 1 if arrive else 0, _stream(stream)),
+           "kda_selftest_bounded_wait")
 
 
 def kda_prefill_varlen_noalloc(q, k, v, g, beta, cu_seqlens, out, *, scale: float | None = None,

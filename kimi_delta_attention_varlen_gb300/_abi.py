@@ -40,6 +40,7 @@ EXPORTED = (
     "kda_status_string",
     "kda_last_cuda_error_string",
     "kda_prefill_workspace_status",
+    "kda_selftest_bounded_wait",
 )
 
 
@@ -121,6 +122,8 @@ def lib():
         L.kda_last_cuda_error_string.restype = ctypes.c_char_p
         L.kda_prefill_workspace_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
         L.kda_prefill_workspace_status.restype = ctypes.c_int
+        L.kda_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint32, ctypes.c_int32, vp]
+        L.kda_selftest_bounded_wait.restype = ctypes.c_int
         _lib = L
         return _lib
 

@@ -402,6 +402,13 @@ const char *kda_status_string(int32_t status)
 
 const char *kda_last_cuda_error_string(void) { return cudaGetErrorString(t_last_cuda); }
 
+int kda_selftest_bounded_wait(int32_t *status_dev, uint32_t polls, int32_t arrive, void *stream)
+{
+    if (status_dev == nullptr) return KDA_ERR_NULL;
+    if (polls == 0) return KDA_ERR_RANGE;
+    return cuda_status(kda::launch_bounded_wait_selftest(status_dev, polls, arrive, static_cast<cudaStream_t>(stream)));
+}
+
 int kda_prefill_workspace_status(const void *workspace, int32_t *status_out, void *stream)
 {
     if (workspace == nullptr || status_out == nullptr) return KDA_ERR_NULL;

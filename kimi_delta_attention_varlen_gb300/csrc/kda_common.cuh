@@ -155,11 +155,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
 // Wait until the barrier's phase `parity` has completed.  Bounded: gives up
-// after `limit` polls and returns false (the caller records the failure).
+// after `limit` polls or about one second (the global timer, read every 256
+// polls), whichever comes first, and returns false (the caller records the
+// failure).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit)
 {
     const uint32_t a = smem_u32(bar);
+    uint64_t t0 = 0;
     for (uint32_t i = 0; i < limit; ++i) {
         uint32_t done;
         asm volatile(
@@ -170,6 +180,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
             : "r"(a), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((i & 255u) == 255u) {
+            const uint64_t t = global_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > 1000000000ull) return false;
+        }
     }
     return false;
 }

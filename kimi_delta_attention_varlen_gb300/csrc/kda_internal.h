@@ -139,4 +139,8 @@ struct PrefillArgs {
 };
 cudaError_t launch_prefill(const PrefillArgs &a, const PrefillLayout &L, cudaStream_t st);
 
+// One CTA that waits, with the bounded mbarrier wait of the kernels, on a barrier
+// that gets its arrival (arrive != 0) or never does; *status = 0 or 1 (expired).
+cudaError_t launch_bounded_wait_selftest(int32_t *status, uint32_t polls, int32_t arrive, cudaStream_t st);
+
 }  // namespace kda

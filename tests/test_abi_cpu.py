@@ -254,3 +254,8 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         kda.kda_status_string(0)
+
+
+def test_selftest_bounded_wait_rejections(L):
+    assert L.kda_selftest_bounded_wait(None, 1000, 0, None) == NULL
+    assert L.kda_selftest_bounded_wait(ctypes.c_void_p(A), 0, 0, None) == RANGE
