@@ -29,6 +29,8 @@
 // tokens of decay.  beta is folded into the columns of T' and e^G = P L_K
 // (L_K = e^{G_mK}) into the fragments of the k P tile, so neither beta V nor
 // beta k e^G needs a tile of its own.
+#include <cudaTypedefs.h>
+
 #include <type_traits>
 
 #include "prefill_common.cuh"
@@ -39,6 +41,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr uint32_t kPrepWaitLimit = 1u << 22;  // bounded mbarrier polls (and about one second)
 
 template <int D> struct PrepSmem {
     static constexpr int TILE = C * D * 2;                 // bf16 [64][D]
@@ -56,7 +59,8 @@ template <int D> struct PrepSmem {
     static constexpr int MEND = AD + 4 * 16 * 17 * 4;
     static constexpr int SUMS = 0;                         // fp32 [8][D] warp totals, [4][D] first rows
     static constexpr int MREG0 = MEND > 12 * D * 4 ? MEND : 12 * D * 4;
-    static constexpr int MREG = (MREG0 + 127) / 128 * 128;
+    // operand tiles on 1024-byte boundaries: whole 128-byte-swizzle atoms for the tensor copies
+    static constexpr int MREG = (MREG0 + 1023) / 1024 * 1024;
     static constexpr int KP = MREG;      // k P: Gram A operand, W right-hand side -> W
     static constexpr int QP = KP + TILE; // q P: Gram A operand -> U^T staging [D][64]
     static constexpr int KR = QP + TILE; // k R: Gram B operand -> v (bf16), the U right-hand side -> U
@@ -171,7 +175,7 @@ __device__ __forceinline__ float pick4(const float v0, const float v1, const flo
 
 template <int D, typename IO>
 __global__ void __launch_bounds__(kThreads, sizeof(IO) == 2 ? 3 : 2)  // bf16: 3 CTAs per SM (≈69 KB smem each)
-chunk_prep_kernel(PrepParams p)
+chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
 {
     using SM = PrepSmem<D>;
     using R = Rec<D>;
@@ -205,6 +209,15 @@ chunk_prep_kernel(PrepParams p)
     const int I = warp >> 1;
     const int cb = lane * CPL;
     constexpr bool kStage = sizeof(IO) == 2;  // bf16 rows are staged into their swizzled tiles
+    constexpr bool kTma = kStage && D >= 64;  // ... by tensor copies (128-byte swizzle = the tile layout)
+    __shared__ __align__(8) uint64_t ld_bar;   // tensor-copy completion: phase 0 q and k, phase 1 v
+    bool gave_up = false;
+    auto wait_loads = [&](uint32_t parity) {
+        if (!gave_up && !mbar_wait(&ld_bar, parity, kPrepWaitLimit)) {
+            gave_up = true;
+            if (lane == 0) atomicExch(p.status, 3);
+        }
+    };
     Slice<IO, CPL> rq[kStage ? 1 : PRE], rk[kStage ? 1 : PRE];
     auto load_rows = [&](int j0) {
 #pragma unroll
@@ -220,7 +233,19 @@ chunk_prep_kernel(PrepParams p)
             }
         }
     };
-    if constexpr (kStage) {  // q -> QP, k -> KP tiles, 16-byte chunks, zeros past the end
+    if constexpr (kTma) {  // q -> QP, k -> KP: one tensor copy per 64-channel slab (rows past the
+                           // sequence hold the next one's tokens or zeros; beta = 0 there cancels them)
+        if (tid == 0) {
+            mbar_init(&ld_bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&ld_bar, 2 * SM::TILE);
+#pragma unroll
+            for (int sl = 0; sl < D / 64; ++sl) {
+                tma_load_3d(smem + SM::QP + sl * C * 128, &maps.q, 64 * sl, h, static_cast<int>(t0), &ld_bar);
+                tma_load_3d(smem + SM::KP + sl * C * 128, &maps.k, 64 * sl, h, static_cast<int>(t0), &ld_bar);
+            }
+        }
+    } else if constexpr (kStage) {  // q -> QP, k -> KP tiles, 16-byte chunks, zeros past the end
         constexpr int CH = D / 8;    // 16-byte chunks per row
 #pragma unroll
         for (int e = tid; e < C * CH; e += kThreads) {
@@ -269,6 +294,7 @@ chunk_prep_kernel(PrepParams p)
     if (warp & 1) st_f32<CPL>(sSum + (kWarps + I) * D + cb, gr[0]);  // row 16 I + 8: the block midpoint
     cp_async_wait_all();
     __syncthreads();
+    if constexpr (kTma) wait_loads(0);  // q and k are in their tiles
     float gm[4][CPL], glast[CPL], off[CPL];
     {
         float run[CPL];
@@ -568,7 +594,15 @@ chunk_prep_kernel(PrepParams p)
 
     // v -> the k R tile (free after the Gram products), bf16, zeros past the end; its
     // latency overlaps the diagonal inverses (the rows were prefetched into L2)
-    if constexpr (kStage) {
+    if constexpr (kTma) {
+        if (tid == 0) {
+            fence_proxy_async_smem();  // the Gram's reads of k R precede the tensor copies into it
+            mbar_arrive_expect_tx(&ld_bar, SM::TILE);
+#pragma unroll
+            for (int sl = 0; sl < D / 64; ++sl)
+                tma_load_3d(smem + SM::KR + sl * C * 128, &maps.v, 64 * sl, h, static_cast<int>(t0), &ld_bar);
+        }
+    } else if constexpr (kStage) {
         constexpr int CH = D / 8;
 #pragma unroll
         for (int e = tid; e < C * CH; e += kThreads) {
@@ -660,6 +694,7 @@ chunk_prep_kernel(PrepParams p)
     }
     cp_async_wait_all();  // v has landed (each thread its own copies; the barrier publishes them)
     __syncthreads();
+    if constexpr (kTma) wait_loads(1);  // ... or its tensor copies have completed
 
     // ---- 6. W = T' (K e^G) and U = T' V, block row I from blocks K <= I: warps 0-3 W,
     //         warps 4-7 U, each warp D / NW columns.  The right-hand sides are read into
@@ -740,14 +775,50 @@ chunk_prep_kernel(PrepParams p)
     }
 }
 
+// cuTensorMapEncodeTiled from the driver, resolved once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// Map of a bf16 [T][H][D] input: dims (D, H, T), boxes of 64 channels x 1 head x 64
+// tokens, 128-byte swizzle (the tiles' layout), zeros outside the tensor.
+bool encode_rows(CUtensorMap *m, const void *base, int64_t T, int32_t H, int D)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (fn == nullptr || T < 1) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(C)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, typename IO>
 cudaError_t launch_typed(const PrepParams &p, int64_t n_chunk_max, int32_t h, cudaStream_t st)
 {
+    if (p.total_tokens < 1) return cudaSuccess;  // no chunk has rows: every CTA would exit at once
     auto kern = chunk_prep_kernel<D, IO>;
     constexpr int smem = PrepSmem<D>::BYTES;
+    PrepMaps maps{};
+    if constexpr (sizeof(IO) == 2 && D >= 64) {
+        if (!encode_rows(&maps.q, p.q, p.total_tokens, h, D) || !encode_rows(&maps.k, p.k, p.total_tokens, h, D) ||
+            !encode_rows(&maps.v, p.v, p.total_tokens, h, D))
+            return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(static_cast<unsigned>(n_chunk_max), static_cast<unsigned>(h)), kThreads, smem, st>>>(p);
+    kern<<<dim3(static_cast<unsigned>(n_chunk_max), static_cast<unsigned>(h)), kThreads, smem, st>>>(p, maps);
     return cudaGetLastError();
 }
 

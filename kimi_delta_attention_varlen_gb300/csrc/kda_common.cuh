@@ -189,6 +189,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return false;
 }
 
+// 3-D tiled tensor copy global -> shared (the box and swizzle encoded in the map),
+// completion signalled on `bar` as transaction bytes.  Coordinates are elements
+// (x fastest); x times the element size must be a multiple of 16 bytes.  `map`
+// is the generic address of a __grid_constant__ kernel parameter.
+__device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *map, int x, int y, int z, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n"
+        ::"r"(smem_u32(dst_smem)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // global -> shared bulk copy (16-byte aligned addresses, size % 16 == 0),
 // completion signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,

@@ -389,7 +389,8 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     if ((e = mark(1)) != cudaSuccess) return e;
 
     if (L.n_chunk_max > 0) {
-        const prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, chunk_info, a.h, a.scale, a.l2norm, records};
+        const prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, chunk_info, a.h, a.scale, a.l2norm, records, status,
+                                     a.total_tokens};
         e = prefill::launch_chunk_prep(D, a.io_dtype, pp, L.n_chunk_max, a.h, st);
         if (e != cudaSuccess) return e;
     }

@@ -3,6 +3,8 @@
 // and small load/store helpers.
 #pragma once
 
+#include <cuda.h>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -56,6 +58,15 @@ struct PrepParams {
     float scale;
     int32_t l2norm;
     char *records;
+    int32_t *status;       // workspace status word (3: a bounded wait of the prep expired)
+    int64_t total_tokens;  // rows of q, k, v (host side: the tensor maps' extent)
+};
+
+// Tensor maps of the bf16 q, k, v inputs [T][H][D] (3-D: channel, head, token;
+// boxes of 64 channels x 1 head x 64 tokens, 128-byte swizzle), encoded on the
+// host per call and passed as a __grid_constant__ kernel parameter.
+struct PrepMaps {
+    CUtensorMap q, k, v;
 };
 
 struct PassParams {
