@@ -444,7 +444,7 @@ const char *kda_last_cuda_error_string(void);
  * 0 when every internal wait completed, otherwise a non-zero code (1: a
  * record copy awaited by the register state pass did not complete within its
  * bound; 2: a record copy or MMA awaited by the tensor-memory state pass did
- * not).  A kernel whose wait expires stops waiting, finishes without touching
+ * not; 3: an input tensor copy awaited by the chunk preparation did not).  A kernel whose wait expires stops waiting, finishes without touching
  * memory it has not been given and releases its tensor memory, so the context
  * stays usable.  This is the one call that synchronises: it copies 4 bytes on
  * `stream` and waits. */
