@@ -228,8 +228,6 @@ __device__ __forceinline__ void bulk_wait_all_read()
     asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
-
 // Make generic-proxy shared-memory writes visible to the async (bulk copy) proxy.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
@@ -249,14 +247,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src, u
                  : "memory");
 }
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-
-// Wait until at most N of this thread's committed cp.async groups are pending.
-template <int N> __device__ __forceinline__ void cp_async_wait_group()
-{
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void cp_async_wait_all()
 {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
@@ -269,15 +259,6 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void *p)
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ float4 ld_nc_f4(const void *p)
-{
-    float4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
                  : "l"(p));
     return r;
 }
