@@ -11,11 +11,12 @@
 //
 // GPU mapping: one CTA (8 warps) per (chunk, head), three CTAs per SM for
 // bf16 inputs (two for fp32, whose row pass holds more registers).  All
-// global loads of the chunk are issued up front: q/k rows by cp.async into
-// their operand tiles, v rows into L2 only (they move to shared memory after
-// the Gram products, into the k R tile), and each warp's 8 consecutive g rows
-// into registers, where the in-chunk cumulative sum runs (warp totals are
-// exchanged once through shared memory).  The gated Gram products and W, U
+// global loads of the chunk are issued up front: the q/k tiles by TMA tensor
+// copies (bf16, head size >= 64; the maps' 128-byte swizzle is the tiles' own
+// layout) or per-thread cp.async, v rows into L2 only (they move to shared
+// memory after the Gram products, into the k R tile, the same way), and each
+// warp's 8 consecutive g rows into registers, where the in-chunk cumulative
+// sum runs (warp totals are exchanged once through shared memory).  The gated Gram products and W, U
 // run on the tensor cores (bf16 operands, fp32 accumulate).  T' = (I + A_kk)^-1
 // diag(beta) is formed blockwise: the four 16x16 diagonal inverses by fp32
 // forward substitution, the six blocks below them by MMAs (T'_IJ = -T_II
