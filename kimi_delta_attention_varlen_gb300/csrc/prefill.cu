@@ -39,6 +39,8 @@
 // R_j = e^{G_mJ - G_j}; each of P and R spans at most 8 tokens of decay, so
 // the products stay in fp32/bf16 range while that decay is above -80.  All
 // inter-chunk factors (e^G, e^{G_last - G}, e^{G_last}) are <= 1 for g <= 0.
+#include <atomic>
+
 #include "prefill_common.cuh"
 
 namespace kda {
@@ -352,6 +354,20 @@ state_pass_kernel(PassParams p)
     if (ob >= 0) put_state(p.se.out_cache, p.se.out_dtype, ob);
 }
 
+// Multiprocessors of the current device (queried once per device; no synchronisation).
+int64_t sm_count()
+{
+    static std::atomic<int32_t> count[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    int32_t n = count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 template <int D, typename IO, int WARPS>
 cudaError_t launch_pass(const PassParams &pp, int64_t items, cudaStream_t st)
 {
@@ -406,7 +422,8 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     int warps = D / 16;
     while (warps > 1 && items * (D / (16 * warps)) < 120) warps /= 2;
     if constexpr (D == 128 && sizeof(IO) == 2) {  // one CTA per (sequence, head): tensor-memory state pass
-        if (warps == 8) {
+        // also when the split register pass (one CTA per SM) would need a second wave
+        if (warps == 8 || items * (D / (16 * warps)) > sm_count()) {
             if ((e = prefill::launch_state_pass_tc(sp, items, st)) != cudaSuccess) return e;
             return mark(3);
         }
