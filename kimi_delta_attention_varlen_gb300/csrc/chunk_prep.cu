@@ -9,8 +9,10 @@
 // plus the state-pass operands Q~ = scale q e^G, K~ = k e^{G_last - G} and
 // gamma = e^{G_last}.
 //
-// GPU mapping: one CTA (8 warps) per (chunk, head), three CTAs per SM for
-// bf16 inputs (two for fp32, whose row pass holds more registers).  All
+// GPU mapping: one CTA (8 warps) per (chunk, head), heads fastest in the grid
+// (the heads of a chunk run together: their input rows are whole [H][D] token
+// rows and their records are adjacent), three CTAs per SM for bf16 inputs (two
+// for fp32, whose row pass holds more registers).  All
 // global loads of the chunk are issued up front: the q/k tiles by TMA tensor
 // copies (bf16, head size >= 64; the maps' 128-byte swizzle is the tiles' own
 // layout) or per-thread cp.async, v rows into L2 only (they move to shared
@@ -188,8 +190,8 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, ri = lane & 7;
-    const int64_t chunk = blockIdx.x;
-    const int h = blockIdx.y;
+    const int64_t chunk = blockIdx.x / p.H;  // heads fastest: the heads of one chunk run together
+    const int h = static_cast<int>(blockIdx.x % p.H);
     const int2 info = p.chunk_info[chunk];
     const int len = info.y;
     if (len <= 0) return;  // past the last chunk (uniform over the CTA)
@@ -809,6 +811,7 @@ template <int D, typename IO>
 cudaError_t launch_typed(const PrepParams &p, int64_t n_chunk_max, int32_t h, cudaStream_t st)
 {
     if (p.total_tokens < 1) return cudaSuccess;  // no chunk has rows: every CTA would exit at once
+    if (n_chunk_max * h > 0x7fffffffLL) return cudaErrorInvalidConfiguration;  // one-dimensional grid
     auto kern = chunk_prep_kernel<D, IO>;
     constexpr int smem = PrepSmem<D>::BYTES;
     PrepMaps maps{};
@@ -819,7 +822,7 @@ cudaError_t launch_typed(const PrepParams &p, int64_t n_chunk_max, int32_t h, cu
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(static_cast<unsigned>(n_chunk_max), static_cast<unsigned>(h)), kThreads, smem, st>>>(p, maps);
+    kern<<<static_cast<unsigned>(n_chunk_max * h), kThreads, smem, st>>>(p, maps);
     return cudaGetLastError();
 }
 

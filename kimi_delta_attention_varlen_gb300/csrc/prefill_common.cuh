@@ -145,7 +145,7 @@ __device__ __forceinline__ void store_state2(void *base, int32_t dtype, int64_t 
 // (sequence, head)) over `items` = num_seqs x h CTAs.
 cudaError_t launch_state_pass_tc(const PassParams &p, int64_t items, cudaStream_t st);
 
-// Launches the chunk-preparation kernel over n_chunk_max x h CTAs.
+// Launches the chunk-preparation kernel over n_chunk_max x h CTAs (heads fastest).
 cudaError_t launch_chunk_prep(int d, int32_t io_dtype, const PrepParams &p, int64_t n_chunk_max, int32_t h,
                               cudaStream_t st);
 
