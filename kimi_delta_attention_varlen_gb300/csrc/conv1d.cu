@@ -144,8 +144,10 @@ template <int W, typename IO, int TT>
 __global__ void __launch_bounds__(kConvThreads, 3)
 conv_varlen_kernel(ConvArgs a)
 {
-    const int64_t c0 = (static_cast<int64_t>(blockIdx.y) * kConvThreads + threadIdx.x) * kVec;
-    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TT;
+    // channel blocks fastest: the blocks of one token tile run together (whole rows of x and y)
+    const int64_t ncb = (a.C + kConvThreads * kVec - 1) / (kConvThreads * kVec);
+    const int64_t c0 = ((static_cast<int64_t>(blockIdx.x) % ncb) * kConvThreads + threadIdx.x) * kVec;
+    const int64_t t0 = (static_cast<int64_t>(blockIdx.x) / ncb) * TT;
     if (c0 >= a.C || t0 >= a.T) return;
     const int64_t C = a.C;
     const IO *x = static_cast<const IO *>(a.x);
@@ -330,14 +332,15 @@ template <int W> cudaError_t varlen_w(const ConvArgs &a, cudaStream_t st)
 {
     const unsigned gy = static_cast<unsigned>((a.C + kConvThreads * kVec - 1) / (kConvThreads * kVec));
     if (a.T > 0) {
+        if ((a.T + 15) / 8 * static_cast<int64_t>(gy) > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         if (a.io_dtype == KDA_BF16) {
             constexpr int TT = 16;
             conv_varlen_kernel<W, __nv_bfloat16, TT>
-                <<<dim3(static_cast<unsigned>((a.T + TT - 1) / TT), gy), kConvThreads, 0, st>>>(a);
+                <<<static_cast<unsigned>((a.T + TT - 1) / TT * gy), kConvThreads, 0, st>>>(a);
         } else {
             constexpr int TT = 8;
             conv_varlen_kernel<W, float, TT>
-                <<<dim3(static_cast<unsigned>((a.T + TT - 1) / TT), gy), kConvThreads, 0, st>>>(a);
+                <<<static_cast<unsigned>((a.T + TT - 1) / TT * gy), kConvThreads, 0, st>>>(a);
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
