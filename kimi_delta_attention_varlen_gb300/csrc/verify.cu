@@ -11,11 +11,12 @@
 //   a_v = sum_k k_k e^{g_k} S[k][v],  b_v = sum_k q_k e^{g_k} S[k][v],
 //   u_v = beta (v_v - a_v),  S'[k][v] = e^{g_k} S[k][v] + k_k u_v,
 //   o_v = scale (b_v + (q.k) u_v).
-// GPU mapping: one CTA per (request, head); D/8 lanes share a state row, each
-// holding 8 channels of ROWS rows in registers for all L tokens, so the state
-// is read once and each intermediate state is one coalesced write.  The draft
-// tokens' inputs are staged in shared memory 8 tokens at a time (one memory
-// latency per group, in flight together with the state).
+// GPU mapping: persistent CTAs over the (request, head) items; D/8 lanes share
+// a state row, each holding 8 channels of ROWS rows in registers for all L
+// tokens, so the state is read once and each intermediate state is one
+// coalesced write.  Each thread copies its own slices of the next item's
+// state into shared memory while it computes the current one; the draft
+// tokens' inputs are staged in shared memory 8 tokens at a time.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -83,6 +84,13 @@ template <int D, typename IO> struct VerifyLayout {
     static constexpr int BYTES = BETA + kVT * 4;
 };
 
+// Bytes of the token staging, rounded to 16 (the state slots follow it).
+template <int D, typename IO> __host__ __device__ constexpr int verify_stage_bytes() { return (VerifyLayout<D, IO>::BYTES + 15) / 16 * 16; }
+
+// Persistent CTAs over the (request, head) items.  Every thread copies its own slices of the
+// next item's state into its own shared-memory slots (cp.async) while it computes the current
+// item, so the state read overlaps the work and needs no block barrier; the current item's
+// token inputs are staged cooperatively first, so one wait covers both.
 template <int D, typename IO, typename IdxT>
 __global__ void __launch_bounds__(verify_threads<D>())
 verify_kernel(VerifyArgs a)
@@ -95,28 +103,18 @@ verify_kernel(VerifyArgs a)
     const int c0 = 8 * (tid % LPR);               // this lane's channels
     const int r0 = tid / LPR;                     // rows r0 + RPP j
     const int64_t H = a.h;
-    const int64_t req = blockIdx.x / H;
-    const int h = static_cast<int>(blockIdx.x % H);
-    const int64_t row = static_cast<int64_t>(static_cast<const IdxT *>(a.idx)[req]);
-    const bool valid = row >= 0 && row < a.cache.n_rows;
-    const int64_t blk = (static_cast<int64_t>(h) * D) * D;  // head block within a cache / pool row
-
-    float s[ROWS][8];
-#pragma unroll
-    for (int j = 0; j < ROWS; ++j) {
-        if (valid) {
-            load8(a.cache.data, a.cache.dtype, row * a.cache.row_stride + blk + (r0 + RPP * j) * D + c0, s[j]);
-        } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) s[j][c] = 0.f;
-        }
-    }
+    const int64_t items = a.batch * H;
+    int64_t it = blockIdx.x;
+    if (it >= items) return;  // (uniform over the CTA)
     const IO *qg = static_cast<const IO *>(a.q);
     const IO *kg = static_cast<const IO *>(a.k);
     const IO *vg = static_cast<const IO *>(a.v);
     IO *og = static_cast<IO *>(a.out);
     const IdxT *inter = static_cast<const IdxT *>(a.inter_idx);
-    // token inputs, staged VT tokens at a time: q, k, v [VT][D] io, g [VT][D] fp32, beta [VT]
+    const int esz = a.cache.dtype == KDA_F32 ? 4 : 2;
+    const int v16 = esz / 2;  // 16-byte pieces per 8-channel slice
+    // token inputs, staged VT tokens at a time: q, k, v [VT][D] io, g [VT][D] fp32, beta [VT];
+    // then the state slots [2 stages][ROWS][v16][THREADS] x 16 bytes
     extern __shared__ __align__(16) char smem[];
     using VL = VerifyLayout<D, IO>;
     IO *sq = reinterpret_cast<IO *>(smem + VL::Q);
@@ -124,11 +122,30 @@ verify_kernel(VerifyArgs a)
     IO *sv = reinterpret_cast<IO *>(smem + VL::V);
     float *sg = reinterpret_cast<float *>(smem + VL::G);
     float *sb = reinterpret_cast<float *>(smem + VL::BETA);
+    uint4 *slots = reinterpret_cast<uint4 *>(smem + verify_stage_bytes<D, IO>());
     constexpr int IOCH = D * static_cast<int>(sizeof(IO)) / 16;  // 16-byte chunks of one io row
     constexpr int GCH = D * 4 / 16;                               // ... of one g row
-    for (int t0 = 0; t0 < a.L; t0 += kVT) {
-        const int nt = a.L - t0 < kVT ? a.L - t0 : kVT;
-        __syncthreads();  // the previous group's inputs are consumed
+
+    auto row_of = [&](int64_t item) -> int64_t {
+        const int64_t r = static_cast<int64_t>(static_cast<const IdxT *>(a.idx)[item / H]);
+        return r >= 0 && r < a.cache.n_rows ? r : -1;
+    };
+    // this thread's slices of item `item`'s cached state -> stage st (nothing for an invalid row)
+    auto prefetch_state = [&](int64_t item, int st) {
+        const int64_t row = row_of(item);
+        if (row >= 0) {
+            const char *src = static_cast<const char *>(a.cache.data) +
+                              (row * a.cache.row_stride + (item % H) * D * D) * esz;
+#pragma unroll
+            for (int j = 0; j < ROWS; ++j)
+                for (int w = 0; w < v16; ++w)
+                    cp_async16(smem_u32(&slots[((st * ROWS + j) * v16 + w) * THREADS + tid]),
+                               src + (static_cast<int64_t>(r0 + RPP * j) * D + c0) * esz + 16 * w, 16u);
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+    // the inputs of tokens t0 .. t0 + nt - 1 of request req, head h -> the staging
+    auto stage_tokens = [&](int64_t req, int h, int t0, int nt) {
         for (int e = tid; e < nt * (3 * IOCH + GCH); e += THREADS) {
             const int tt = e / (3 * IOCH + GCH), part = e % (3 * IOCH + GCH);
             const int64_t base = ((req * a.L + t0 + tt) * H + h) * D;
@@ -145,9 +162,50 @@ verify_kernel(VerifyArgs a)
             }
         }
         if (tid < nt) sb[tid] = a.beta[(req * a.L + t0 + tid) * H + h];
-        cp_async_wait_all();
-        __syncthreads();
-        for (int tt = 0; tt < nt; ++tt) {
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+
+    prefetch_state(it, 0);
+    for (int st = 0; it < items; it += gridDim.x, st ^= 1) {
+        const int64_t req = it / H;
+        const int h = static_cast<int>(it % H);
+        const int64_t blk = (static_cast<int64_t>(h) * D) * D;  // head block within a cache / pool row
+        const bool valid = row_of(it) >= 0;
+        __syncthreads();  // the previous item's staged inputs are consumed
+        stage_tokens(req, h, 0, a.L < kVT ? a.L : kVT);
+        if (it + gridDim.x < items) prefetch_state(it + gridDim.x, st ^ 1);
+        else asm volatile("cp.async.commit_group;\n" ::: "memory");
+        asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // this item's state and first inputs
+        __syncthreads();  // ... including the inputs other threads staged
+        float s[ROWS][8];
+#pragma unroll
+        for (int j = 0; j < ROWS; ++j) {
+            if (valid) {
+                const uint4 x = slots[((st * ROWS + j) * v16) * THREADS + tid];
+                if (v16 == 1) {
+                    s[j][0] = bf16_lo(x.x); s[j][1] = bf16_hi(x.x); s[j][2] = bf16_lo(x.y); s[j][3] = bf16_hi(x.y);
+                    s[j][4] = bf16_lo(x.z); s[j][5] = bf16_hi(x.z); s[j][6] = bf16_lo(x.w); s[j][7] = bf16_hi(x.w);
+                } else {
+                    const uint4 y = slots[((st * ROWS + j) * v16 + 1) * THREADS + tid];
+                    s[j][0] = __uint_as_float(x.x); s[j][1] = __uint_as_float(x.y);
+                    s[j][2] = __uint_as_float(x.z); s[j][3] = __uint_as_float(x.w);
+                    s[j][4] = __uint_as_float(y.x); s[j][5] = __uint_as_float(y.y);
+                    s[j][6] = __uint_as_float(y.z); s[j][7] = __uint_as_float(y.w);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) s[j][c] = 0.f;
+            }
+        }
+        for (int t0 = 0; t0 < a.L; t0 += kVT) {
+            const int nt = a.L - t0 < kVT ? a.L - t0 : kVT;
+            if (t0 > 0) {  // later groups of more than kVT draft tokens
+                __syncthreads();
+                stage_tokens(req, h, t0, nt);
+                cp_async_wait_all();
+                __syncthreads();
+            }
+            for (int tt = 0; tt < nt; ++tt) {
             const int64_t tok = req * a.L + t0 + tt;
             const int64_t base = (tok * H + h) * D;
             float qv[8], kv[8], gv[8], vv[ROWS];
@@ -243,14 +301,27 @@ verify_kernel(VerifyArgs a)
                                       slot * a.pool.row_stride + blk + (r0 + RPP * j) * D + c0, s[j]);
                 }
             }
+            }
         }
     }
 }
 
 template <int D, typename IO, typename IdxT> cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t st)
 {
-    verify_kernel<D, IO, IdxT>
-        <<<static_cast<unsigned>(a.batch * a.h), verify_threads<D>(), VerifyLayout<D, IO>::BYTES, st>>>(a);
+    constexpr int THREADS = verify_threads<D>();
+    constexpr int ROWS = D / (THREADS / (D / 8));
+    const int v16 = a.cache.dtype == KDA_F32 ? 2 : 1;
+    const int smem = verify_stage_bytes<D, IO>() + 2 * ROWS * v16 * THREADS * 16;
+    auto kern = verify_kernel<D, IO, IdxT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem)) != cudaSuccess) return e;
+    const int64_t items = a.batch * a.h;
+    const int64_t resident = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    kern<<<static_cast<unsigned>(items < resident ? items : resident), THREADS, smem, st>>>(a);
     return cudaGetLastError();
 }
 
