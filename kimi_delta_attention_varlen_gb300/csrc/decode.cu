@@ -14,10 +14,12 @@
 //   S'[k][v] = e^{g_k} S[k][v] + k_k u_v,   o_v = scale (b_v + (q.k) u_v)
 // so one pass over the state suffices: read row, two dot products, write row.
 //
-// GPU mapping: one CTA (up to 256 threads) per (request, head).  D/8 lanes
-// share a state row, each holding 8 channels (one 16-byte bf16 vector); every
-// thread issues the loads of all its rows before using any, so a CTA keeps
-// its whole 32 KiB (bf16, D = 128) state block in flight.  The kernel is bound
+// GPU mapping: persistent CTAs (up to 256 threads) over the (request, head)
+// items.  D/8 lanes share a state row, each holding 8 channels (one 16-byte
+// bf16 vector).  Every thread copies its own slices of the next item's state
+// into its own shared-memory slots (cp.async, two stages) and holds the next
+// item's token inputs in registers, so the state read of one item overlaps
+// the work on the previous one without a block barrier.  The kernel is bound
 // by HBM: 2 * D * D * sizeof(cache) bytes per (request, head).
 #include "kda_common.cuh"
 #include "kda_internal.h"
