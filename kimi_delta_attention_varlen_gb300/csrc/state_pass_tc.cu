@@ -1,5 +1,5 @@
 // Inter-chunk state pass on the 5th-generation tensor cores (tcgen05, TMEM),
-// for head size 128 with bf16 output: one CTA of 256 threads per (sequence,
+// for head size 128 with bf16 output: one CTA of 512 threads per (sequence,
 // head), walking the sequence's chunks in order.
 //
 // Per chunk, with S the K x V state and the chunk's record (W, Q~, K~, A_qk,
@@ -13,7 +13,7 @@
 //
 // Layout: S^T (fp32, 128 lanes x 128 columns), X^T (64 columns) and two
 // Y^T/O^T buffers (64 columns each) live in tensor memory.  Value row v is TMEM
-// lane v; two warps share each 32-lane quadrant and split its columns.  The MMA
+// lane v; four warps share each 32-lane quadrant and split its columns.  The MMA
 // operands are bf16 in shared memory in the 128-byte-swizzle layout: S^T and
 // V_new^T written by the threads each chunk, W, Q~, A_qk (K-major) and K~
 // (MN-major) straight from the bulk-copied record.  One thread issues the MMAs;
@@ -31,7 +31,10 @@ namespace kda {
 namespace prefill {
 namespace {
 
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 512;
+constexpr int kTcParts = kTcThreads / 128;   // warps sharing one 32-lane TMEM quadrant
+constexpr int kTcSCols = 128 / kTcParts;     // S^T columns per thread
+constexpr int kTcYCols = 64 / kTcParts;      // X^T / Y^T columns per thread
 constexpr uint32_t kTcWaitLimit = 1u << 22;
 constexpr int kTcD = 128;
 using RT = Rec<kTcD>;
@@ -45,6 +48,13 @@ constexpr uint32_t kColS = 0, kColX = 128, kColY = 192, kTmemCols = 512;  // Y b
 __device__ __forceinline__ uint32_t op_off(int rows, int row, int col)
 {
     return static_cast<uint32_t>((col >> 6) * rows * 128) + swz_off<128>(row, col & 63);
+}
+
+// N (32 or 16) consecutive TMEM columns of this thread's lane
+template <int N> __device__ __forceinline__ void ld_cols(uint32_t t, uint32_t (&r)[N])
+{
+    if constexpr (N == 32) tc::ld32(t, r);
+    else tc::ld16(t, r);
 }
 
 __device__ __forceinline__ uint4 pack8(const uint32_t *r)
@@ -64,7 +74,7 @@ state_pass_tc_kernel(PassParams p)
     __shared__ uint32_t tmem_base;
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int quad = warp & 3, half = warp >> 2;   // TMEM lane quadrant; which half of the columns
+    const int quad = warp & 3, part = warp >> 2;   // TMEM lane quadrant; which part of the columns
     const int v = 32 * quad + (tid & 31);          // value row = TMEM lane
     const int64_t H = p.H;
     const int64_t item = blockIdx.x;
@@ -99,12 +109,12 @@ state_pass_tc_kernel(PassParams p)
                                      __uint_as_float(r[e + 3])));
     };
 
-    // initial state: columns [64 half, 64 half + 64) of S^T row v (= cache row [v][k])
+    // initial state: this thread's columns of S^T row v (= cache row [v][k])
     {
         const int64_t base = init_base(p.se, b, H * kTcD * kTcD);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int c0 = 64 * half + 32 * j;
+        for (int j = 0; j < kTcSCols / 32; ++j) {
+            const int c0 = kTcSCols * part + 32 * j;
             uint32_t r[32];
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
@@ -147,11 +157,12 @@ state_pass_tc_kernel(PassParams p)
     // after a CTA barrier, whole output rows from the staging to global memory (store_outputs).
     __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(smem + kOS);
     auto stage_outputs = [&](int32_t c) {
-        uint32_t y[32];
-        tc::ld32(tl + kColY + 64 * (c & 1) + 32 * half, y);
+        uint32_t y[kTcYCols];
+        ld_cols(tl + kColY + 64 * (c & 1) + kTcYCols * part, y);
         tc::wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) os[(32 * half + e) * kTcD + v] = __float2bfloat16_rn(__uint_as_float(y[e]));
+        for (int e = 0; e < kTcYCols; ++e)
+            os[(kTcYCols * part + e) * kTcD + v] = __float2bfloat16_rn(__uint_as_float(y[e]));
     };
     auto store_outputs = [&](int32_t c) {
         const int64_t t0 = tok_begin + static_cast<int64_t>(c) * C;
@@ -176,8 +187,8 @@ state_pass_tc_kernel(PassParams p)
             const int64_t ck = ckpt_slot(p.se, b, i - 1, tok_end - tok_begin);
             if (ck >= 0) {
 #pragma unroll 1
-                for (int j = 0; j < 2; ++j) {
-                    const int c0 = 64 * half + 32 * j;
+                for (int j = 0; j < kTcSCols / 32; ++j) {
+                    const int c0 = kTcSCols * part + 32 * j;
                     uint32_t r[32];
                     tc::ld32(tl + kColS + c0, r);
                     tc::wait_ld();
@@ -187,8 +198,8 @@ state_pass_tc_kernel(PassParams p)
         }
         // (A) S^T row v, this warp's 64 columns -> bf16 operand (undecayed); decay the TMEM copy by gamma
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int c0 = 64 * half + 32 * j;
+        for (int j = 0; j < kTcSCols / 32; ++j) {
+            const int c0 = kTcSCols * part + 32 * j;
             uint32_t r[32];
             tc::ld32(tl + kColS + c0, r);
             tc::wait_ld();
@@ -234,13 +245,13 @@ state_pass_tc_kernel(PassParams p)
 
         // (C) V_new^T row v, this warp's 32 columns = U^T - X^T -> bf16 operand (slab 0 of S^T's)
         {
-            uint32_t x[32];
-            tc::ld32(tl + kColX + 32 * half, x);
+            uint32_t x[kTcYCols];
+            ld_cols(tl + kColX + kTcYCols * part, x);
             tc::wait_ld();
             const char *ut = sb + RT::UT;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t off = swz_off<128>(v, 32 * half + 8 * q);
+            for (int q = 0; q < kTcYCols / 8; ++q) {
+                const uint32_t off = swz_off<128>(v, kTcYCols * part + 8 * q);
                 const uint4 u = *reinterpret_cast<const uint4 *>(ut + off);
                 const uint32_t *xx = x + 8 * q;
                 uint4 w;
@@ -288,8 +299,8 @@ state_pass_tc_kernel(PassParams p)
         const int64_t ck = n_chunks > 0 ? ckpt_slot(p.se, b, n_chunks - 1, tok_end - tok_begin) : -1;
         if (p.se.final_state != nullptr || ob >= 0 || ck >= 0) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int c0 = 64 * half + 32 * j;
+            for (int j = 0; j < kTcSCols / 32; ++j) {
+                const int c0 = kTcSCols * part + 32 * j;
                 uint32_t r[32];
                 tc::ld32(tl + kColS + c0, r);
                 tc::wait_ld();
