@@ -197,3 +197,20 @@ def test_full_long_sequence_sampled():
     w = wl.long_seq()
     _full_workload(w, [(0, 5)])
     torch.cuda.empty_cache()
+
+
+# 16 (sequence, head) pairs fit one wave of the split register pass; 96 would need a
+# second wave, so the tensor-memory pass runs instead.
+@pytest.mark.parametrize("lengths,H", [([327, 100, 1, 0], 4), ([200, 65, 131], 32)])
+def test_prefill_state_pass_dispatch(lengths, H):
+    """Both sides of the state-pass choice at head size 128, bf16, against the oracle."""
+    D = 128
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    inp = wl.token_inputs(cu[-1], H, D, D, torch.bfloat16, seed=len(lengths) + H, device=DEV, decay_scale=0.1)
+    init = torch.randn(len(lengths), H, D, D, generator=wl.generator(9, DEV), device=DEV) * 0.5
+    scale = D ** -0.5
+    out, fin = run_prefill(inp, cu, H, D, init=init, scale=scale)
+    heads = None if H <= 4 else [0, 13, 31]
+    check_against_oracle(inp, cu, H, D, init, out, fin, scale, heads=heads)
