@@ -30,7 +30,10 @@
 //                           enough pairs to fill the GPU), or
 //      state_pass_kernel    one CTA per (sequence, head, value slice), S in
 //                           registers (fp32 accumulators), double-buffering
-//                           the records into shared memory with bulk copies.
+//                           the records into shared memory with bulk copies;
+//                           for few pairs at head size 128 its warp-pair form
+//                           (state_pass_pair_kernel) splits each value group's
+//                           key channels over two warps.
 // All products run on the tensor cores (bf16 operands, fp32 accumulation).
 //
 // Exponent ranges.  Factors e^{G_i - G_j} are split through a reference row:
@@ -354,6 +357,254 @@ state_pass_kernel(PassParams p)
     if (ob >= 0) put_state(p.se.out_cache, p.se.out_dtype, ob);
 }
 
+// Warp-pair variant of the state pass for few (sequence, head) pairs: each 16-row value group
+// of S^T is held by two warps, one per half of the key channels.  Per chunk the two halves
+// are swapped as bf16 fragments through shared memory; warp A (role 0) forms X^T = S^T W^T and
+// V_new^T = U^T - X^T, warp B (role 1) forms Y^T = S^T Q~^T and O^T = Y^T + V_new^T A_qk^T, and
+// each updates its own half, S^T <- S^T Diag(gamma) + V_new^T K~.  A chunk then costs a warp
+// 96 (A) or 116 (B) tensor-core instructions instead of 212, which is what bounds the chunk
+// when every warp has a scheduler to itself.
+template <int D, typename IO, int PAIRS>
+__global__ void __launch_bounds__(PAIRS * 64)
+state_pass_pair_kernel(PassParams p)
+{
+    using R = Rec<D>;
+    constexpr int VT = 16 * PAIRS;          // value columns per CTA
+    constexpr int NSPLIT = D / VT;
+    constexpr int HEAD = R::UT;             // W, Q~, K~, A_qk, gamma
+    constexpr int UT_BYTES = VT * C * 2;    // this CTA's rows of U^T
+    constexpr int STAGE = HEAD + UT_BYTES;
+    constexpr int KH = D / 2;               // key channels per warp
+    constexpr int KSH = KH / 16;            // k-steps per half
+    constexpr int XS = KSH * 512;           // half of S^T as bf16 A fragments [KSH][32 lanes][16 B]
+    constexpr int XV = 4 * 512;             // V_new^T as bf16 A fragments [4][32 lanes][16 B]
+    constexpr int XG = 2 * XS + XV;         // exchange bytes per group
+    static_assert(NSPLIT * VT == D && KSH >= 1, "value split");
+    extern __shared__ __align__(1024) char smem[];
+    __shared__ __align__(8) uint64_t bars[2];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, ri = lane & 7;
+    const int grp = warp >> 1, role = warp & 1;  // role = the key half this warp owns
+    const int64_t H = p.H;
+    const int64_t item = blockIdx.x;
+    const int vs = static_cast<int>(item % NSPLIT);
+    const int h = static_cast<int>((item / NSPLIT) % H);
+    const int64_t b = p.seq_order[item / (NSPLIT * H)];
+    const int32_t c_begin = p.chunk_off[b], n_chunks = p.chunk_off[b + 1] - c_begin;
+    const int64_t tok_begin = p.cu[b], tok_end = p.cu[b + 1];
+    const int vl0 = 16 * grp;               // first value column of this group within the CTA
+    const int vg0 = vs * VT + vl0;          // ... within the head
+    const int kb = role * KH;               // first key channel of this warp's half
+    char *xg = smem + 2 * STAGE + grp * XG;  // this group's exchange area
+    IO *sO = reinterpret_cast<IO *>(smem + 2 * STAGE + PAIRS * XG) + grp * (C * 16);
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;\n" ::"r"(1 + grp) : "memory"); };
+
+    // S^T accumulator fragments of this warp's half:
+    // s[n][e] = S^T(v = vg0 + gid + 8 (e >> 1), k = kb + 8 n + 2 tig + (e & 1))
+    float s[KH / 8][4];
+    const int64_t per_seq = H * D * D;
+    auto elem = [&](int n, int hr) {
+        return (static_cast<int64_t>(h) * D + vg0 + gid + 8 * hr) * D + kb + 8 * n + 2 * tig;
+    };
+    auto put_state = [&](void *dst, int32_t dtype, int64_t base) {
+#pragma unroll
+        for (int n = 0; n < KH / 8; ++n)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr)
+                store_state2(dst, dtype, base + elem(n, hr), make_float2(s[n][2 * hr], s[n][2 * hr + 1]));
+    };
+    {
+        const int64_t base = init_base(p.se, b, per_seq);
+#pragma unroll
+        for (int n = 0; n < KH / 8; ++n) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                float2 x = make_float2(0.f, 0.f);
+                if (base >= 0) x = load_state2(p.se.init, p.se.init_dtype, base + elem(n, hr));
+                s[n][2 * hr] = x.x;
+                s[n][2 * hr + 1] = x.y;
+            }
+        }
+    }
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int32_t i, int st) {
+        const char *rec = p.records + (static_cast<int64_t>(c_begin + i) * H + h) * R::BYTES;
+        char *dst = smem + st * STAGE;
+        mbar_arrive_expect_tx(&bars[st], STAGE);
+        bulk_g2s(dst, rec, HEAD, &bars[st]);
+        bulk_g2s(dst + HEAD, rec + R::UT + vs * UT_BYTES, UT_BYTES, &bars[st]);
+    };
+    if (tid == 0) {
+        if (n_chunks > 0) issue(0, 0);
+        if (n_chunks > 1) issue(1, 1);
+    }
+
+    IO *out = static_cast<IO *>(p.out);
+    bool gave_up = false;  // after one expired wait, stop waiting (the status word reports it)
+    for (int32_t i = 0; i < n_chunks; ++i) {
+        const int st = i & 1;
+        if (!gave_up && !mbar_wait(&bars[st], (i >> 1) & 1, kWaitLimit)) {
+            gave_up = true;
+            if (lane == 0) atomicExch(p.status, 1);
+        }
+        const char *sb = smem + st * STAGE;
+        const int64_t t0 = tok_begin + static_cast<int64_t>(i) * C;
+        const int len = static_cast<int>(tok_end - t0 < C ? tok_end - t0 : C);
+
+        // (1) S^T as bf16 A fragments (M = 16 value rows, K = key channels): this warp's half
+        //     packed and published, the partner's half read back
+        uint32_t slo[KSH][4], shi[KSH][4];  // key steps of the first and second half
+        {
+            uint32_t own[KSH][4];
+#pragma unroll
+            for (int ks = 0; ks < KSH; ++ks) {
+                own[ks][0] = pack_bf16x2(s[2 * ks][0], s[2 * ks][1]);
+                own[ks][1] = pack_bf16x2(s[2 * ks][2], s[2 * ks][3]);
+                own[ks][2] = pack_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+                own[ks][3] = pack_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+                *reinterpret_cast<uint4 *>(xg + role * XS + (ks * 32 + lane) * 16) =
+                    make_uint4(own[ks][0], own[ks][1], own[ks][2], own[ks][3]);
+            }
+            pair_sync();
+#pragma unroll
+            for (int ks = 0; ks < KSH; ++ks) {
+                const uint4 o = *reinterpret_cast<const uint4 *>(xg + (role ^ 1) * XS + (ks * 32 + lane) * 16);
+                if (role == 0) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) slo[ks][e] = own[ks][e];
+                    shi[ks][0] = o.x; shi[ks][1] = o.y; shi[ks][2] = o.z; shi[ks][3] = o.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) shi[ks][e] = own[ks][e];
+                    slo[ks][0] = o.x; slo[ks][1] = o.y; slo[ks][2] = o.z; slo[ks][3] = o.w;
+                }
+            }
+        }
+        // (2) role 0: X^T = S^T W^T; role 1: Y^T = S^T Q~^T   (N = 64 chunk rows)
+        float x[8][4] = {};
+        {
+            const char *opnd = sb + (role ? R::QT : R::W);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t bw[4];
+                    ldmatrix_x4(bw, smem_u32(opnd + tile_off<D, C>(16 * np + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
+                    const uint32_t *a = ks < KSH ? slo[ks % KSH] : shi[ks % KSH];
+                    mma_bf16(x[2 * np], a, bw[0], bw[1]);
+                    mma_bf16(x[2 * np + 1], a, bw[2], bw[3]);
+                }
+            }
+        }
+        // (3) role 0: V_new^T = U^T - X^T as bf16 A fragments (K = chunk rows), published;
+        //     role 1 reads them
+        uint32_t va[4][4];
+        if (role == 0) {
+            const char *ut = sb + HEAD;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                const uint32_t u0 = *reinterpret_cast<const uint32_t *>(ut + swz_off<128>(vl0 + gid, 8 * n + 2 * tig));
+                const uint32_t u1 =
+                    *reinterpret_cast<const uint32_t *>(ut + swz_off<128>(vl0 + gid + 8, 8 * n + 2 * tig));
+                x[n][0] = bf16_lo(u0) - x[n][0];
+                x[n][1] = bf16_hi(u0) - x[n][1];
+                x[n][2] = bf16_lo(u1) - x[n][2];
+                x[n][3] = bf16_hi(u1) - x[n][3];
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                va[ks][0] = pack_bf16x2(x[2 * ks][0], x[2 * ks][1]);
+                va[ks][1] = pack_bf16x2(x[2 * ks][2], x[2 * ks][3]);
+                va[ks][2] = pack_bf16x2(x[2 * ks + 1][0], x[2 * ks + 1][1]);
+                va[ks][3] = pack_bf16x2(x[2 * ks + 1][2], x[2 * ks + 1][3]);
+                *reinterpret_cast<uint4 *>(xg + 2 * XS + (ks * 32 + lane) * 16) =
+                    make_uint4(va[ks][0], va[ks][1], va[ks][2], va[ks][3]);
+            }
+        }
+        pair_sync();
+        if (role == 1) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint4 o = *reinterpret_cast<const uint4 *>(xg + 2 * XS + (ks * 32 + lane) * 16);
+                va[ks][0] = o.x; va[ks][1] = o.y; va[ks][2] = o.z; va[ks][3] = o.w;
+            }
+            // (4) O^T = Y^T + V_new^T A_qk^T   (A_qk causal: chunk row t needs s <= t)
+#pragma unroll
+            for (int tp = 0; tp < 4; ++tp) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    if (ks <= tp) {
+                        uint32_t ba[4];
+                        ldmatrix_x4(ba, smem_u32(sb + R::AQK +
+                                                 swz_off<128>(16 * tp + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
+                        mma_bf16(x[2 * tp], va[ks], ba[0], ba[1]);
+                        mma_bf16(x[2 * tp + 1], va[ks], ba[2], ba[3]);
+                    }
+                }
+            }
+            // output rows through the group's staging tile [64][16]
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 8 * n + 2 * tig + (e & 1);
+                    const int vl = gid + 8 * (e >> 1);
+                    sO[t * 16 + vl] = from_f32<IO>(x[n][e]);
+                }
+            }
+            __syncwarp();
+            constexpr int PARTS = 16 * static_cast<int>(sizeof(IO)) / 16;  // uint4 per staged row
+            const uint4 *src = reinterpret_cast<const uint4 *>(sO);
+            for (int e = lane; e < C * PARTS; e += 32) {
+                const int t = e / PARTS, part = e % PARTS;
+                if (t < len) {
+                    IO *dst = out + ((t0 + t) * H + h) * D + vg0;
+                    reinterpret_cast<uint4 *>(dst)[part] = src[e];
+                }
+            }
+            __syncwarp();
+        }
+        // (5) this warp's half: S^T <- S^T Diag(gamma) + V_new^T K~
+        {
+            const float *gam = reinterpret_cast<const float *>(sb + R::GAMMA) + kb;
+#pragma unroll
+            for (int n = 0; n < KH / 8; ++n) {
+                const float2 gm = *reinterpret_cast<const float2 *>(gam + 8 * n + 2 * tig);
+                s[n][0] *= gm.x;
+                s[n][1] *= gm.y;
+                s[n][2] *= gm.x;
+                s[n][3] *= gm.y;
+            }
+#pragma unroll
+            for (int np = 0; np < KH / 16; ++np) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    uint32_t bk[4];
+                    ldmatrix_x4_trans(bk, smem_u32(sb + R::KT + tile_off<D, C>(16 * ks + ri + 8 * (mi & 1),
+                                                                                 kb + 16 * np + 8 * (mi >> 1))));
+                    mma_bf16(s[2 * np], va[ks], bk[0], bk[1]);
+                    mma_bf16(s[2 * np + 1], va[ks], bk[2], bk[3]);
+                }
+            }
+        }
+        __syncthreads();  // every warp is done with this stage (and with the exchange area)
+        if (tid == 0 && i + 2 < n_chunks) issue(i + 2, st);
+        const int64_t ck = ckpt_slot(p.se, b, i, tok_end - tok_begin);  // S is the state after chunk i
+        if (ck >= 0) put_state(p.se.ckpt, p.se.ckpt_dtype, ck * per_seq);
+    }
+
+    if (p.se.final_state != nullptr) put_state(p.se.final_state, KDA_F32, b * per_seq);
+    const int64_t ob = out_base(p.se, b);
+    if (ob >= 0) put_state(p.se.out_cache, p.se.out_dtype, ob);
+}
+
 // Multiprocessors of the current device (queried once per device; no synchronisation).
 int64_t sm_count()
 {
@@ -378,6 +629,20 @@ cudaError_t launch_pass(const PassParams &pp, int64_t items, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(items * (D / VT)), WARPS * 32, smem, st>>>(pp);
+    return cudaGetLastError();
+}
+
+template <int D, typename IO, int PAIRS>
+cudaError_t launch_pair(const PassParams &pp, int64_t items, cudaStream_t st)
+{
+    constexpr int VT = 16 * PAIRS;
+    constexpr int STAGE = Rec<D>::UT + VT * C * 2;
+    constexpr int XG = 2 * (D / 32) * 512 + 4 * 512;
+    const int smem = 2 * STAGE + PAIRS * XG + PAIRS * C * 16 * static_cast<int>(sizeof(IO));
+    auto kern = state_pass_pair_kernel<D, IO, PAIRS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(items * (D / VT)), PAIRS * 64, smem, st>>>(pp);
     return cudaGetLastError();
 }
 
@@ -428,11 +693,11 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
             return mark(3);
         }
     }
-    if constexpr (D == 128) {
+    if constexpr (D == 128) {  // at most two 16-column groups per CTA: two warps per group
         if (warps == 8) e = launch_pass<D, IO, 8>(sp, items, st);
         else if (warps == 4) e = launch_pass<D, IO, 4>(sp, items, st);
-        else if (warps == 2) e = launch_pass<D, IO, 2>(sp, items, st);
-        else e = launch_pass<D, IO, 1>(sp, items, st);
+        else if (warps == 2) e = launch_pair<D, IO, 2>(sp, items, st);
+        else e = launch_pair<D, IO, 1>(sp, items, st);
     } else if constexpr (D == 64) {
         if (warps == 4) e = launch_pass<D, IO, 4>(sp, items, st);
         else if (warps == 2) e = launch_pass<D, IO, 2>(sp, items, st);
