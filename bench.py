@@ -10,7 +10,10 @@ One step = one pass of the whole hot path over one batch of synthetic input:
 value = prefill tokens per second of the whole step (decode time included).
 The state-copy bandwidth of the copy workload (fp32 cache [4096,32,128,128]
 with 64 KiB page gaps, 256 rows) is measured in the same run and reported
-next to it, as the metric names both.
+next to it, as the metric names both.  Further legs, each timed on its own:
+the fused cache-indexed prefill with checkpoints, INT8 checkpoints, the short
+convolution, target verification and the long single-sequence prefill
+(131,072 tokens, the few-chain state pass).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
@@ -345,6 +348,40 @@ def conv1d_measure(P, steps: int, warmup: int, W: int = 4) -> dict:
             "shape": f"x [{T}, {C}] bf16, width {W}, SiLU, bf16 states"}
 
 
+def long_prefill_measure(dev, steps: int, warmup: int, tokens: int | None = None) -> dict:
+    """The long single-sequence prefill (131,072 tokens unless `tokens` says otherwise; 32 heads,
+    head size 128, bf16, zero initial state, final state out).  Its state pass is one serial chain of
+    T / 64 chunks per head over only 32 (sequence, head) pairs, the few-chain shape; chunk
+    preparation and state pass are timed separately with events inside the call."""
+    import kimi_delta_attention_varlen_gb300 as kda
+    from kimi_delta_attention_varlen_gb300 import workloads as wl
+    w = wl.long_seq(0, T=tokens) if tokens else wl.long_seq(0)
+    T, H, D = w.lengths[0], w.H, w.K
+    inp = wl.token_inputs(T, H, D, D, w.io_dtype, seed=7, device=dev)
+    out = torch.empty(T, H, D, dtype=w.io_dtype, device=dev)
+    fin = torch.empty(1, H, D, D, dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.kda_prefill_workspace_size(T, 1, H, D, D), dtype=torch.uint8, device=dev)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+
+    def call(ev=None):
+        kda.kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu, out, ws,
+                               final_state=fin, events=ev)
+
+    for _ in range(warmup):
+        call()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in evs:
+        call(e)
+    torch.cuda.synchronize()
+    med = statistics.median
+    prep = med(e[1].elapsed_time(e[2]) for e in evs)
+    pas = med(e[2].elapsed_time(e[3]) for e in evs)
+    tot = med(e[0].elapsed_time(e[3]) for e in evs)
+    del inp, out, fin, ws
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "prep_ms": prep, "pass_ms": pas, "ms": tot, "tokens_per_s": T / (tot * 1e-3)}
+
+
 def verify_measure(P, steps: int, warmup: int, L: int = 4, requests: int | None = None) -> dict:
     """Speculative target verification of L draft tokens for the decode workload's
     requests (bf16 cache [2048, 32, 128, 128], R = 512): every token's state to its own
@@ -508,7 +545,8 @@ def native(args, ranks: Ranks) -> dict | None:
         legs = {"cached_prefill": cached_measure(P, 1, 1),
                 "ckpt_int8": ckpt_int8_measure(P, 1, 1, pairs=64),
                 "conv1d": conv1d_measure(P, 1, 1),
-                "target_verify": verify_measure(P, 1, 1, requests=128)}
+                "target_verify": verify_measure(P, 1, 1, requests=128),
+                "long_prefill": long_prefill_measure(dev, 1, 3, tokens=16384)}
         return {"metric": METRIC, "value": value, "unit": UNIT, "workload": P["w"].name, "tokens": T,
                 "breakdown_ms": br, "legs": legs} if ranks.rank == 0 else None
 
@@ -575,6 +613,7 @@ def native(args, ranks: Ranks) -> dict | None:
     ck8 = ckpt_int8_measure(P, max(5, args.steps), max(3, args.warmup))
     conv = conv1d_measure(P, max(5, args.steps), max(3, args.warmup))
     ver = verify_measure(P, max(5, args.steps), max(3, args.warmup))
+    long_pf = long_prefill_measure(dev, 5, 3)
     pk, pk_kind = peaks()
     nb = prefill_bytes(P)
     flops = prefill_flops(P)
@@ -618,6 +657,7 @@ def native(args, ranks: Ranks) -> dict | None:
         "cached_prefill": {**fused, "unfused_ms": br["gather"] + prefill_ms + br["scatter"]},
         "conv1d": {**conv, "frac": conv["gbs"] / pk["hbm_gbs"]},
         "target_verify": {**ver, "frac": ver["gbs"] / pk["hbm_gbs"]},
+        "long_prefill": long_pf,
         "ckpt_int8": {**ck8, "store_frac": ck8["store"]["gbs"] / pk["hbm_gbs"],
                       "load_frac": ck8["load"]["gbs"] / pk["hbm_gbs"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
