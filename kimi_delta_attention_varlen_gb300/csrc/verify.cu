@@ -16,7 +16,9 @@
 // tokens, so the state is read once and each intermediate state is one
 // coalesced write.  Each thread copies its own slices of the next item's
 // state into shared memory while it computes the current one; the draft
-// tokens' inputs are staged in shared memory 8 tokens at a time.
+// tokens' inputs are staged in shared memory 8 tokens at a time, and each
+// token's factors (norms, q^.k^, e^g, k^ e^g, q^ e^g) are formed once, by one
+// row group, for all rows.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -81,7 +83,13 @@ template <int D, typename IO> struct VerifyLayout {
     static constexpr int V = K + kVT * ROW;
     static constexpr int G = V + kVT * ROW;
     static constexpr int BETA = G + kVT * D * 4;
-    static constexpr int BYTES = BETA + kVT * 4;
+    // per-token factors, fp32 [kVT][D] each: e^g, k^ (normalised k), k^ e^g, q^ e^g; then q^.k^ [kVT]
+    static constexpr int E = BETA + kVT * 4;
+    static constexpr int KN = E + kVT * D * 4;
+    static constexpr int KE = KN + kVT * D * 4;
+    static constexpr int QE = KE + kVT * D * 4;
+    static constexpr int QK = QE + kVT * D * 4;
+    static constexpr int BYTES = QK + kVT * 4;
 };
 
 // Bytes of the token staging, rounded to 16 (the state slots follow it).
@@ -122,6 +130,11 @@ verify_kernel(VerifyArgs a)
     IO *sv = reinterpret_cast<IO *>(smem + VL::V);
     float *sg = reinterpret_cast<float *>(smem + VL::G);
     float *sb = reinterpret_cast<float *>(smem + VL::BETA);
+    float *fe = reinterpret_cast<float *>(smem + VL::E);
+    float *fkn = reinterpret_cast<float *>(smem + VL::KN);
+    float *fke = reinterpret_cast<float *>(smem + VL::KE);
+    float *fqe = reinterpret_cast<float *>(smem + VL::QE);
+    float *fqk = reinterpret_cast<float *>(smem + VL::QK);
     uint4 *slots = reinterpret_cast<uint4 *>(smem + verify_stage_bytes<D, IO>());
     constexpr int IOCH = D * static_cast<int>(sizeof(IO)) / 16;  // 16-byte chunks of one io row
     constexpr int GCH = D * 4 / 16;                               // ... of one g row
@@ -165,6 +178,58 @@ verify_kernel(VerifyArgs a)
         asm volatile("cp.async.commit_group;\n" ::: "memory");
     };
 
+    // The factors of staged token tt, computed once by row group tt (its LPR lanes hold all D
+    // channels, 8 each, exactly as every row group used them) into shared memory.  Groups past
+    // the last token repeat token 0 and store nothing: every lane of a warp takes part in the
+    // full-warp shuffles of the group sums.
+    static_assert(THREADS / LPR >= kVT, "one row group per staged token");
+    auto token_factors = [&](int nt) {
+        const bool mine = tid / LPR < nt;
+        const int tt = mine ? tid / LPR : 0;
+        float qv[8], kv[8], gv[8];
+        load8(sq + tt * D, sizeof(IO) == 4 ? KDA_F32 : KDA_BF16, c0, qv);
+        load8(sk + tt * D, sizeof(IO) == 4 ? KDA_F32 : KDA_BF16, c0, kv);
+        load8(sg + tt * D, KDA_F32, c0, gv);
+        // channel pairs (c, c + 1) go through the packed fp32x2 instructions
+        float2 sq2 = make_float2(0.f, 0.f), sk2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 8; c += 2) {
+            const float2 q2 = make_float2(qv[c], qv[c + 1]), k2 = make_float2(kv[c], kv[c + 1]);
+            sq2 = fma2(q2, q2, sq2);
+            sk2 = fma2(k2, k2, sk2);
+        }
+        const float sqs = group_sum<LPR>(sq2.x + sq2.y);
+        const float sks = group_sum<LPR>(sk2.x + sk2.y);
+        const float nq = a.l2norm ? rsqrtf(sqs + 1e-6f) : 1.f, nk = a.l2norm ? rsqrtf(sks + 1e-6f) : 1.f;
+        float2 qk2 = make_float2(0.f, 0.f);
+        float e[8], kn[8], ke[8], qe[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float2 q2 = mul2(make_float2(qv[2 * c], qv[2 * c + 1]), make_float2(nq, nq));
+            const float2 k2 = mul2(make_float2(kv[2 * c], kv[2 * c + 1]), make_float2(nk, nk));
+            qk2 = fma2(q2, k2, qk2);
+            const float2 e2 = make_float2(ex2_approx(gv[2 * c] * 1.4426950408889634f),  // e^g
+                                          ex2_approx(gv[2 * c + 1] * 1.4426950408889634f));
+            const float2 ke2 = mul2(k2, e2), qe2 = mul2(q2, e2);
+            e[2 * c] = e2.x; e[2 * c + 1] = e2.y;
+            kn[2 * c] = k2.x; kn[2 * c + 1] = k2.y;
+            ke[2 * c] = ke2.x; ke[2 * c + 1] = ke2.y;
+            qe[2 * c] = qe2.x; qe[2 * c + 1] = qe2.y;
+        }
+        const float qk = group_sum<LPR>(qk2.x + qk2.y);
+        if (!mine) return;
+        const int o = tt * D + c0;
+        *reinterpret_cast<float4 *>(fe + o) = make_float4(e[0], e[1], e[2], e[3]);
+        *reinterpret_cast<float4 *>(fe + o + 4) = make_float4(e[4], e[5], e[6], e[7]);
+        *reinterpret_cast<float4 *>(fkn + o) = make_float4(kn[0], kn[1], kn[2], kn[3]);
+        *reinterpret_cast<float4 *>(fkn + o + 4) = make_float4(kn[4], kn[5], kn[6], kn[7]);
+        *reinterpret_cast<float4 *>(fke + o) = make_float4(ke[0], ke[1], ke[2], ke[3]);
+        *reinterpret_cast<float4 *>(fke + o + 4) = make_float4(ke[4], ke[5], ke[6], ke[7]);
+        *reinterpret_cast<float4 *>(fqe + o) = make_float4(qe[0], qe[1], qe[2], qe[3]);
+        *reinterpret_cast<float4 *>(fqe + o + 4) = make_float4(qe[4], qe[5], qe[6], qe[7]);
+        if (tid % LPR == 0) fqk[tt] = qk;
+    };
+
     prefetch_state(it, 0);
     for (int st = 0; it < items; it += gridDim.x, st ^= 1) {
         const int64_t req = it / H;
@@ -177,6 +242,8 @@ verify_kernel(VerifyArgs a)
         else asm volatile("cp.async.commit_group;\n" ::: "memory");
         asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // this item's state and first inputs
         __syncthreads();  // ... including the inputs other threads staged
+        token_factors(a.L < kVT ? a.L : kVT);
+        __syncthreads();
         float s[ROWS][8];
 #pragma unroll
         for (int j = 0; j < ROWS; ++j) {
@@ -204,40 +271,32 @@ verify_kernel(VerifyArgs a)
                 stage_tokens(req, h, t0, nt);
                 cp_async_wait_all();
                 __syncthreads();
+                token_factors(nt);
+                __syncthreads();
             }
             for (int tt = 0; tt < nt; ++tt) {
             const int64_t tok = req * a.L + t0 + tt;
             const int64_t base = (tok * H + h) * D;
-            float qv[8], kv[8], gv[8], vv[ROWS];
-            load8(sq + tt * D, sizeof(IO) == 4 ? KDA_F32 : KDA_BF16, c0, qv);
-            load8(sk + tt * D, sizeof(IO) == 4 ? KDA_F32 : KDA_BF16, c0, kv);
-            load8(sg + tt * D, KDA_F32, c0, gv);
+            float vv[ROWS];
 #pragma unroll
             for (int j = 0; j < ROWS; ++j) vv[j] = load_as_f32(sv + tt * D + r0 + RPP * j);
             const float bt = sb[tt];
-            // channel pairs (c, c + 1) go through the packed fp32x2 instructions
-            float2 sq2 = make_float2(0.f, 0.f), sk2 = make_float2(0.f, 0.f);
+            float2 e[4], ke[4], qe[4], kn[4];
+            {
+                const int o = tt * D + c0;
 #pragma unroll
-            for (int c = 0; c < 8; c += 2) {
-                const float2 q2 = make_float2(qv[c], qv[c + 1]), k2 = make_float2(kv[c], kv[c + 1]);
-                sq2 = fma2(q2, q2, sq2);
-                sk2 = fma2(k2, k2, sk2);
+                for (int h4 = 0; h4 < 2; ++h4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(fe + o + 4 * h4);
+                    const float4 b4 = *reinterpret_cast<const float4 *>(fkn + o + 4 * h4);
+                    const float4 c4 = *reinterpret_cast<const float4 *>(fke + o + 4 * h4);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(fqe + o + 4 * h4);
+                    e[2 * h4] = make_float2(a4.x, a4.y); e[2 * h4 + 1] = make_float2(a4.z, a4.w);
+                    kn[2 * h4] = make_float2(b4.x, b4.y); kn[2 * h4 + 1] = make_float2(b4.z, b4.w);
+                    ke[2 * h4] = make_float2(c4.x, c4.y); ke[2 * h4 + 1] = make_float2(c4.z, c4.w);
+                    qe[2 * h4] = make_float2(d4.x, d4.y); qe[2 * h4 + 1] = make_float2(d4.z, d4.w);
+                }
             }
-            const float sqs = group_sum<LPR>(sq2.x + sq2.y);
-            const float sks = group_sum<LPR>(sk2.x + sk2.y);
-            const float nq = a.l2norm ? rsqrtf(sqs + 1e-6f) : 1.f, nk = a.l2norm ? rsqrtf(sks + 1e-6f) : 1.f;
-            float2 qk2 = make_float2(0.f, 0.f), e[4], ke[4], qe[4], kn[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float2 q2 = mul2(make_float2(qv[2 * c], qv[2 * c + 1]), make_float2(nq, nq));
-                kn[c] = mul2(make_float2(kv[2 * c], kv[2 * c + 1]), make_float2(nk, nk));
-                qk2 = fma2(q2, kn[c], qk2);
-                e[c] = make_float2(ex2_approx(gv[2 * c] * 1.4426950408889634f),  // e^g
-                                   ex2_approx(gv[2 * c + 1] * 1.4426950408889634f));
-                ke[c] = mul2(kn[c], e[c]);
-                qe[c] = mul2(q2, e[c]);
-            }
-            const float qk = group_sum<LPR>(qk2.x + qk2.y);
+            const float qk = fqk[tt];
             const int64_t slot = static_cast<int64_t>(inter[tok]);
             const bool keep = slot >= 0 && slot < a.pool.n_rows;
             if constexpr (2 * ROWS == LPR) {
