@@ -46,12 +46,13 @@ def make_case(lengths, H, D, io, cache_dtype, itype, seed, n_rows=24, gap=64):
     return cu, inp, pc, idx_in, flags, idx_out
 
 
-@pytest.mark.parametrize("D,H,io", [(128, 40, torch.bfloat16), (64, 3, torch.bfloat16), (32, 2, torch.float32)])
+@pytest.mark.parametrize("D,H,io", [(128, 40, torch.bfloat16), (128, 2, torch.bfloat16), (128, 2, torch.float32),
+                                    (64, 3, torch.bfloat16), (32, 2, torch.float32)])
 @pytest.mark.parametrize("cache_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("itype", [torch.int32, torch.int64])
 def test_cached_equals_unfused_bit_for_bit(D, H, io, cache_dtype, itype):
-    """D = 128 with 40 heads x 4 sequences runs the tensor-memory state pass; the
-    others the register pass with value splits."""
+    """D = 128 with 40 heads x 4 sequences runs the tensor-memory state pass, with 2 heads
+    the warp-pair register pass; the others the register pass with value splits."""
     lengths = [130, 0, 64, 257]
     cu, inp, pc, idx_in, flags, idx_out = make_case(lengths, H, D, io, cache_dtype, itype, seed=D + H)
     B, T = len(lengths), cu[-1]
@@ -115,7 +116,7 @@ def test_cached_in_place_slot_reuse_against_oracle():
     assert np.array_equal(after[~touched], before[~touched])  # every other byte untouched
 
 
-@pytest.mark.parametrize("D,H", [(128, 40), (64, 3)])
+@pytest.mark.parametrize("D,H", [(128, 40), (128, 2), (64, 3)])  # tensor-memory, warp-pair, one-warp passes
 @pytest.mark.parametrize("ckpt_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("every", [64, 128, 192])
 def test_checkpoints_match_oracle(D, H, ckpt_dtype, every):
