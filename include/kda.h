@@ -188,7 +188,8 @@ int kda_prefill_varlen(const void *q, const void *k, const void *v, int32_t io_d
  * `events`) on `stream`: events[0] before the chunk-table kernel, events[1]
  * before the chunk-preparation kernel, events[2] before the state-pass
  * kernel, events[3] after it.  For measuring each kernel's device time.
- * events == NULL or any NULL entry returns KDA_ERR_NULL.
+ * events == NULL returns KDA_ERR_NULL; a NULL entry leaves its boundary
+ * unrecorded (each record costs a few microseconds of stream time).
  * ---------------------------------------------------------------------- */
 int kda_prefill_varlen_timed(const void *q, const void *k, const void *v, int32_t io_dtype,
                              const float *g, const float *beta, const int32_t *cu_seqlens,

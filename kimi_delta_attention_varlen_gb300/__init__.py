@@ -121,7 +121,7 @@ def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, out, workspace, *, scale: f
     None; final_state: [B, H, V, K] fp32 or None; workspace: uint8 device tensor of at
     least kda_prefill_workspace_size(T, B, H, K, V) bytes.  events: optional list of four
     torch.cuda.Event (timing enabled) recorded at the boundaries of the three kernels
-    (kda_prefill_varlen_timed)."""
+    (kda_prefill_varlen_timed); a None entry leaves that boundary unrecorded."""
     T, H, K = q.shape
     V = v.shape[2]
     B = cu_seqlens.numel() - 1
@@ -149,9 +149,12 @@ def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, out, workspace, *, scale: f
     if events is None:
         _check(lib().kda_prefill_varlen(*args), "kda_prefill_varlen")
         return
-    _need(len(events) == 4, "events: four torch.cuda.Event")
+    _need(len(events) == 4, "events: four torch.cuda.Event (None leaves that boundary unrecorded)")
     handles = []
     for ev in events:
+        if ev is None:
+            handles.append(None)
+            continue
         if not ev.cuda_event:  # torch creates the event lazily at its first record
             ev.record()
         handles.append(ev.cuda_event)

@@ -165,9 +165,7 @@ int kda_prefill_varlen_timed(const void *q, const void *k, const void *v, int32_
                              int32_t qk_l2norm, const void *init_state, int32_t init_dtype, float *final_state,
                              void *out, void *workspace, size_t ws_bytes, void *stream, void *const *events)
 {
-    if (events == nullptr) return KDA_ERR_NULL;
-    for (int i = 0; i < 4; ++i)
-        if (events[i] == nullptr) return KDA_ERR_NULL;
+    if (events == nullptr) return KDA_ERR_NULL;  // NULL entries: boundaries left unrecorded
     return prefill_impl(q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, dv, scale,
                         qk_l2norm, packed_ends(init_state, init_dtype, final_state), out, workspace, ws_bytes,
                         stream, events);

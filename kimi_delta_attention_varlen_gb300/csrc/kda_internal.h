@@ -135,7 +135,7 @@ struct PrefillArgs {
     StateEnds se;  // ckpt_off is filled in from the workspace
     void *out;
     void *workspace;
-    void *const *events;  // NULL, or 4 cudaEvent_t recorded at the kernel boundaries
+    void *const *events;  // NULL, or 4 cudaEvent_t (NULL entries skipped) recorded at the kernel boundaries
 };
 cudaError_t launch_prefill(const PrefillArgs &a, const PrefillLayout &L, cudaStream_t st);
 

@@ -659,7 +659,7 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     const int32_t ckpt_every = a.se.ckpt != nullptr ? a.se.ckpt_every : 0;
 
     auto mark = [&](int i) -> cudaError_t {
-        return a.events ? cudaEventRecord(static_cast<cudaEvent_t>(a.events[i]), st) : cudaSuccess;
+        return a.events && a.events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(a.events[i]), st) : cudaSuccess;
     };
     cudaError_t e = mark(0);
     if (e != cudaSuccess) return e;

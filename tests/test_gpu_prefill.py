@@ -214,3 +214,25 @@ def test_prefill_state_pass_dispatch(lengths, H):
     out, fin = run_prefill(inp, cu, H, D, init=init, scale=scale)
     heads = None if H <= 4 else [0, 13, 31]
     check_against_oracle(inp, cu, H, D, init, out, fin, scale, heads=heads)
+
+
+def test_timed_prefill_with_unrecorded_boundaries():
+    """events=[None, a, b, None] records only the chunk-preparation interval; the outputs
+    are those of the untimed call, bit for bit."""
+    lengths, H, D = [300, 64, 5], 2, 128
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    T, B = cu[-1], len(lengths)
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=17, device=DEV)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    ws = torch.empty(kda_prefill_workspace_size(T, B, H, D, D), dtype=torch.uint8, device=DEV)
+    outs = []
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for ev in (None, [None, a, b, None]):
+        out = torch.empty(T, H, D, dtype=torch.bfloat16, device=DEV)
+        kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, out, ws, events=ev)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert a.elapsed_time(b) > 0.0
+    assert torch.equal(outs[0].view(torch.uint8), outs[1].view(torch.uint8))
