@@ -172,6 +172,14 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_
  *   workspace   device scratch of at least kda_prefill_workspace_size(...)
  *               bytes, 256-byte aligned; its contents on entry do not matter.
  *   Calls on one workspace must not overlap in time.
+ * Errors, checked on the host before anything is launched: KDA_ERR_DTYPE;
+ * KDA_ERR_SHAPE (num_seqs < 1, total_tokens < 0, h, dk or dv < 1);
+ * KDA_ERR_UNSUPPORTED (head sizes); KDA_ERR_RANGE (total_tokens >= 2^31,
+ * num_seqs >= 2^30, h > 65535, chunk bound x h >= 2^31 or num_seqs x h x 8
+ * >= 2^31: the kernels' one-dimensional grids); KDA_ERR_NULL; KDA_ERR_ALIGN
+ * (16-byte aligned tensors, 4-byte aligned beta and cu_seqlens);
+ * KDA_ERR_WORKSPACE (256-byte alignment, size).  KDA_ERR_CUDA when a launch
+ * fails.
  * ---------------------------------------------------------------------- */
 int kda_prefill_varlen(const void *q, const void *k, const void *v, int32_t io_dtype,
                        const float *g, const float *beta, const int32_t *cu_seqlens,

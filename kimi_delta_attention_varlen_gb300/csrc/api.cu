@@ -131,6 +131,9 @@ int prefill_impl(const void *q, const void *k, const void *v, int32_t io_dtype, 
     kda::PrefillLayout L{};
     if (!kda::prefill_layout(total_tokens, num_seqs, h, dk, &L)) return KDA_ERR_SHAPE;
     if (L.n_chunk_max >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
+    // one-dimensional launch grids: chunk preparation (chunks x heads) and the state pass
+    // ((sequence, head) pairs x at most 8 value slices), checked before anything is launched
+    if (L.n_chunk_max * h >= (INT64_C(1) << 31) || num_seqs * h * 8 >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
     if (!aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
     if (ws_bytes < L.total) return KDA_ERR_WORKSPACE;
     kda::PrefillArgs a{q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, scale,

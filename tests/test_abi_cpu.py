@@ -119,6 +119,8 @@ def test_prefill_rejections(L):
     assert prefill(L, dk=128, dv=64) == UNSUPPORTED
     assert prefill(L, dk=48, dv=48) == UNSUPPORTED
     assert prefill(L, T=1 << 31) == RANGE
+    assert prefill(L, T=1 << 30, h=128) == RANGE  # chunk-preparation grid: 2^24 chunks x 128 heads
+    assert prefill(L, B=1 << 25, h=8) == RANGE  # state-pass grid: 2^28 pairs x up to 8 value slices
     assert prefill(L, cu=None) == NULL
     assert prefill(L, ws=None) == NULL
     assert prefill(L, q=None) == NULL
