@@ -364,8 +364,9 @@ int kda_target_verify(const void *q, const void *k, const void *v, int32_t io_dt
  * channels must be a multiple of 8; all arrays 16-byte aligned (cu_seqlens
  * and indices: their element size).  Errors: KDA_ERR_UNSUPPORTED for W
  * outside 2..4, KDA_ERR_SHAPE for channels % 8 != 0, an unknown activation
- * or a conv cache that does not match W and channels; the others as for the
- * calls above.  Nothing is launched on an error; batch == 0 launches nothing.
+ * or a conv cache that does not match W and channels, KDA_ERR_RANGE for
+ * channels > 65535 * 1024 or (total_tokens + 15) / 8 * ceil(channels / 1024)
+ * > 2^31 - 1 (the kernels' grids); the others as for the calls above.  Nothing is launched on an error; batch == 0 launches nothing.
  * ---------------------------------------------------------------------- */
 int kda_conv1d_varlen(const void *x, int32_t io_dtype, const int32_t *cu_seqlens, int64_t num_seqs,
                       int64_t total_tokens, int64_t channels, int32_t width, const float *weight,

@@ -333,7 +333,8 @@ int check_conv_common(const void *x, int32_t io_dtype, int64_t channels, int32_t
     if (width < 2 || width > 4 || channels < 1) return KDA_ERR_UNSUPPORTED;
     if (channels % 8 != 0) return KDA_ERR_SHAPE;
     if (activation != 0 && activation != 1) return KDA_ERR_SHAPE;
-    if (channels > (INT64_C(1) << 30)) return KDA_ERR_RANGE;
+    // channel blocks sit in the y dimension of the per-sequence and update grids
+    if (channels > INT64_C(65535) * kda::kConvChannelsPerBlock) return KDA_ERR_RANGE;
     if (weight == nullptr) return KDA_ERR_NULL;
     const void *vec16[] = {x, weight, bias, y};
     for (const void *p : vec16)
@@ -353,6 +354,9 @@ int kda_conv1d_varlen(const void *x, int32_t io_dtype, const int32_t *cu_seqlens
     if (num_seqs < 1 || total_tokens < 0) return KDA_ERR_SHAPE;
     if (num_seqs >= (INT64_C(1) << 30) || total_tokens >= (INT64_C(1) << 36)) return KDA_ERR_RANGE;
     if ((total_tokens + 15) / 16 >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
+    // one-dimensional grid of (token block, channel block) pairs, token blocks of 8 or more tokens
+    const int64_t cblocks = (channels + kda::kConvChannelsPerBlock - 1) / kda::kConvChannelsPerBlock;
+    if ((total_tokens + 15) / 8 * cblocks > INT64_C(0x7fffffff)) return KDA_ERR_RANGE;
     if (cu_seqlens == nullptr) return KDA_ERR_NULL;
     if (total_tokens > 0 && (x == nullptr || y == nullptr)) return KDA_ERR_NULL;
     if (!aligned(cu_seqlens, 4)) return KDA_ERR_ALIGN;

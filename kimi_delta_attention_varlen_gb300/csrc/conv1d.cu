@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kConvThreads = 128;
 constexpr int kVec = 8;  // channels per thread
+static_assert(kConvThreads * kVec == kConvChannelsPerBlock, "channel block of the host-side grid checks");
 
 template <typename T> struct Vec8;
 template <> struct Vec8<__nv_bfloat16> {

@@ -17,6 +17,9 @@ struct CacheDesc {
 };
 
 constexpr int kChunk = 64;  // tokens per chunk (the report's extend listing fixes 64)
+// Channels per CTA of the short convolution; the per-sequence and update kernels put these
+// channel blocks in the grid's y dimension (at most 65,535 of them).
+constexpr int kConvChannelsPerBlock = 1024;
 
 cudaError_t launch_state_gather(const CacheDesc &c, const void *idx, int32_t idx_type, int64_t selected,
                                 const uint8_t *flags, void *packed, cudaStream_t st);

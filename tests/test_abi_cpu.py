@@ -261,3 +261,23 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 def test_selftest_bounded_wait_rejections(L):
     assert L.kda_selftest_bounded_wait(None, 1000, 0, None) == NULL
     assert L.kda_selftest_bounded_wait(ctypes.c_void_p(A), 0, 0, None) == RANGE
+
+
+def conv(L, **kw):
+    a = dict(x=A, io=1, cu=A, B=2, T=100, C=64, W=4, w=A, b=None, act=1, init=None, fin=None, sd=1, y=A)
+    a.update(kw)
+    return L.kda_conv1d_varlen(a["x"], a["io"], a["cu"], a["B"], a["T"], a["C"], a["W"], a["w"], a["b"], a["act"],
+                               a["init"], a["fin"], a["sd"], a["y"], None)
+
+
+def test_conv1d_rejections(L):
+    assert conv(L, W=5) == UNSUPPORTED
+    assert conv(L, W=1) == UNSUPPORTED
+    assert conv(L, C=12) == SHAPE
+    assert conv(L, act=2) == SHAPE
+    assert conv(L, io=4) == DTYPE
+    assert conv(L, C=65536 * 1024) == RANGE  # channel blocks beyond the grid's y dimension
+    assert conv(L, T=1 << 30, C=1 << 20) == RANGE  # (token block, channel block) pairs beyond 2^31 - 1
+    assert conv(L, B=0) == SHAPE
+    assert conv(L, w=None) == NULL
+    assert conv(L, x=A + 8) == ALIGN
