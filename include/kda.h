@@ -153,7 +153,10 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_
  *               blocks; results are exact to rounding while every channel's
  *               decay over any 8 consecutive tokens stays above -80
  *               (sum of g > -80); the pages' gate -softplus(N(0,1)) stays
- *               above -30.  g > 0 (growth) is accepted within the same bound.
+ *               above -30.  g > 0 (growth) is accepted within the same bound;
+ *               a growing state amplifies the rounding of the bf16
+ *               tensor-core operands, so the outputs keep the tolerance of
+ *               decaying gates only while growth stays slow.
  *   beta        [total_tokens, h] device fp32
  *   cu_seqlens  [num_seqs + 1] device int32, cu_seqlens[0] = 0, non-
  *               decreasing, cu_seqlens[num_seqs] = total_tokens (precondition,

@@ -236,3 +236,26 @@ def test_timed_prefill_with_unrecorded_boundaries():
     torch.cuda.synchronize()
     assert a.elapsed_time(b) > 0.0
     assert torch.equal(outs[0].view(torch.uint8), outs[1].view(torch.uint8))
+
+
+@pytest.mark.parametrize("D,io", [(128, torch.bfloat16), (32, torch.float32)])
+@pytest.mark.parametrize("gate", ["mixed_sign", "slow_growth", "range_limit"])
+def test_gates_across_the_documented_range(D, io, gate):
+    """Gates inside the documented range: signs mixed with a net decay (about a quarter
+    of the g > 0), a slow steady growth, and a decay of 79.2 nats over any 8 consecutive
+    tokens (just inside the stated -80).  States that grow fast (zero-mean gates of
+    spread 0.5) amplify the bf16 operand rounding beyond the tolerance on every path."""
+    H, lengths = 2, [150, 37, 64]
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    inp = wl.token_inputs(cu[-1], H, D, D, io, seed=D + len(gate), device=DEV)
+    if gate == "mixed_sign":
+        inp["g"].copy_(torch.randn(inp["g"].shape, generator=wl.generator(31, DEV), device=DEV) * 0.5 - 0.3)
+    elif gate == "slow_growth":
+        inp["g"].fill_(0.05)
+    else:
+        inp["g"].fill_(-9.9)
+    init = torch.randn(len(lengths), H, D, D, generator=wl.generator(32, DEV), device=DEV) * 0.5
+    out, fin = run_prefill(inp, cu, H, D, init=init, scale=D ** -0.5)
+    check_against_oracle(inp, cu, H, D, init, out, fin, D ** -0.5)
