@@ -22,9 +22,9 @@
 // run on the tensor cores (bf16 operands, fp32 accumulate).  T' = (I + A_kk)^-1
 // diag(beta) is formed blockwise: the four 16x16 diagonal inverses by fp32
 // forward substitution, the six blocks below them by MMAs (T'_IJ = -T_II
-// sum_K A_IK T'_KJ); then W = T' (K e^G) and U = T' V are plain block
-// products, written in place over their right-hand sides.  W and U^T leave
-// through two bulk copies.
+// sum_K A_IK T'_KJ); then W = T' (K e^G) is a plain block product written in
+// place over its right-hand side, and U^T = V^T T'^T is formed directly in the
+// record's layout.  W and U^T leave through two bulk copies.
 //
 // Exponents: e^{G_i - G_j} = P_i F_IJ R_j with P_i = e^{G_i - G_mI},
 // R_j = e^{G_mJ - G_j} (m = midpoint of the 16-row block) and F_IJ =
@@ -701,18 +701,16 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
 
     // ---- 6. W = T' (K e^G) and U = T' V, block row I from blocks K <= I: warps 0-3 W,
     //         warps 4-7 U, each warp D / NW columns.  The right-hand sides are read into
-    //         registers once (k P tile with e^G = P L_K applied to the fragments, or v), so
-    //         Y_I overwrites them in place; U^T is staged in the q P tile in the record's
-    //         layout. ----
+    //         registers once (k P tile with e^G = P L_K applied to the fragments, or v);
+    //         W_I overwrites its rows of the k P tile in place, U^T goes to the q P tile
+    //         in the record's layout. ----
     {
         constexpr int NW = D / 16 < 4 ? D / 16 : 4;  // warps per matrix with work
         constexpr int COLS = D / NW, NP = COLS / 16;
         const int q4 = warp & 3;
         const int c0 = q4 * COLS;
-        auto product = [&](auto is_u_tag) {
-            constexpr bool kU = decltype(is_u_tag)::value;
-            char *ytile = smem + (kU ? SM::KR : SM::KP);  // right-hand sides in, Y = U or W rows out
-            char *utile = smem + SM::QP;                  // U^T [D][64] bf16, 128-byte swizzled rows
+        auto product_w = [&]() {
+            char *ytile = smem + SM::KP;  // right-hand sides in, W rows out
             uint32_t b[4][NP][4];
 #pragma unroll
             for (int K = 0; K < 4; ++K)
@@ -720,14 +718,13 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
                 for (int np = 0; np < NP; ++np) {
                     ldmatrix_x4_trans(b[K][np], smem_u32(ytile + tile_off<D, C>(16 * K + ri + 8 * (mi & 1),
                                                                               c0 + 16 * np + 8 * (mi >> 1))));
-                    if constexpr (!kU) {  // row k of block K times L_K = e^{G_mK}, column gid of each n8 tile
-                        const float l0 = sL[K * D + c0 + 16 * np + gid], l1 = sL[K * D + c0 + 16 * np + 8 + gid];
-                        const uint32_t f0 = pack_bf16x2(l0, l0), f1 = pack_bf16x2(l1, l1);
-                        b[K][np][0] = mul_bf16x2(b[K][np][0], f0);
-                        b[K][np][1] = mul_bf16x2(b[K][np][1], f0);
-                        b[K][np][2] = mul_bf16x2(b[K][np][2], f1);
-                        b[K][np][3] = mul_bf16x2(b[K][np][3], f1);
-                    }
+                    // row k of block K times L_K = e^{G_mK}, column gid of each n8 tile
+                    const float l0 = sL[K * D + c0 + 16 * np + gid], l1 = sL[K * D + c0 + 16 * np + 8 + gid];
+                    const uint32_t f0 = pack_bf16x2(l0, l0), f1 = pack_bf16x2(l1, l1);
+                    b[K][np][0] = mul_bf16x2(b[K][np][0], f0);
+                    b[K][np][1] = mul_bf16x2(b[K][np][1], f0);
+                    b[K][np][2] = mul_bf16x2(b[K][np][2], f1);
+                    b[K][np][3] = mul_bf16x2(b[K][np][3], f1);
                 }
             __syncwarp();  // every lane holds its fragments before Y overwrites the tile
 #pragma unroll
@@ -752,18 +749,53 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
                         const int i = 16 * I + gid + 8 * hr;
                         const float y0 = acc[n][2 * hr], y1 = acc[n][2 * hr + 1];
                         *reinterpret_cast<uint32_t *>(ytile + static_cast<uint32_t>(i) * ROWB + co) = pack_bf16x2(y0, y1);
-                        if constexpr (kU) {
-                            const int c = c0 + 8 * n + 2 * tig;
-                            *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c, i)) = f32_to_bf16_bits(y0);
-                            *reinterpret_cast<uint16_t *>(utile + swz_off<128>(c + 1, i)) = f32_to_bf16_bits(y1);
-                        }
                     }
                 }
             }
         };
+        // U^T = V^T T'^T formed directly (A: V_K^T by transposed loads of the v tile, B: T'_IK^T
+        // by plain loads of the T' blocks): its accumulators are U^T rows, stored as bf16 pairs in
+        // the record's layout; the U rows themselves are never needed.
+        auto product_ut = [&]() {
+            const char *vtile = smem + SM::KR;
+            char *utile = smem + SM::QP;  // U^T [D][64] bf16, 128-byte swizzled rows
+            uint32_t a[4][NP][4];
+#pragma unroll
+            for (int K = 0; K < 4; ++K)
+#pragma unroll
+                for (int np = 0; np < NP; ++np)
+                    ldmatrix_x4_trans(a[K][np], smem_u32(vtile + tile_off<D, C>(16 * K + ri + 8 * (mi >> 1),
+                                                                               c0 + 16 * np + 8 * (mi & 1))));
+#pragma unroll
+            for (int I = 0; I < 4; ++I) {
+                float acc[NP][2][4] = {};
+#pragma unroll
+                for (int K = 0; K <= I; ++K) {
+                    uint32_t bt[4];
+                    const int tb = K == I ? SM::TS + I * 512 : SM::TO + fslot(I, K) * 512;
+                    ldmatrix_x4(bt, smem_u32(smem + tb + blk_off(0, ri + 8 * (mi >> 1), 8 * (mi & 1))));
+#pragma unroll
+                    for (int np = 0; np < NP; ++np) {
+                        mma_bf16(acc[np][0], a[K][np], bt[0], bt[1]);
+                        mma_bf16(acc[np][1], a[K][np], bt[2], bt[3]);
+                    }
+                }
+#pragma unroll
+                for (int np = 0; np < NP; ++np)
+#pragma unroll
+                    for (int hn = 0; hn < 2; ++hn)
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int c = c0 + 16 * np + gid + 8 * hr;  // value row of U^T
+                            const int t = 16 * I + 8 * hn + 2 * tig;    // token column pair
+                            *reinterpret_cast<uint32_t *>(utile + swz_off<128>(c, t)) =
+                                pack_bf16x2(acc[np][hn][2 * hr], acc[np][hn][2 * hr + 1]);
+                        }
+            }
+        };
         if (q4 < NW) {
-            if (warp >= 4) product(std::true_type{});
-            else product(std::false_type{});
+            if (warp >= 4) product_ut();
+            else product_w();
         }
     }
     fence_proxy_async_smem();  // the W and U^T tiles are read by the bulk copies below
