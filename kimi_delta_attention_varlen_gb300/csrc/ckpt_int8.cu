@@ -35,8 +35,8 @@ template <typename IdxT> __device__ __forceinline__ int64_t idx_at(const void *p
 __device__ __forceinline__ int quantize(float x, float sc, float rc)
 {
     float y = __fmul_rn(x, rc);
-    const float t = y - rintf(y);                        // in [-0.5, 0.5]
-    if (fabsf(fabsf(t) - 0.5f) < 1e-3f) y = __fdiv_rn(x, sc);
+    const float t = y - rintf(y);                        // exact, in [-0.5, 0.5]
+    if (fabsf(t) > 0.499f) y = __fdiv_rn(x, sc);         // within 1e-3 of a half-integer
     const int q = __float2int_rn(y);                     // ties to even
     return q > 127 ? 127 : (q < -127 ? -127 : q);
 }
