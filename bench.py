@@ -99,7 +99,7 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, ranks: Ranks) -> t
 # ---------------------------------------------------------------- clocks --
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) during the timed region."""
+    """nvidia-smi samples (every 100 ms) during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -113,7 +113,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
 
@@ -424,38 +424,62 @@ def verify_measure(P, steps: int, warmup: int, L: int = 4, requests: int | None 
             "tokens_per_s": R * L / (ms * 1e-3)}
 
 
-def copy_measure(dev, steps: int, warmup: int) -> dict:
+def _time_calls(fn, steps: int, warmup: int) -> float:
+    """Median device time (ms) of `steps` calls, events on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def copy_measure(dev, steps: int, warmup: int, hbm_gbs: float, rows: int = 4096) -> dict:
+    """The state-copy workload ([4096, 32, 128, 128] cache, 64 KiB page gaps, 256 selected
+    rows, 10% invalid, flags p = 0.8) in every variant it names: fp32 cache with int32 and
+    int64 indices, bf16 cache with int32 indices, and the scatter of fp32 packed states into
+    the bf16 cache (RNE cast).  Algorithmic bytes: gather reads the valid flagged rows and
+    writes every packed row; scatter reads and writes each valid row (4 B read + 2 B written
+    per element when casting)."""
     import kimi_delta_attention_varlen_gb300 as kda
     from kimi_delta_attention_varlen_gb300 import workloads as wl
-    w = wl.copy_fp32()
-    pc = wl.paged_cache(w.N, w.H, w.V, w.K, w.dtype, w.row_stride, seed=w.seed, device=dev)
-    gidx = wl.gather_indices(w.S, w.N, w.p_invalid, seed=w.seed + 1).to(dev)
-    flags = wl.bernoulli_flags(w.S, w.p_flag, seed=w.seed + 2).to(dev)
-    sidx = wl.scatter_indices(w.S, w.N, w.p_invalid, seed=w.seed + 3).to(dev)
-    packed = torch.empty(w.S, w.H, w.V, w.K, dtype=w.dtype, device=dev)
-    P = w.H * w.V * w.K
-    g_cpu, s_cpu = gidx.cpu(), sidx.cpu()
-    n_g = int(((g_cpu >= 0) & (g_cpu < w.N) & flags.cpu()).sum())
-    n_s = int(((s_cpu >= 0) & (s_cpu < w.N)).sum())
-    g_bytes = (n_g + w.S) * P * 4          # read valid rows, write every packed row
-    s_bytes = 2 * n_s * P * 4              # read + write each valid row
     res = {}
-    for name, fn, nbytes in (("gather", lambda: kda.kda_state_gather(pc.view, gidx, packed, flags), g_bytes),
-                             ("scatter", lambda: kda.kda_state_scatter(pc.view, sidx, packed), s_bytes)):
-        for _ in range(warmup):
-            fn()
-        torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for a, b in evs:
-            a.record()
-            fn()
-            b.record()
-        torch.cuda.synchronize()
-        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-        res[name] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes}
-    del pc, packed
-    torch.cuda.empty_cache()
-    return {"workload": w.name, "index_dtype": "int32", **res}
+    for w in (wl.copy_fp32(N=rows), wl.copy_bf16(N=rows)):
+        pc = wl.paged_cache(w.N, w.H, w.V, w.K, w.dtype, w.row_stride, seed=w.seed, device=dev)
+        es = pc.view.element_size()
+        P = w.H * w.V * w.K
+        flags = wl.bernoulli_flags(w.S, w.p_flag, seed=w.seed + 2).to(dev)
+        packed = torch.empty(w.S, w.H, w.V, w.K, dtype=w.dtype, device=dev)
+        tag = "fp32" if w.dtype == torch.float32 else "bf16"
+        itypes = (torch.int32, torch.int64) if w.dtype == torch.float32 else (torch.int32,)
+        for it in itypes:
+            gidx = wl.gather_indices(w.S, w.N, w.p_invalid, seed=w.seed + 1, dtype=it).to(dev)
+            sidx = wl.scatter_indices(w.S, w.N, w.p_invalid, seed=w.seed + 3, dtype=it).to(dev)
+            g_cpu, s_cpu = gidx.cpu(), sidx.cpu()
+            n_g = int(((g_cpu >= 0) & (g_cpu < w.N) & flags.cpu()).sum())
+            n_s = int(((s_cpu >= 0) & (s_cpu < w.N)).sum())
+            name = f"{tag}_{'int32' if it == torch.int32 else 'int64'}"
+            for op, fn, nbytes in (
+                    ("gather", lambda: kda.kda_state_gather(pc.view, gidx, packed, flags), (n_g + w.S) * P * es),
+                    ("scatter", lambda: kda.kda_state_scatter(pc.view, sidx, packed), 2 * n_s * P * es)):
+                ms = _time_calls(fn, steps, warmup)
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                res[f"{op}_{name}"] = {"ms": ms, "gbs": gbs, "frac": gbs / hbm_gbs, "bytes": nbytes}
+            if w.dtype == torch.bfloat16:  # fp32 packed states cast into the bf16 cache
+                src = torch.randn(w.S, w.H, w.V, w.K, device=dev)
+                nbytes = n_s * P * (4 + 2)
+                ms = _time_calls(lambda: kda.kda_state_scatter(pc.view, sidx, src), steps, warmup)
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                res["scatter_fp32_to_bf16_int32"] = {"ms": ms, "gbs": gbs, "frac": gbs / hbm_gbs, "bytes": nbytes}
+                del src
+        del pc, packed
+        torch.cuda.empty_cache()
+    return {"workload": f"copy: cache [{rows},32,128,128] stride payload+64KiB, S=256, 10% invalid, flags p=0.8",
+            "variants": res, "hbm_peak_gbs": hbm_gbs}
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -510,6 +534,11 @@ def native(args, ranks: Ranks) -> dict | None:
     import kimi_delta_attention_varlen_gb300 as kda  # noqa: F401  (fails loudly if libkda.so is missing)
     dev = torch.device("cuda", ranks.local)
     torch.cuda.set_device(dev)
+    if args.workload == "copy":  # the state-copy legs alone (profiler captures on a smaller cache)
+        pk, pk_kind = peaks()
+        res = copy_measure(dev, args.steps, args.warmup, pk["hbm_gbs"], rows=args.copy_rows)
+        return {"metric": METRIC, "unit": "GB/s", "state_copy": res, "peak_source": pk_kind} if ranks.rank == 0 \
+            else None
     P = build_inputs(dev, small=args.workload == "small")
     T = P["cu_list"][-1]
     stream = torch.cuda.current_stream()
@@ -618,24 +647,30 @@ def native(args, ranks: Ranks) -> dict | None:
     e2e_value, _ = aggregate(T * e2e_steps, a.elapsed_time(b) * 1e-3, ranks)
     del Q, sets
 
-    copy = copy_measure(dev, max(5, args.steps), max(3, args.warmup))
-    fused = cached_measure(P, max(5, args.steps), max(3, args.warmup))
-    ck8 = ckpt_int8_measure(P, max(5, args.steps), max(3, args.warmup))
-    conv = conv1d_measure(P, max(5, args.steps), max(3, args.warmup))
-    ver = verify_measure(P, max(5, args.steps), max(3, args.warmup))
-    long_pf = long_prefill_measure(dev, 5, 3)
     pk, pk_kind = peaks()
+    leg_steps = max(5, min(args.steps, 50))  # the secondary legs report medians of up to 50 calls
+    copy = copy_measure(dev, max(5, min(args.steps, 20)), max(3, args.warmup), pk["hbm_gbs"])
+    fused = cached_measure(P, leg_steps, max(3, args.warmup))
+    ck8 = ckpt_int8_measure(P, leg_steps, max(3, args.warmup))
+    conv = conv1d_measure(P, leg_steps, max(3, args.warmup))
+    ver = verify_measure(P, leg_steps, max(3, args.warmup))
+    long_pf = long_prefill_measure(dev, 5, 3)
     nb = prefill_bytes(P)
     flops = prefill_flops(P)
     prefill_ms = br["chunk_table"] + br["chunk_prep"] + br["state_pass"]
-    # dominant kernel of the step, by measured time
-    kern = {"chunk_prep": (br["chunk_prep"], nb["prep"]), "state_pass": (br["state_pass"], nb["pass"]),
-            "state_gather": (br["gather"], None), "decode_step": (br["decode"], None)}
+    # dominant kernel of the step, by measured time.  Its roofline uses the method's algorithmic
+    # bytes for the units the launch processes: a prefill kernel processes the whole batch
+    # (49,280 B per token at H = 32, K = V = 128 bf16, plus 2 H D^2 4 B of initial and final
+    # state per sequence); the kernel's own compulsory bytes (its inputs plus the per-(chunk,
+    # head) records it writes or reads) are reported beside them.
+    kern = {"chunk_prep": (br["chunk_prep"], nb["method"], nb["prep"]),
+            "state_pass": (br["state_pass"], nb["method"], nb["pass"]),
+            "state_gather": (br["gather"], None, None), "decode_step": (br["decode"], None, None)}
     dom = max(kern, key=lambda k2: kern[k2][0])
-    dom_ms, dom_bytes = kern[dom]
+    dom_ms, dom_bytes, dom_compulsory = kern[dom]
     if dom_bytes is None:
         dw = P["dw"]
-        dom_bytes = 2 * int((dw.idx >= 0).sum()) * dw.H * dw.K * dw.V * 2
+        dom_bytes = dom_compulsory = 2 * int((dw.idx >= 0).sum()) * dw.H * dw.K * dw.V * 2
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = traffic_record(dom, nb["n_chunks"] * P["w"].H)
 
@@ -652,7 +687,10 @@ def native(args, ranks: Ranks) -> dict | None:
                             "number of fully instrumented steps right after the timed region",
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "peak_source": pk_kind, "bytes_per_launch": dom_bytes},
+                     "peak_source": pk_kind, "bytes_per_launch": dom_bytes,
+                     "bytes_convention": "algorithmic: 49,280 B per token + 2 H D^2 4 B per sequence",
+                     "compulsory_bytes_per_launch": dom_compulsory,
+                     "compulsory_frac": dom_compulsory / (dom_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "prefill_roofline": {
             "ms": prefill_ms, "algorithmic_bytes": nb["method"],
             "achieved_gbs": nb["method"] / (prefill_ms * 1e-3) / 1e9,
@@ -662,9 +700,7 @@ def native(args, ranks: Ranks) -> dict | None:
             "attainable_frac": (nb["method"] / (prefill_ms * 1e-3)) /
                                min(pk["bf16_tflops"] * 1e12 * nb["method"] / flops, pk["hbm_gbs"] * 1e9),
             "flop_convention": "dense 64x64 tiles", "peak_source": pk_kind},
-        "state_copy": {**copy, "hbm_peak_gbs": pk["hbm_gbs"],
-                       "gather_frac": copy["gather"]["gbs"] / pk["hbm_gbs"],
-                       "scatter_frac": copy["scatter"]["gbs"] / pk["hbm_gbs"]},
+        "state_copy": copy,
         "decode": {"ms": br["decode"], "requests_per_s": P["dw"].R / (br["decode"] * 1e-3)},
         "cached_prefill": {**fused, "unfused_ms": br["gather"] + prefill_ms + br["scatter"]},
         "conv1d": {**conv, "frac": conv["gbs"] / pk["hbm_gbs"]},
@@ -721,12 +757,14 @@ def reference(args, ranks: Ranks) -> dict | None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["full", "small"], default="full",
+    ap.add_argument("--workload", choices=["full", "small", "copy"], default="full",
                     help="small: 4-sequence varlen batch, step timing plus one call of each next-row leg "
-                         "at reduced sizes (for profiler captures)")
+                         "at reduced sizes (for profiler captures); copy: the state-copy variants alone")
+    ap.add_argument("--copy-rows", type=int, default=4096,
+                    help="cache rows of the state-copy workload (--workload copy; 4096 is the full size)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

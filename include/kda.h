@@ -296,6 +296,11 @@ int64_t kda_prefill_checkpoint_count(const int32_t *cu_seqlens_host, int64_t num
  *   - Every call shares the one array: calls that overlap on the GPU (other
  *     streams, or other threads without ordering) race and corrupt each
  *     other's results.  Its contents left by the previous call do not matter.
+ *   - The caller cannot see the array, so the device status word that
+ *     kda_prefill_workspace_status reads from a workspace is read here by
+ *     kda_prefill_noalloc_status.  The precondition cu_seqlens[num_seqs] ==
+ *     total_tokens also sizes the array's records: a call that breaks it gets
+ *     status 4 and reads no record beyond the array.
  * ---------------------------------------------------------------------- */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
 
@@ -304,6 +309,14 @@ int kda_prefill_varlen_noalloc(const void *q, const void *k, const void *v, int3
                                int64_t num_seqs, int64_t total_tokens, int32_t h, int32_t dk,
                                int32_t dv, float scale, int32_t qk_l2norm, const void *init_state,
                                int32_t init_dtype, float *final_state, void *out, void *stream);
+
+/* The device status word of the last kda_prefill_varlen_noalloc call on the
+ * current device (the codes of kda_prefill_workspace_status), read from the
+ * library's fixed array.  Like kda_prefill_workspace_status it copies 4 bytes
+ * on `stream` and waits; order it after the prefill call (same stream).  The
+ * pages have no counterpart.  KDA_ERR_NULL for a NULL status_out,
+ * KDA_ERR_CUDA if the array's address cannot be looked up or the copy fails. */
+int kda_prefill_noalloc_status(int32_t *status_out, void *stream);
 
 /* ------------------------------------------------------------------------
  * kda_target_verify
@@ -400,7 +413,8 @@ int kda_conv1d_update(const void *x, int32_t io_dtype, int64_t batch, int64_t ch
  *   row's [h][v][k] block x (upcast to fp32):
  *     amax = max_v |x[h][v][k]|,  scale[dst][h][k] = amax / 127,
  *     qdata[dst][h][v][k] = round_half_even(x / scale) clamped to
- *     [-127, 127] (0 when amax == 0),
+ *     [-127, 127]; a scale below the smallest normal fp32 (amax == 0, or
+ *     amax < 127 * 2^-126) is stored as 0 with all codes 0,
  *   each a correctly rounded fp32 operation.  Pairs with an invalid index
  *   are skipped; other slots are not touched.
  * load: for each pair s with 0 <= src_slots[s] < n_slots and
@@ -457,10 +471,14 @@ const char *kda_last_cuda_error_string(void);
  * 0 when every internal wait completed, otherwise a non-zero code (1: a
  * record copy awaited by the register state pass did not complete within its
  * bound; 2: a record copy or MMA awaited by the tensor-memory state pass did
- * not; 3: an input tensor copy awaited by the chunk preparation did not).  A kernel whose wait expires stops waiting, finishes without touching
- * memory it has not been given and releases its tensor memory, so the context
- * stays usable.  This is the one call that synchronises: it copies 4 bytes on
- * `stream` and waits. */
+ * not; 3: an input tensor copy awaited by the chunk preparation did not; 4:
+ * cu_seqlens gave more chunks than total_tokens allows, a broken
+ * precondition whose results are undefined, though no record beyond the
+ * workspace is read).  A kernel whose wait expires stops waiting, finishes
+ * without touching memory it has not been given and releases its tensor
+ * memory, so the context stays usable.  This call and
+ * kda_prefill_noalloc_status are the ones that synchronise: each copies 4
+ * bytes on `stream` and waits. */
 int kda_prefill_workspace_status(const void *workspace, int32_t *status_out, void *stream);
 
 /* Diagnostic of the bounded waits above (infra-level failure detection: a

@@ -25,7 +25,8 @@ from ._abi import (EXPORTED, KDA_BF16, KDA_F32, KDA_I32, KDA_I64, LIB_PATH, KdaC
 
 __all__ = [
     "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
-    "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc", "kda_decode_step",
+    "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc",
+    "kda_prefill_noalloc_status", "kda_decode_step",
     "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_conv1d_varlen", "kda_conv1d_update", "kda_target_verify",
     "kda_status_string", "kda_prefill_workspace_status", "kda_selftest_bounded_wait", "cache_descriptor",
     "KdaError", "EXPORTED", "LIB_PATH",
@@ -413,3 +414,13 @@ def kda_prefill_varlen_noalloc(q, k, v, g, beta, cu_seqlens, out, *, scale: floa
                                           _ptr(init_state), init_code, _ptr(final_state), _ptr(out),
                                           _stream(stream))
     _check(rc, "kda_prefill_varlen_noalloc")
+
+
+def kda_prefill_noalloc_status(stream=None) -> int:
+    """Device status word of the last kda_prefill_varlen_noalloc call on the current
+    device (0 = every internal wait completed; the codes of kda_prefill_workspace_status).
+    The caller never sees the library's fixed scratch array, so this is the only way to
+    read it.  Synchronises the stream."""
+    out = ctypes.c_int32(-1)
+    _check(lib().kda_prefill_noalloc_status(ctypes.byref(out), _stream(stream)), "kda_prefill_noalloc_status")
+    return int(out.value)

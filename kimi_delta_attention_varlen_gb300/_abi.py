@@ -29,6 +29,7 @@ EXPORTED = (
     "kda_prefill_varlen",
     "kda_prefill_varlen_timed",
     "kda_prefill_varlen_noalloc",
+    "kda_prefill_noalloc_status",
     "kda_prefill_varlen_cached",
     "kda_prefill_checkpoint_count",
     "kda_target_verify",
@@ -97,6 +98,8 @@ def lib():
         L.kda_prefill_varlen_timed.restype = ctypes.c_int
         L.kda_prefill_varlen_noalloc.argtypes = L.kda_prefill_varlen.argtypes[:18] + [vp]
         L.kda_prefill_varlen_noalloc.restype = ctypes.c_int
+        L.kda_prefill_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+        L.kda_prefill_noalloc_status.restype = ctypes.c_int
         L.kda_prefill_varlen_cached.argtypes = [vp, vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, i32, f32, i32,
                                                 cache_p, vp, vp, vp, i32, vp, vp, i32, i32, i64, vp, vp, sz, vp]
         L.kda_prefill_varlen_cached.restype = ctypes.c_int

@@ -59,6 +59,8 @@ int check_index_array(const void *idx, int32_t idx_type)
 
 }  // namespace
 
+int kda::record_cuda_status(cudaError_t e) { return cuda_status(e); }
+
 extern "C" {
 
 int kda_state_gather(const kda_cache *cache, const void *idx, int32_t idx_type, int64_t selected,

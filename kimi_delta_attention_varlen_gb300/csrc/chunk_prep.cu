@@ -31,7 +31,12 @@
 // e^{G_mI - G_mJ} <= 1 applied to the A fragments; P and R each span at most 8
 // tokens of decay.  beta is folded into the columns of T' and e^G = P L_K
 // (L_K = e^{G_mK}) into the fragments of the k P tile, so neither beta V nor
-// beta k e^G needs a tile of its own.
+// beta k e^G needs a tile of its own.  The split is exact only while P and R
+// stay in range: the row pass records the largest |G_i - G_mI| of the chunk,
+// and a chunk where it exceeds 2^64 (a decay of more than 44 nats within
+// 8 tokens of some channel) takes exact_gram instead, which forms every
+// e^{G_i - G_j} (i >= j) from its own exponent difference, so any decay,
+// however strong, underflows to zero where it should and nowhere else.
 #include <cudaTypedefs.h>
 
 #include <type_traits>
@@ -174,6 +179,171 @@ template <int N> __device__ __forceinline__ void st_f32(float *p, const float x[
 __device__ __forceinline__ float pick4(const float v0, const float v1, const float v2, const float v3, int idx)
 {
     return idx == 0 ? v0 : idx == 1 ? v1 : idx == 2 ? v2 : v3;
+}
+
+// Largest |G_i - G_mI| (log2 units) for which the block split of the Gram is used:
+// P, R <= 2^64, so a product P F R that underflows is below 2^-62 where it is lost.
+constexpr float kSpanLimit = 64.f;
+
+// Exact gated Gram for a chunk whose decay is too strong for the block split.
+// Every e^{G_i - G_j} (i >= j) is the exponential of its own difference, so it
+// underflows to zero exactly when the true factor is below fp32's range.  Writes
+// what the split path writes: Q~, K~, A_qk (causal, zeros above) and gamma to the
+// record, beta A_kk to the matrix region (blocks below the diagonal in bf16, the
+// diagonal blocks in fp32), the W right-hand side k e^G into the k P tile with
+// L_K = 1.  Scratch while it runs: G^T fp32 in the k P (channels < D/2) and k R
+// tiles, q^T and k^T (bf16, unnormalised) in the q P tile and the matrix region,
+// row norms in the L table.  Rows past the chunk's length are zeros.
+// Transposed tiles [channel][row] put row r of channel c at r ^ (c & 31).
+template <int D, typename IO>
+__device__ __noinline__ void exact_gram(const IO *__restrict__ qg, const IO *__restrict__ kg,
+                                        const float *__restrict__ gg, int32_t Hh, float scale, int32_t l2norm,
+                                        char *smem, char *rec, int64_t t0, int len, int h)
+{
+    using SM = PrepSmem<D>;
+    using R = Rec<D>;
+    constexpr int CPL = D / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t H = Hh;
+    float *rn = reinterpret_cast<float *>(smem + SM::TAB);  // [0, 64) q norms, [64, 128) k norms
+    const float *sBeta = reinterpret_cast<const float *>(smem + SM::BETA);
+    auto gt = [&](int c, int r) -> float * {  // G^T [c][r]
+        char *base = c < D / 2 ? smem + SM::KP : smem + SM::KR;
+        return reinterpret_cast<float *>(base) + (c % (D / 2)) * C + (r ^ (c & 31));
+    };
+    auto qt_at = [&](int c, int r) { return reinterpret_cast<uint16_t *>(smem + SM::QP) + c * C + (r ^ (c & 31)); };
+    auto kt_at = [&](int c, int r) { return reinterpret_cast<uint16_t *>(smem + SM::MREG) + c * C + (r ^ (c & 31)); };
+
+    // (1) row norms: warp w owns rows 8w .. 8w + 7, lanes split the channels
+    for (int j = 0; j < C / kWarps; ++j) {
+        const int i = (C / kWarps) * warp + j;
+        float qv[CPL], kv[CPL];
+        if (i < len) {
+            load_slice<IO, CPL>(qg + ((t0 + i) * H + h) * D + lane * CPL, qv);
+            load_slice<IO, CPL>(kg + ((t0 + i) * H + h) * D + lane * CPL, kv);
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) qv[c] = kv[c] = 0.f;
+        }
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            sq = fmaf(qv[c], qv[c], sq);
+            sk = fmaf(kv[c], kv[c], sk);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        }
+        if (lane == 0) {
+            rn[i] = l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
+            rn[C + i] = l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+        }
+    }
+    // (2) one thread per channel: the in-chunk cumulative sum G (log2 units), raw q and k
+    //     as bf16 operands, and gamma = 2^{G_last}
+    if (tid < D) {
+        const int c = tid;
+        float G = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < C; ++i) {
+            float gv = 0.f, qv = 0.f, kv = 0.f;
+            if (i < len) {
+                const int64_t o = ((t0 + i) * H + h) * D + c;
+                gv = gg[o];
+                qv = load_as_f32<IO>(qg + o);
+                kv = load_as_f32<IO>(kg + o);
+            }
+            G = fmaf(gv, kLog2e, G);
+            *gt(c, i) = G;
+            *qt_at(c, i) = f32_to_bf16_bits(qv);
+            *kt_at(c, i) = f32_to_bf16_bits(kv);
+        }
+        reinterpret_cast<float *>(rec + R::GAMMA)[c] = ex2_approx(G);
+    }
+    __syncthreads();
+
+    // (3) thread t: row i = t / 4, columns j = (t % 4) + 4 m; sums over the channels of
+    //     k_jc e^{G_ic - G_jc} times k_ic (A_kk) and q_ic (A_qk); -inf exponents above the diagonal
+    const int i = tid >> 2, ph = tid & 3;
+    float akk[C / 4], aqk[C / 4];
+#pragma unroll
+    for (int m = 0; m < C / 4; ++m) akk[m] = aqk[m] = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < D; ++c) {
+        const float Gi = *gt(c, i);
+        const float qi = bf16_bits_to_f32(*qt_at(c, i)), ki = bf16_bits_to_f32(*kt_at(c, i));
+#pragma unroll
+        for (int m = 0; m < C / 4; ++m) {
+            const int j = ph + 4 * m;
+            const float d = j <= i ? Gi - *gt(c, j) : -INFINITY;
+            const float t = bf16_bits_to_f32(*kt_at(c, j)) * ex2_approx(d);
+            akk[m] = fmaf(ki, t, akk[m]);
+            aqk[m] = fmaf(qi, t, aqk[m]);
+        }
+    }
+    const float rqi = rn[i], rki = rn[C + i], bi = sBeta[i];
+    float rkj[C / 4];
+#pragma unroll
+    for (int m = 0; m < C / 4; ++m) rkj[m] = rn[C + ph + 4 * m];
+
+    // (4) one thread per channel: Q~ = scale q^ e^G and K~ = k^ e^{G_last - G} to the
+    //     record; k^ e^G (the W right-hand side) kept in registers until G^T is free
+    uint32_t kp[C / 2];
+    if (tid < D) {
+        const int c = tid;
+        const float Gl = *gt(c, C - 1);
+#pragma unroll
+        for (int i2 = 0; i2 < C; i2 += 2) {
+            float kpv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = i2 + e;
+                float qv = 0.f, kv = 0.f;
+                if (r < len) {
+                    const int64_t o = ((t0 + r) * H + h) * D + c;
+                    qv = load_as_f32<IO>(qg + o);
+                    kv = load_as_f32<IO>(kg + o);
+                }
+                const float G = *gt(c, r);
+                const float qh = qv * rn[r], kh = kv * rn[C + r];
+                const float eg = ex2_approx(G);
+                const uint32_t o2 = tile_off<D, C>(r, c);
+                *reinterpret_cast<uint16_t *>(rec + R::QT + o2) = f32_to_bf16_bits(qh * eg * scale);
+                *reinterpret_cast<uint16_t *>(rec + R::KT + o2) = f32_to_bf16_bits(kh * ex2_approx(Gl - G));
+                kpv[e] = kh * eg;
+            }
+            kp[i2 / 2] = pack_bf16x2(kpv[0], kpv[1]);
+        }
+    }
+    __syncthreads();  // every read of the scratch tiles is done
+
+    // (5) results: k e^G into the k P tile, L = 1, beta A_kk to the matrix region, A_qk to the record
+    if (tid < D) {
+#pragma unroll
+        for (int i2 = 0; i2 < C; i2 += 2) {
+            *reinterpret_cast<uint16_t *>(smem + SM::KP + tile_off<D, C>(i2, tid)) =
+                static_cast<uint16_t>(kp[i2 / 2] & 0xffffu);
+            *reinterpret_cast<uint16_t *>(smem + SM::KP + tile_off<D, C>(i2 + 1, tid)) =
+                static_cast<uint16_t>(kp[i2 / 2] >> 16);
+        }
+    }
+    for (int e = tid; e < 4 * D; e += kThreads) rn[e] = 1.f;  // the norms were read above
+    float *sAd = reinterpret_cast<float *>(smem + SM::AD);
+    const int I = i >> 4;
+#pragma unroll
+    for (int m = 0; m < C / 4; ++m) {
+        const int j = ph + 4 * m, J = j >> 4;
+        const float ykk = j < i ? akk[m] * rki * rkj[m] * bi : 0.f;
+        const float yqk = j <= i ? aqk[m] * rqi * rkj[m] * scale : 0.f;
+        if (J < I)
+            *reinterpret_cast<uint16_t *>(smem + SM::AB + blk_off(fslot(I, J), i - 16 * I, j - 16 * J)) =
+                f32_to_bf16_bits(ykk);
+        else if (J == I)
+            sAd[I * 16 * 17 + (i - 16 * I) * 17 + (j - 16 * J)] = ykk;
+        *reinterpret_cast<uint16_t *>(rec + R::AQK + swz_off<128>(i, j)) = f32_to_bf16_bits(yqk);
+    }
 }
 
 template <int D, typename IO>
@@ -415,6 +585,7 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
             nks[j] = __shfl_sync(0xffffffffu, rn, 4 * j + 2);
         }
     }
+    float span = 0.f;  // largest |G_i - G_mI| of this thread's elements (log2 units)
 #pragma unroll
     for (int j0 = 0; j0 < ROWS; j0 += PRE) {
         if (!kStage && j0 > 0) load_rows(j0);
@@ -454,6 +625,7 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
 #pragma unroll
                 for (int c = 0; c < CPL; c += 2) {
                     const float d0 = gr[j0 + j][c] - gmi[c], d1 = gr[j0 + j][c + 1] - gmi[c + 1];
+                    span = fmaxf(span, fmaxf(fabsf(d0), fabsf(d1)));
                     const float2 P = make_float2(ex2_approx(d0), ex2_approx(d1));     // e^{G_i - G_m}
                     const float2 Rr = make_float2(ex2_approx(-d0), ex2_approx(-d1));  // e^{G_m - G_i}
                     const float2 qh = mul2(make_float2(qv[c], qv[c + 1]), make_float2(nq, nq));
@@ -471,6 +643,7 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
 #pragma unroll
                 for (int c = 0; c < CPL; ++c) {
                     const float gi = gr[j0 + j][c];
+                    span = fmaxf(span, fabsf(gi - gmi[c]));
                     const float P = ex2_approx(gi - gmi[c]);   // e^{G_i - G_m}
                     const float Rr = ex2_approx(gmi[c] - gi);  // e^{G_m - G_i}
                     const float qh = qv[c] * nq, kh = kv[c] * nk;
@@ -488,111 +661,115 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
             store_bf16<CPL>(rec + R::KT, o, kt);
         }
     }
-    __syncthreads();
-
-    // A_qk blocks above the diagonal are zero (the record is used as a full 64 x 64 operand)
-    for (int e = tid; e < 6 * 16 * 2; e += kThreads) {
-        const int b = e >> 5, r = (e >> 1) & 15, ch = e & 1;
-        const int I = b < 3 ? 0 : b < 5 ? 1 : 2;        // upper blocks (I, J), J > I
-        const int J = b < 3 ? b + 1 : b < 5 ? b - 1 : 3;
-        *reinterpret_cast<uint4 *>(rec + R::AQK + swz_off<128>(16 * I + r, 16 * J + 8 * ch)) =
-            make_uint4(0u, 0u, 0u, 0u);
-    }
-    // ---- 3. gated Gram products, 20 (matrix, I, J) block pairs over 8 warps ----
-    // A_kk (x beta_i, strictly lower) -> bf16 tile for the substitution products, and its
-    // diagonal blocks in fp32 for their inverses; A_qk (x scale, causal) -> the record.
-    float *sAd = reinterpret_cast<float *>(smem + SM::AD);  // [4][16][17] fp32
-    {
-        // Pairs by slot: u = 0 an off-diagonal pair (warp w: the w-th of 12), u = 1 a diagonal
-        // pair (the w-th of 8), u = 2 (warps 0-3) the off-diagonal pair 8 + w.  Off-diagonal
-        // pairs scale by F_IJ; diagonal ones need no factor.  The first six of each kind are A_kk.
-        constexpr int MAXP = 3;
-        const int npairs = warp < 4 ? 3 : 2;
-        int pI[MAXP], pJ[MAXP];
-        bool pqk[MAXP];
+    // A decay too strong for the block split anywhere in the chunk (uniform over the CTA):
+    // the exact Gram replaces everything the split formed.
+    if (__syncthreads_or(!(span <= kSpanLimit))) {
+        exact_gram<D, IO>(qg, kg, p.g, p.H, p.scale, p.l2norm, smem, rec, t0, len, h);
+    } else {
+        // A_qk blocks above the diagonal are zero (the record is used as a full 64 x 64 operand)
+        for (int e = tid; e < 6 * 16 * 2; e += kThreads) {
+            const int b = e >> 5, r = (e >> 1) & 15, ch = e & 1;
+            const int I = b < 3 ? 0 : b < 5 ? 1 : 2;        // upper blocks (I, J), J > I
+            const int J = b < 3 ? b + 1 : b < 5 ? b - 1 : 3;
+            *reinterpret_cast<uint4 *>(rec + R::AQK + swz_off<128>(16 * I + r, 16 * J + 8 * ch)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        // ---- 3. gated Gram products, 20 (matrix, I, J) block pairs over 8 warps ----
+        // A_kk (x beta_i, strictly lower) -> bf16 tile for the substitution products, and its
+        // diagonal blocks in fp32 for their inverses; A_qk (x scale, causal) -> the record.
+        float *sAd = reinterpret_cast<float *>(smem + SM::AD);  // [4][16][17] fp32
+        {
+            // Pairs by slot: u = 0 an off-diagonal pair (warp w: the w-th of 12), u = 1 a diagonal
+            // pair (the w-th of 8), u = 2 (warps 0-3) the off-diagonal pair 8 + w.  Off-diagonal
+            // pairs scale by F_IJ; diagonal ones need no factor.  The first six of each kind are A_kk.
+            constexpr int MAXP = 3;
+            const int npairs = warp < 4 ? 3 : 2;
+            int pI[MAXP], pJ[MAXP];
+            bool pqk[MAXP];
 #pragma unroll
-        for (int u = 0; u < MAXP; ++u) {
-            if (u == 1) {  // diagonal: index w in 0..7
-                pqk[u] = warp >= 4;
-                pI[u] = pJ[u] = warp & 3;
-            } else {       // off-diagonal: index w or 8 + w in 0..11
-                const int o = u == 0 ? warp : 8 + warp;
-                const int sl = o % 6;  // F slot (I, J), J < I
-                pqk[u] = o >= 6;
-                pI[u] = sl < 1 ? 1 : sl < 3 ? 2 : 3;
-                pJ[u] = sl - pI[u] * (pI[u] - 1) / 2;
+            for (int u = 0; u < MAXP; ++u) {
+                if (u == 1) {  // diagonal: index w in 0..7
+                    pqk[u] = warp >= 4;
+                    pI[u] = pJ[u] = warp & 3;
+                } else {       // off-diagonal: index w or 8 + w in 0..11
+                    const int o = u == 0 ? warp : 8 + warp;
+                    const int sl = o % 6;  // F slot (I, J), J < I
+                    pqk[u] = o >= 6;
+                    pI[u] = sl < 1 ? 1 : sl < 3 ? 2 : 3;
+                    pJ[u] = sl - pI[u] * (pI[u] - 1) / 2;
+                }
             }
-        }
-        float acc[MAXP][2][4] = {};
-        // One k-step of pair u; off-diagonal pairs: a <- a * F_IJ on the fragment's four
-        // channels (bf16x2 products).
-        auto step = [&](int u, int ks, auto scaled) {
-            const int I = pI[u], J = pJ[u];
-            uint32_t a[4], b[4];
-            ldmatrix_x4(a, smem_u32(smem + (pqk[u] ? SM::QP : SM::KP) +
-                                    tile_off<D, C>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
-            if constexpr (decltype(scaled)::value) {
-                const uint16_t *f = sFb + fslot(I, J) * D + 16 * ks + 2 * tig;
-                const uint32_t f01 = *reinterpret_cast<const uint32_t *>(f);
-                const uint32_t f23 = *reinterpret_cast<const uint32_t *>(f + 8);
-                a[0] = mul_bf16x2(a[0], f01);
-                a[1] = mul_bf16x2(a[1], f01);
-                a[2] = mul_bf16x2(a[2], f23);
-                a[3] = mul_bf16x2(a[3], f23);
+            float acc[MAXP][2][4] = {};
+            // One k-step of pair u; off-diagonal pairs: a <- a * F_IJ on the fragment's four
+            // channels (bf16x2 products).
+            auto step = [&](int u, int ks, auto scaled) {
+                const int I = pI[u], J = pJ[u];
+                uint32_t a[4], b[4];
+                ldmatrix_x4(a, smem_u32(smem + (pqk[u] ? SM::QP : SM::KP) +
+                                        tile_off<D, C>(16 * I + ri + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1))));
+                if constexpr (decltype(scaled)::value) {
+                    const uint16_t *f = sFb + fslot(I, J) * D + 16 * ks + 2 * tig;
+                    const uint32_t f01 = *reinterpret_cast<const uint32_t *>(f);
+                    const uint32_t f23 = *reinterpret_cast<const uint32_t *>(f + 8);
+                    a[0] = mul_bf16x2(a[0], f01);
+                    a[1] = mul_bf16x2(a[1], f01);
+                    a[2] = mul_bf16x2(a[2], f23);
+                    a[3] = mul_bf16x2(a[3], f23);
+                }
+                ldmatrix_x4(b, smem_u32(smem + SM::KR +
+                                        tile_off<D, C>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
+                mma_bf16(acc[u][0], a, b[0], b[1]);
+                mma_bf16(acc[u][1], a, b[2], b[3]);
+            };
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {  // every warp: an off-diagonal and a diagonal pair
+                step(0, ks, std::true_type{});
+                step(1, ks, std::false_type{});
             }
-            ldmatrix_x4(b, smem_u32(smem + SM::KR +
-                                    tile_off<D, C>(16 * J + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
-            mma_bf16(acc[u][0], a, b[0], b[1]);
-            mma_bf16(acc[u][1], a, b[2], b[3]);
-        };
+            if (npairs > 2) {  // warps 0-3: one more off-diagonal pair
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // every warp: an off-diagonal and a diagonal pair
-            step(0, ks, std::true_type{});
-            step(1, ks, std::false_type{});
-        }
-        if (npairs > 2) {  // warps 0-3: one more off-diagonal pair
+                for (int ks = 0; ks < D / 16; ++ks) step(2, ks, std::true_type{});
+            }
+            // Epilogue of pair u (one branch per pair on its kind, none per element).
+            auto epilogue = [&](int u) {
+                const int I = pI[u], J = pJ[u];
+                if (!pqk[u]) {  // beta_i A_kk, strictly lower -> bf16 tile (+ fp32 copy of a diagonal block)
+                    float *d = I == J ? sAd + I * 16 * 17 : nullptr;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) step(2, ks, std::true_type{});
-        }
-        // Epilogue of pair u (one branch per pair on its kind, none per element).
-        auto epilogue = [&](int u) {
-            const int I = pI[u], J = pJ[u];
-            if (!pqk[u]) {  // beta_i A_kk, strictly lower -> bf16 tile (+ fp32 copy of a diagonal block)
-                float *d = I == J ? sAd + I * 16 * 17 : nullptr;
+                    for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int i = 16 * I + gid + 8 * hr, j = 16 * J + 8 * nt + 2 * tig;
+                            const float bi = sBeta[i];
+                            const float y0 = j < i ? acc[u][nt][2 * hr] * bi : 0.f;
+                            const float y1 = j + 1 < i ? acc[u][nt][2 * hr + 1] * bi : 0.f;
+                            if (I != J)
+                                *reinterpret_cast<uint32_t *>(smem + SM::AB + blk_off(fslot(I, J), i - 16 * I, j - 16 * J)) =
+                                    pack_bf16x2(y0, y1);
+                            if (d) {  // rows of 17 floats: scalar stores (odd rows are not 8-byte aligned)
+                                d[(i - 16 * I) * 17 + (j - 16 * J)] = y0;
+                                d[(i - 16 * I) * 17 + (j - 16 * J) + 1] = y1;
+                            }
+                        }
+                    }
+                } else {  // scale A_qk, causal -> the record
 #pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int i = 16 * I + gid + 8 * hr, j = 16 * J + 8 * nt + 2 * tig;
-                        const float bi = sBeta[i];
-                        const float y0 = j < i ? acc[u][nt][2 * hr] * bi : 0.f;
-                        const float y1 = j + 1 < i ? acc[u][nt][2 * hr + 1] * bi : 0.f;
-                        if (I != J)
-                            *reinterpret_cast<uint32_t *>(smem + SM::AB + blk_off(fslot(I, J), i - 16 * I, j - 16 * J)) =
-                                pack_bf16x2(y0, y1);
-                        if (d) {  // rows of 17 floats: scalar stores (odd rows are not 8-byte aligned)
-                            d[(i - 16 * I) * 17 + (j - 16 * J)] = y0;
-                            d[(i - 16 * I) * 17 + (j - 16 * J) + 1] = y1;
+                    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int i = 16 * I + gid + 8 * hr, j = 16 * J + 8 * nt + 2 * tig;
+                            const float y0 = j <= i ? acc[u][nt][2 * hr] * p.scale : 0.f;
+                            const float y1 = j + 1 <= i ? acc[u][nt][2 * hr + 1] * p.scale : 0.f;
+                            *reinterpret_cast<uint32_t *>(rec + R::AQK + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
                         }
                     }
                 }
-            } else {  // scale A_qk, causal -> the record
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int i = 16 * I + gid + 8 * hr, j = 16 * J + 8 * nt + 2 * tig;
-                        const float y0 = j <= i ? acc[u][nt][2 * hr] * p.scale : 0.f;
-                        const float y1 = j + 1 <= i ? acc[u][nt][2 * hr + 1] * p.scale : 0.f;
-                        *reinterpret_cast<uint32_t *>(rec + R::AQK + swz_off<128>(i, j)) = pack_bf16x2(y0, y1);
-                    }
-                }
-            }
-        };
-        epilogue(0);
-        epilogue(1);
-        if (npairs > 2) epilogue(2);
-    }
+            };
+            epilogue(0);
+            epilogue(1);
+            if (npairs > 2) epilogue(2);
+        }
+    }  // block split
     __syncthreads();
 
     // v -> the k R tile (free after the Gram products), bf16, zeros past the end; its
@@ -627,7 +804,7 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
     //         stored as they are (TD) and with their columns scaled by beta (TS) ----
     if (warp < 4 && lane < 16) {  // one column per lane
         const int I = warp, j = lane;
-        const float *A = sAd + I * 16 * 17;
+        const float *A = reinterpret_cast<const float *>(smem + SM::AD) + I * 16 * 17;
         // Right-looking: once tcol[k] is final it is subtracted from every later row, so
         // row i still accumulates its terms in the order k = 0, 1, .., i - 1 but the
         // dependent chain is one step per row instead of one per term.

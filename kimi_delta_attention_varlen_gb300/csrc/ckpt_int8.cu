@@ -4,7 +4,8 @@
 //
 // Per (slot, head, key channel k) one fp32 scale from the max-abs over the
 // value dimension: scale = amax / 127, code = round_half_even(x / scale)
-// clamped to [-127, 127] (0 for an all-zero column); loading writes
+// clamped to [-127, 127]; a scale below the smallest normal fp32 (an all-zero
+// column, or every |x| < 127 * 2^-126) is stored as 0 with codes 0; loading writes
 // code * scale in the active row's dtype.  Codes are decided with correctly
 // rounded fp32 division and a round-to-nearest-even conversion.
 //
@@ -131,7 +132,8 @@ ckpt_store_kernel(const ElemT *__restrict__ active, int64_t n_rows, int64_t row_
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         sc[e] = __fdiv_rn(m[e], 127.f);
-        rc[e] = __frcp_rn(sc[e]);
+        if (sc[e] < 1.17549435e-38f) sc[e] = 0.f;  // subnormal scales are stored as 0 (codes 0)
+        rc[e] = sc[e] > 0.f ? __frcp_rn(sc[e]) : 0.f;
     }
     const int64_t sbase = (c * H + h) * static_cast<int64_t>(D);
     const int col = sl * DS + 4 * cg;  // first key column of this thread
@@ -146,7 +148,7 @@ ckpt_store_kernel(const ElemT *__restrict__ active, int64_t n_rows, int64_t row_
         uint32_t packed = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int q = m[e] > 0.f ? quantize(x[e], sc[e], rc[e]) : 0;
+            const int q = sc[e] > 0.f ? quantize(x[e], sc[e], rc[e]) : 0;
             packed |= (static_cast<uint32_t>(q) & 0xffu) << (8 * e);
         }
         *reinterpret_cast<uint32_t *>(qb + static_cast<int64_t>(v) * D + col) = packed;

@@ -10,6 +10,10 @@
 
 namespace kda {
 
+// Maps a CUDA result to a kda_status, remembering a failure for
+// kda_last_cuda_error_string (api.cu).  For entry points defined outside api.cu.
+int record_cuda_status(cudaError_t e);
+
 struct CacheDesc {
     void *data;
     int32_t dtype;

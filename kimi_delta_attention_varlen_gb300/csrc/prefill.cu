@@ -115,6 +115,15 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_ma
     if (tid == 0) *status = 0;
     const int32_t total = block_prefix(
         cu, B, chunk_off, [](int32_t len) { return len > 0 ? (len + C - 1) / C : 0; }, warp_tot, &carry);
+    // cu_seqlens[B] > total_tokens (a broken caller precondition) would give more chunks than
+    // the workspace holds records for: record it and clamp the offsets, so that no state pass
+    // reads a record beyond the workspace.
+    if (total > n_chunk_max) {  // uniform: every thread read the same total
+        if (tid == 0) *status = 4;
+        for (int64_t b = tid; b <= B; b += 1024)
+            if (chunk_off[b] > n_chunk_max) chunk_off[b] = static_cast<int32_t>(n_chunk_max);
+        __syncthreads();
+    }
     if (ckpt_every > 0)  // checkpoints of sequence b: after every ckpt_every tokens, up to its length
         block_prefix(
             cu, B, ckpt_off, [ckpt_every](int32_t len) { return len > 0 ? len / ckpt_every : 0; }, warp_tot, &carry);

@@ -18,7 +18,9 @@
 // GPU (on different streams, or from different threads without ordering) race
 // and corrupt each other's results.  Nothing in the array needs clearing
 // between calls: every byte the kernels read is written earlier in the same
-// call.  No function here allocates.
+// call (the chunk table kernel resets the status word at the array's start).
+// kda_prefill_noalloc_status reads that status word.  No function here
+// allocates.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -29,8 +31,10 @@ namespace {
 
 constexpr size_t kScratchBytes = KDA_NOALLOC_SCRATCH_BYTES;
 
-// Host code sees only a host-side stand-in for this name; the device address
-// comes from cudaGetSymbolAddress below.
+// Device memory.  Host code must never dereference this name or take its
+// address for use as a pointer (on the host it names a shadow variable, not
+// the device array); the device address comes only from cudaGetSymbolAddress
+// in scratch_address below, cached per device.
 __device__ __align__(256) char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -66,7 +70,17 @@ extern "C" int kda_prefill_varlen_noalloc(const void *q, const void *k, const vo
     const size_t need = kda_prefill_workspace_size(total_tokens, num_seqs, h, dk, dv);
     if (need > kScratchBytes) return KDA_ERR_WORKSPACE;  // batch too large for the fixed scratch
     void *scratch = nullptr;
-    if (scratch_address(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
+    const cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) return kda::record_cuda_status(e);
     return kda_prefill_varlen(q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, dv, scale,
                               qk_l2norm, init_state, init_dtype, final_state, out, scratch, kScratchBytes, stream);
+}
+
+extern "C" int kda_prefill_noalloc_status(int32_t *status_out, void *stream)
+{
+    if (status_out == nullptr) return KDA_ERR_NULL;
+    void *scratch = nullptr;
+    const cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) return kda::record_cuda_status(e);
+    return kda_prefill_workspace_status(scratch, status_out, stream);
 }

@@ -72,6 +72,7 @@
  * the caller, so the oracle sees exactly the values the GPU sees.
  * Parity status: pinned (see tests/test_oracle_pins.py for each pin).
  */
+#include <float.h>
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
@@ -187,8 +188,9 @@ static float orc_load_f32(const void *base, int dtype, int64_t e)
  * 0 <= src[s] < n_rows and 0 <= dst[s] < n_slots, and each head h and key
  * channel k of the row's [H, V, K] block x (upcast to fp32):
  *   amax = max over v of |x[h][v][k]|;  scale = amax / 127;
- *   code[v] = round_half_even(x[h][v][k] / scale), clamped to [-127, 127]
- *             (all codes 0 when amax == 0);
+ *   code[v] = round_half_even(x[h][v][k] / scale), clamped to [-127, 127];
+ *   a scale below FLT_MIN (amax == 0, or amax < 127 * 2^-126) is stored
+ *   as 0 with all codes 0 (a reading: the page does not say);
  * qdata[dst][h][v][k] = code, scale_out[dst][h][k] = scale.  Every operation
  * is one correctly rounded fp32 operation (the precision in which the codes
  * are decided on the GPU as well).  Pairs with an invalid index are skipped. */
@@ -208,11 +210,15 @@ int oracle_ckpt_store_int8(const void *active, int dtype, int64_t n_rows, int64_
                     const float a = fabsf(orc_load_f32(active, dtype, r * row_stride + (h * V + v) * K + k));
                     if (a > amax) amax = a;
                 }
-                const float sc = amax / 127.0f;
+                float sc = amax / 127.0f;
+                /* Reading where the page is silent: a scale below the smallest normal
+                 * float (every |x| < 127 * 2^-126) is stored as 0 with all codes 0, so
+                 * no code is ever formed by dividing by a subnormal scale. */
+                if (sc < FLT_MIN) sc = 0.0f;
                 scale_out[(c * H + h) * K + k] = sc;
                 for (int64_t v = 0; v < V; ++v) {
                     int q = 0;
-                    if (amax > 0.0f) {
+                    if (sc > 0.0f) {
                         const float y = orc_load_f32(active, dtype, r * row_stride + (h * V + v) * K + k) / sc;
                         const float rq = nearbyintf(y); /* default rounding: to nearest, ties to even */
                         q = rq > 127.0f ? 127 : rq < -127.0f ? -127 : (int)rq;

@@ -80,3 +80,33 @@ def test_int8_round_trip_error_is_half_a_step():
     assert torch.all(err <= sc.unsqueeze(2) * (0.5 + 1e-5))
     amax = pc.view.abs().amax(dim=2)
     assert torch.allclose(sc, amax / 127, rtol=1e-6)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_int8_store_subnormal_scales(dtype):
+    """Columns whose amax / 127 is 0 or subnormal get scale 0 and codes 0 on both sides;
+    columns just above the smallest normal scale keep the ordinary rule; bit for bit."""
+    H, D = 1, 32
+    tiny = float(torch.finfo(torch.float32).tiny)  # 2^-126
+    x = torch.randn(D, D, generator=wl.generator(5, "cpu"))
+    x[:, 0] = x[:, 0].sign() * 1e-45                # subnormal values: amax / 127 -> 0
+    x[:, 1] = x[:, 1] / x[:, 1].abs().max() * 100 * tiny  # amax = 100 * 2^-126: amax / 127 subnormal
+    x[:, 2] = x[:, 2] * 1e-40
+    x[:, 3] = torch.linspace(-1, 1, D) * 127 * tiny * 2  # amax / 127 = 2^-125, normal
+    x[:, 4] = 0.0
+    x = x.to(dtype).float()  # the values the cache holds
+    pc = wl.paged_cache(2, H, D, D, dtype, None, seed=1, device=DEV)
+    pc.view[1, 0] = x.to(dtype).to(DEV)
+    idx = torch.tensor([1], dtype=torch.int32, device=DEV)
+    q = torch.full((1, H, D, D), 55, dtype=torch.int8, device=DEV)
+    sc = torch.full((1, H, D), -1.0, dtype=torch.float32, device=DEV)
+    kda_ckpt_store_int8(pc.view, idx, torch.zeros_like(idx), q, sc)
+    torch.cuda.synchronize()
+    host = raw(pc.backing)
+    body = np.ascontiguousarray(host[pc.front:pc.front + 2 * pc.row_stride])
+    q_ref = np.full((1, H, D, D), 55, dtype=np.int8)
+    sc_ref = np.full((1, H, D), -1.0, dtype=np.float32)
+    oracle.ckpt_store_int8(body, 2, pc.row_stride, H, D, D, [1], [0], q_ref, sc_ref)
+    assert np.all(sc_ref[0, 0, [0, 1, 2, 4]] == 0.0) and sc_ref[0, 0, 3] > 0.0
+    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), sc_ref.view(np.uint32))

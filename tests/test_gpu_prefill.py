@@ -165,7 +165,7 @@ def test_tiny_workload_gather_prefill_scatter():
     assert np.array_equal(bytes_of(pc.backing), host_before.view(np.uint8))
 
 
-def _full_workload(w, sample_pairs):
+def _full_workload(w, sample_pairs, whole_seqs=()):
     H, D = w.H, w.K
     cu = [0]
     for n in w.lengths:
@@ -177,25 +177,34 @@ def _full_workload(w, sample_pairs):
     out, fin = run_prefill(inp, cu, H, D, init=packed, scale=D ** -0.5)
     kda_state_scatter(pc.view, w.scatter_idx.to(DEV), fin)
     torch.cuda.synchronize()
-    for b, h in sample_pairs:
-        check_against_oracle(inp, cu, H, D, packed, out, fin, D ** -0.5, heads=[h], seqs=[b])
+    for b, h in sample_pairs:  # h: one head, or a list of heads the oracle runs in parallel
+        hs = list(h) if isinstance(h, (list, tuple)) else [h]
+        check_against_oracle(inp, cu, H, D, packed, out, fin, D ** -0.5, heads=hs, seqs=[b])
         r = int(w.scatter_idx[b])
         if 0 <= r < w.cache_rows:  # the scattered row holds exactly the GPU's final state
-            assert torch.equal(pc.view[r, h], fin[b, h].to(pc.view.dtype))
+            assert torch.equal(pc.view[r, hs], fin[b, hs].to(pc.view.dtype))
+    for b in whole_seqs:  # every head of these sequences, the oracle's heads run in parallel
+        check_against_oracle(inp, cu, H, D, packed, out, fin, D ** -0.5, seqs=[b])
+        r = int(w.scatter_idx[b])
+        if 0 <= r < w.cache_rows:
+            assert torch.equal(pc.view[r], fin[b].to(pc.view.dtype))
     return pc, inp, out, fin
 
 
 def test_full_varlen_workload_sampled():
+    """The 16-sequence batch in the benchmark's launch configuration: all 32 heads of the
+    longest and the shortest sequence, plus single heads of others."""
     w = wl.varlen()
     order = sorted(range(w.B), key=lambda b: -w.lengths[b])
-    pairs = [(order[0], 0), (order[0], 31), (order[-1], 7), (order[w.B // 2], 19)]
-    _full_workload(w, pairs)
+    pairs = [(order[1], 0), (order[1], 31), (order[-2], 7), (order[w.B // 2], 19), (order[w.B // 2 + 1], 3)]
+    _full_workload(w, pairs, whole_seqs=(order[0], order[-1]))
     torch.cuda.empty_cache()
 
 
 def test_full_long_sequence_sampled():
+    """The 131,072-token sequence (2,048 chunks per head): four heads against the oracle."""
     w = wl.long_seq()
-    _full_workload(w, [(0, 5)])
+    _full_workload(w, [(0, [0, 5, 18, 31])])
     torch.cuda.empty_cache()
 
 

@@ -606,6 +606,33 @@ def test_int8_checkpoint_power_of_two_scaling_keeps_codes():
     np.testing.assert_array_equal(s2, s1 * 8)
 
 
+def test_int8_checkpoint_subnormal_scales_are_zero():
+    """A column whose amax / 127 falls below the smallest normal float (every value under
+    127 * 2^-126 in magnitude) gets scale 0 and codes 0, whether that scale would be 0 or a
+    subnormal; a column just above keeps the ordinary rule (its max maps to +-127)."""
+    H, V, K = 1, 4, 4
+    tiny = np.float32(np.finfo(np.float32).tiny)  # 2^-126
+    x = np.zeros((1, H, V, K), dtype=np.float32)
+    x[0, 0, :, 0] = [1e-45, -3e-45, 0.0, 2e-45]           # subnormal inputs: amax / 127 -> 0
+    x[0, 0, :, 1] = [100 * tiny, -50 * tiny, 0.0, 1e-40]  # amax / 127 subnormal
+    x[0, 0, :, 2] = [127 * tiny * 2, -tiny, 0.0, 3 * tiny]  # amax / 127 = 2^-125: normal
+    x[0, 0, :, 3] = [0.5, -1.0, 0.25, 0.0]
+    q = np.full((1, H, V, K), 9, dtype=np.int8)
+    sc = np.full((1, H, K), -1.0, dtype=np.float32)
+    oracle.ckpt_store_int8(x.reshape(-1).copy(), 1, V * K, H, V, K, [0], [0], q, sc)
+    assert sc[0, 0, 0] == 0.0 and sc[0, 0, 1] == 0.0
+    assert np.all(q[0, 0, :, :2] == 0)
+    assert sc[0, 0, 2] == np.float32(2 * tiny)  # 254 * 2^-126 / 127 = 2^-125 exactly
+    assert list(q[0, 0, :, 2]) == [127, 0, 0, 2]  # -0.5 -> 0 and 1.5 -> 2: ties to even
+    s3 = np.float32(1.0) / np.float32(127.0)      # correctly rounded, as numpy's float32 division
+    assert sc[0, 0, 3] == s3
+    want = np.rint(x[0, 0, :, 3] / s3).astype(np.int8)  # numpy: IEEE float32 quotient, half-even rint
+    assert list(q[0, 0, :, 3]) == list(want) and want[1] == -127
+    back = np.full(V * K, 7.0, dtype=np.float32)
+    oracle.ckpt_load_int8(q, sc, [0], [0], back, 1, V * K, H, V, K)
+    assert np.all(back.reshape(V, K)[:, :2] == 0.0)
+
+
 # --------------------------------------------------------------------------
 # Short causal convolution
 # --------------------------------------------------------------------------

@@ -1,10 +1,13 @@
 """kda_prefill_varlen_noalloc: the prefill entry point for callers that cannot
 allocate device memory (a host program linking only this library, with no
 device allocator; a runtime whose device memory is fixed at start-up and that
-allows no allocation on the request path).  It must give the same results as
-kda_prefill_varlen with a caller workspace - checked here through the C ABI on
-two calls in a row, since every call reuses the library's one fixed scratch
-array.  The file is named to be collected last."""
+allows no allocation on the request path).  The same kernels run on the same
+inputs, only with the workspace in the library's fixed scratch array, so its
+results must be bit-identical to kda_prefill_varlen with a caller workspace -
+checked here through the C ABI on two calls in a row, since every call reuses
+the one array - and the first batch is also checked against the oracle.  The
+status word of the fixed array (kda_prefill_noalloc_status) must read 0 after
+each call.  The file is named to be collected last."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +15,7 @@ import torch
 import kimi_delta_attention_varlen_gb300 as kda
 from kimi_delta_attention_varlen_gb300 import _abi
 from kimi_delta_attention_varlen_gb300 import workloads as wl
-from tests.helpers import assert_out_close, assert_state_close, f64
+from tests.helpers import assert_out_close, assert_state_close, f64, oracle_prefill_from_device
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -50,13 +53,20 @@ def _noalloc(inp, cu, init):
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     # two different batches back to back: the second call reuses the scratch the first one left
-    for lengths, seed in (([700, 1, 130, 64], 1), ([65, 1000, 300], 2)):
+    for n, (lengths, seed) in enumerate((([700, 1, 130, 64], 1), ([65, 1000, 300], 2))):
         inp, cu, init = _batch(lengths, seed)
         want_out, want_fin = _with_workspace(inp, cu, init)
         got_out, got_fin = _noalloc(inp, cu, init)
-        torch.cuda.synchronize()
-        assert_out_close(f64(got_out), f64(want_out))
-        assert_state_close(f64(got_fin), f64(want_fin))
+        assert kda.kda_prefill_noalloc_status() == 0  # synchronises: every bounded wait completed
+        # same kernels, same inputs: bit for bit the workspace entry point's results
+        assert torch.equal(got_out, want_out)
+        assert torch.equal(got_fin, want_fin)
+        if n == 0:  # and the oracle's, on two heads of every sequence
+            cu_host = cu.tolist()
+            heads = [0, 31]
+            o_ref, f_ref, toks = oracle_prefill_from_device(inp, cu_host, init, 128 ** -0.5, heads=heads)
+            assert_out_close(f64(got_out[toks][:, heads]), o_ref)
+            assert_state_close(f64(got_fin[:, heads]), f_ref)
 
 
 def test_noalloc_rejects_a_batch_beyond_its_scratch():
