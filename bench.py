@@ -226,7 +226,7 @@ def run_step(P, ev=None, prep_only=False):
         ev["d1"].record()
 
 
-LAUNCHES_PER_STEP = 6  # gather, chunk table, chunk prep, state pass, scatter, decode
+LAUNCHES_PER_STEP = 7  # gather, chunk table, chunk prep, exact chunk prep (fix-up list), state pass, scatter, decode
 
 
 def prefill_bytes(P) -> dict:

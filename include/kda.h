@@ -149,14 +149,17 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_
  *   q, k        [total_tokens, h, dk] device, `io_dtype` (bf16 or fp32)
  *   v           [total_tokens, h, dv] device, `io_dtype`
  *   g           [total_tokens, h, dk] device fp32, per-channel log-decay.
- *               The kernels evaluate exp of partial sums of g inside 16-token
- *               blocks; results are exact to rounding while every channel's
- *               decay over any 8 consecutive tokens stays above -80
- *               (sum of g > -80); the pages' gate -softplus(N(0,1)) stays
- *               above -30.  g > 0 (growth) is accepted within the same bound;
- *               a growing state amplifies the rounding of the bf16
- *               tensor-core operands, so the outputs keep the tolerance of
- *               decaying gates only while growth stays slow.
+ *               Any decay (g <= 0, however strong: a factor e^{G_i - G_j}
+ *               below fp32's range is zero, as it is in exact arithmetic to
+ *               within that range).  The kernels split exponentials through
+ *               16-token block midpoints while every channel's partial sums
+ *               stay within 44 nats of them (the pages' gate
+ *               -softplus(N(0,1)) stays within about 15) and evaluate each
+ *               factor from its own exponent difference in the chunks where
+ *               they do not (slower, exact).  g > 0 (growth) is accepted; a
+ *               growing state amplifies the rounding of the bf16 tensor-core
+ *               operands, so the outputs keep the tolerance of decaying gates
+ *               only while growth stays slow.
  *   beta        [total_tokens, h] device fp32
  *   cu_seqlens  [num_seqs + 1] device int32, cu_seqlens[0] = 0, non-
  *               decreasing, cu_seqlens[num_seqs] = total_tokens (precondition,

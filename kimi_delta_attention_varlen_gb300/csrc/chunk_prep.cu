@@ -192,11 +192,11 @@ constexpr float kSpanLimit = 64.f;
 // record, beta A_kk to the matrix region (blocks below the diagonal in bf16, the
 // diagonal blocks in fp32), the W right-hand side k e^G into the k P tile with
 // L_K = 1.  Scratch while it runs: G^T fp32 in the k P (channels < D/2) and k R
-// tiles, q^T and k^T (bf16, unnormalised) in the q P tile and the matrix region,
-// row norms in the L table.  Rows past the chunk's length are zeros.
+// tiles, q^T and k^T (bf16, unnormalised) in the q P tile and the matrix region
+// (offset 0), row norms in the L table.  Rows past the chunk's length are zeros.
 // Transposed tiles [channel][row] put row r of channel c at r ^ (c & 31).
 template <int D, typename IO>
-__device__ __noinline__ void exact_gram(const IO *__restrict__ qg, const IO *__restrict__ kg,
+__device__ __forceinline__ void exact_gram(const IO *__restrict__ qg, const IO *__restrict__ kg,
                                         const float *__restrict__ gg, int32_t Hh, float scale, int32_t l2norm,
                                         char *smem, char *rec, int64_t t0, int len, int h)
 {
@@ -212,7 +212,8 @@ __device__ __noinline__ void exact_gram(const IO *__restrict__ qg, const IO *__r
         return reinterpret_cast<float *>(base) + (c % (D / 2)) * C + (r ^ (c & 31));
     };
     auto qt_at = [&](int c, int r) { return reinterpret_cast<uint16_t *>(smem + SM::QP) + c * C + (r ^ (c & 31)); };
-    auto kt_at = [&](int c, int r) { return reinterpret_cast<uint16_t *>(smem + SM::MREG) + c * C + (r ^ (c & 31)); };
+    auto kt_at = [&](int c, int r) { return reinterpret_cast<uint16_t *>(smem + SM::AB) + c * C + (r ^ (c & 31)); };
+    static_assert(SM::MREG >= SM::TILE, "k^T fits the matrix region");
 
     // (1) row norms: warp w owns rows 8w .. 8w + 7, lanes split the channels
     for (int j = 0; j < C / kWarps; ++j) {
@@ -346,9 +347,13 @@ __device__ __noinline__ void exact_gram(const IO *__restrict__ qg, const IO *__r
     }
 }
 
-template <int D, typename IO>
-__global__ void __launch_bounds__(kThreads, sizeof(IO) == 2 ? 3 : 2)  // bf16: 3 CTAs per SM (≈69 KB smem each)
-chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
+// One (chunk, head): the record.  kExact = false: the block split, or, for a chunk whose
+// decay is out of its range, nothing but an entry in the fix-up list (the CTA leaves before
+// the Gram products); kExact = true: the exact Gram.  `ld_bar` (tensor-copy completion,
+// phase 0 q and k, phase 1 v) is initialised by the kernel; each call completes two phases.
+template <int D, typename IO, bool kExact>
+__device__ __forceinline__ void prep_chunk(const PrepParams &p, const PrepMaps &maps, int64_t chunk, int h,
+                                           char *smem, uint64_t &ld_bar, bool &gave_up)
 {
     using SM = PrepSmem<D>;
     using R = Rec<D>;
@@ -356,12 +361,9 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
     constexpr int CPL = D / 32;                 // channels per lane in the row pass
     constexpr int ROWS = C / kWarps;            // consecutive rows per warp (8: half a 16-row block)
     constexpr int PRE = (sizeof(IO) == 2 || CPL < 4) ? ROWS : ROWS / 2;  // fp32 rows loaded per batch
-    extern __shared__ __align__(1024) char smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, ri = lane & 7;
-    const int64_t chunk = blockIdx.x / p.H;  // heads fastest: the heads of one chunk run together
-    const int h = static_cast<int>(blockIdx.x % p.H);
     const int2 info = p.chunk_info[chunk];
     const int len = info.y;
     if (len <= 0) return;  // past the last chunk (uniform over the CTA)
@@ -383,8 +385,6 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
     const int cb = lane * CPL;
     constexpr bool kStage = sizeof(IO) == 2;  // bf16 rows are staged into their swizzled tiles
     constexpr bool kTma = kStage && D >= 64;  // ... by tensor copies (128-byte swizzle = the tile layout)
-    __shared__ __align__(8) uint64_t ld_bar;   // tensor-copy completion: phase 0 q and k, phase 1 v
-    bool gave_up = false;
     auto wait_loads = [&](uint32_t parity) {
         if (!gave_up && !mbar_wait(&ld_bar, parity, kPrepWaitLimit)) {
             gave_up = true;
@@ -409,8 +409,6 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
     if constexpr (kTma) {  // q -> QP, k -> KP: one tensor copy per 64-channel slab (rows past the
                            // sequence hold the next one's tokens or zeros; beta = 0 there cancels them)
         if (tid == 0) {
-            mbar_init(&ld_bar, 1);
-            fence_mbar_init();
             mbar_arrive_expect_tx(&ld_bar, 2 * SM::TILE);
 #pragma unroll
             for (int sl = 0; sl < D / 64; ++sl) {
@@ -465,8 +463,30 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
     }
     st_f32<CPL>(sSum + warp * D + cb, gr[ROWS - 1]);
     if (warp & 1) st_f32<CPL>(sSum + (kWarps + I) * D + cb, gr[0]);  // row 16 I + 8: the block midpoint
+    // Range of the block split: |G_i - G_mI| (log2 units) of this warp's rows from its local
+    // sums (an odd warp starts at its block's midpoint m; an even warp ends one row before it
+    // and adds g at m).  A chunk where some channel exceeds kSpanLimit goes to the fix-up list,
+    // whose kernel forms the whole record again with the exact Gram; this CTA carries on, and
+    // what it writes is overwritten.  The fast kernel's block index is the item, chunk * H + h.
+    bool wide = false;
+    if constexpr (!kExact) {
+        float gmid[CPL];
+        if (warp & 1) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) gmid[c] = gr[0][c];
+        } else {
+            float g8[CPL] = {};
+            if (r0 + ROWS < len) ldg_f32<CPL>(p.g + ((t0 + r0 + ROWS) * H + h) * D + cb, g8);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) gmid[c] = fmaf(g8[c], kLog2e, gr[ROWS - 1][c]);
+        }
+#pragma unroll
+        for (int j = 0; j < ROWS; ++j)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) wide |= fabsf(gr[j][c] - gmid[c]) > kSpanLimit;
+    }
     cp_async_wait_all();
-    __syncthreads();
+    if (__syncthreads_or(wide) && tid == 0) p.fix_list[atomicAdd(p.fix_count, 1)] = static_cast<int32_t>(blockIdx.x);
     if constexpr (kTma) wait_loads(0);  // q and k are in their tiles
     float gm[4][CPL], glast[CPL], off[CPL];
     {
@@ -585,7 +605,6 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
             nks[j] = __shfl_sync(0xffffffffu, rn, 4 * j + 2);
         }
     }
-    float span = 0.f;  // largest |G_i - G_mI| of this thread's elements (log2 units)
 #pragma unroll
     for (int j0 = 0; j0 < ROWS; j0 += PRE) {
         if (!kStage && j0 > 0) load_rows(j0);
@@ -625,7 +644,6 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
 #pragma unroll
                 for (int c = 0; c < CPL; c += 2) {
                     const float d0 = gr[j0 + j][c] - gmi[c], d1 = gr[j0 + j][c + 1] - gmi[c + 1];
-                    span = fmaxf(span, fmaxf(fabsf(d0), fabsf(d1)));
                     const float2 P = make_float2(ex2_approx(d0), ex2_approx(d1));     // e^{G_i - G_m}
                     const float2 Rr = make_float2(ex2_approx(-d0), ex2_approx(-d1));  // e^{G_m - G_i}
                     const float2 qh = mul2(make_float2(qv[c], qv[c + 1]), make_float2(nq, nq));
@@ -643,7 +661,6 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
 #pragma unroll
                 for (int c = 0; c < CPL; ++c) {
                     const float gi = gr[j0 + j][c];
-                    span = fmaxf(span, fabsf(gi - gmi[c]));
                     const float P = ex2_approx(gi - gmi[c]);   // e^{G_i - G_m}
                     const float Rr = ex2_approx(gmi[c] - gi);  // e^{G_m - G_i}
                     const float qh = qv[c] * nq, kh = kv[c] * nk;
@@ -661,9 +678,8 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
             store_bf16<CPL>(rec + R::KT, o, kt);
         }
     }
-    // A decay too strong for the block split anywhere in the chunk (uniform over the CTA):
-    // the exact Gram replaces everything the split formed.
-    if (__syncthreads_or(!(span <= kSpanLimit))) {
+    __syncthreads();
+    if constexpr (kExact) {
         exact_gram<D, IO>(qg, kg, p.g, p.H, p.scale, p.l2norm, smem, rec, t0, len, h);
     } else {
         // A_qk blocks above the diagonal are zero (the record is used as a full 64 x 64 operand)
@@ -987,6 +1003,47 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
     }
 }
 
+template <int D, typename IO> __device__ __forceinline__ void init_load_barrier(uint64_t &ld_bar)
+{
+    if constexpr (sizeof(IO) == 2 && D >= 64) {
+        if (threadIdx.x == 0) {
+            mbar_init(&ld_bar, 1);
+            fence_mbar_init();
+        }
+    }
+}
+
+// One CTA per (chunk, head), heads fastest in the grid: the heads of one chunk run together.
+template <int D, typename IO>
+__global__ void __launch_bounds__(kThreads, sizeof(IO) == 2 ? 3 : 2)  // bf16: 3 CTAs per SM (≈69 KB smem each)
+chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
+{
+    extern __shared__ __align__(1024) char smem[];
+    __shared__ __align__(8) uint64_t ld_bar;
+    bool gave_up = false;
+    init_load_barrier<D, IO>(ld_bar);
+    prep_chunk<D, IO, false>(p, maps, blockIdx.x / p.H, static_cast<int>(blockIdx.x % p.H), smem, ld_bar, gave_up);
+}
+
+// The (chunk, head) items the block split left in the fix-up list, with the exact Gram;
+// persistent CTAs stride over the list (most calls find it empty and return at once).
+template <int D, typename IO>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_prep_exact_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
+{
+    extern __shared__ __align__(1024) char smem[];
+    __shared__ __align__(8) uint64_t ld_bar;
+    const int32_t n = *p.fix_count;
+    if (static_cast<int32_t>(blockIdx.x) >= n) return;
+    bool gave_up = false;
+    init_load_barrier<D, IO>(ld_bar);
+    for (int32_t i = blockIdx.x; i < n; i += gridDim.x) {
+        const int32_t item = p.fix_list[i];
+        prep_chunk<D, IO, true>(p, maps, item / p.H, item % p.H, smem, ld_bar, gave_up);
+        __syncthreads();  // shared memory and the barrier are reused by the next item
+    }
+}
+
 // cuTensorMapEncodeTiled from the driver, resolved once through the runtime.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
@@ -1032,6 +1089,11 @@ cudaError_t launch_typed(const PrepParams &p, int64_t n_chunk_max, int32_t h, cu
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(n_chunk_max * h), kThreads, smem, st>>>(p, maps);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto fix = chunk_prep_exact_kernel<D, IO>;
+    if ((e = cudaFuncSetAttribute(fix, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+    const int64_t items = n_chunk_max * h, grid = items < 2 * sm_count() ? items : 2 * sm_count();
+    fix<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, maps);
     return cudaGetLastError();
 }
 

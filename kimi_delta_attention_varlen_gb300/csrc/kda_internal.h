@@ -14,6 +14,9 @@ namespace kda {
 // kda_last_cuda_error_string (api.cu).  For entry points defined outside api.cu.
 int record_cuda_status(cudaError_t e);
 
+// Streaming multiprocessors of the current device (cached per device; 152 if unknown).
+int64_t sm_count();
+
 struct CacheDesc {
     void *data;
     int32_t dtype;
@@ -103,7 +106,7 @@ cudaError_t launch_ckpt_load_int8(const CacheDesc &c, const int8_t *qdata, const
 // per (chunk, head) holding the chunk's W, Q~, K~, A_qk, gamma and U^T.
 struct PrefillLayout {
     int64_t n_chunk_max;
-    size_t off_chunk_off, off_seq_order, off_chunk_info, off_ckpt_off, off_records, rec_bytes, total;
+    size_t off_chunk_off, off_seq_order, off_chunk_info, off_ckpt_off, off_fix_list, off_records, rec_bytes, total;
 };
 
 // Where each sequence's initial state comes from and where its final state and

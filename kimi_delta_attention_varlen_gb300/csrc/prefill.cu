@@ -47,6 +47,20 @@
 #include "prefill_common.cuh"
 
 namespace kda {
+
+int64_t sm_count()
+{
+    static std::atomic<int32_t> count[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    int32_t n = count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 namespace {
 
 using prefill::C;
@@ -112,7 +126,10 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_ma
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x;
-    if (tid == 0) *status = 0;
+    if (tid == 0) {
+        status[0] = 0;
+        status[1] = 0;  // the fix-up list of the chunk preparation is empty
+    }
     const int32_t total = block_prefix(
         cu, B, chunk_off, [](int32_t len) { return len > 0 ? (len + C - 1) / C : 0; }, warp_tot, &carry);
     // cu_seqlens[B] > total_tokens (a broken caller precondition) would give more chunks than
@@ -615,18 +632,6 @@ state_pass_pair_kernel(PassParams p)
 }
 
 // Multiprocessors of the current device (queried once per device; no synchronisation).
-int64_t sm_count()
-{
-    static std::atomic<int32_t> count[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-    int32_t n = count[dev].load(std::memory_order_relaxed);
-    if (n <= 0) {
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-        count[dev].store(n, std::memory_order_relaxed);
-    }
-    return n;
-}
 
 template <int D, typename IO, int WARPS>
 cudaError_t launch_pass(const PassParams &pp, int64_t items, cudaStream_t st)
@@ -680,7 +685,8 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
 
     if (L.n_chunk_max > 0) {
         const prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, chunk_info, a.h, a.scale, a.l2norm, records, status,
-                                     a.total_tokens};
+                                     a.total_tokens, status + 1,
+                                     reinterpret_cast<int32_t *>(ws + L.off_fix_list)};
         e = prefill::launch_chunk_prep(D, a.io_dtype, pp, L.n_chunk_max, a.h, st);
         if (e != cudaSuccess) return e;
     }
@@ -733,7 +739,8 @@ bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d
     L.off_seq_order = up(L.off_chunk_off + 4 * static_cast<size_t>(num_seqs + 1), 256);
     L.off_chunk_info = up(L.off_seq_order + 4 * static_cast<size_t>(num_seqs), 256);
     L.off_ckpt_off = up(L.off_chunk_info + 8 * static_cast<size_t>(L.n_chunk_max), 256);
-    L.off_records = up(L.off_ckpt_off + 4 * static_cast<size_t>(num_seqs + 1), 1024);
+    L.off_fix_list = up(L.off_ckpt_off + 4 * static_cast<size_t>(num_seqs + 1), 256);
+    L.off_records = up(L.off_fix_list + 4 * static_cast<size_t>(L.n_chunk_max) * static_cast<size_t>(h), 1024);
     L.total = L.off_records + static_cast<size_t>(L.n_chunk_max) * static_cast<size_t>(h) * L.rec_bytes;
     *out = L;
     return true;

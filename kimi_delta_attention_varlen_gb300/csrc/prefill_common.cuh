@@ -60,6 +60,8 @@ struct PrepParams {
     char *records;
     int32_t *status;       // workspace status word (3: a bounded wait of the prep expired)
     int64_t total_tokens;  // rows of q, k, v (host side: the tensor maps' extent)
+    int32_t *fix_count;    // (chunk, head) items whose decay the block split cannot take ...
+    int32_t *fix_list;     // ... (chunk * H + head), formed by the exact kernel
 };
 
 // Tensor maps of the bf16 q, k, v inputs [T][H][D] (3-D: channel, head, token;

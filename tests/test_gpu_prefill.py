@@ -252,7 +252,7 @@ def test_timed_prefill_with_unrecorded_boundaries():
 def test_gates_across_the_documented_range(D, io, gate):
     """Gates inside the documented range: signs mixed with a net decay (about a quarter
     of the g > 0), a slow steady growth, and a decay of 79.2 nats over any 8 consecutive
-    tokens (just inside the stated -80).  States that grow fast (zero-mean gates of
+    tokens (beyond the block split's range: the chunks take the exact Gram).  States that grow fast (zero-mean gates of
     spread 0.5) amplify the bf16 operand rounding beyond the tolerance on every path."""
     H, lengths = 2, [150, 37, 64]
     cu = [0]
@@ -268,3 +268,43 @@ def test_gates_across_the_documented_range(D, io, gate):
     init = torch.randn(len(lengths), H, D, D, generator=wl.generator(32, DEV), device=DEV) * 0.5
     out, fin = run_prefill(inp, cu, H, D, init=init, scale=D ** -0.5)
     check_against_oracle(inp, cu, H, D, init, out, fin, D ** -0.5)
+
+
+# State-pass forms by shape (the launcher's dispatch): the tensor-memory pass (head size 128,
+# bf16, 96 (sequence, head) pairs), the one-warp register pass (64 pairs), the warp-pair pass
+# (16 pairs), and the register pass at head sizes 64 and 32.
+STRONG_DECAY_FORMS = {
+    "tcgen05": (128, torch.bfloat16, [200, 65, 131], 32, [0, 13, 31]),
+    "one_warp": (128, torch.bfloat16, [150, 71], 32, [0, 21]),
+    "warp_pair": (128, torch.bfloat16, [327, 100, 1, 0], 4, None),
+    "d64": (64, torch.bfloat16, [130, 64, 9], 3, None),
+    "d32_fp32": (32, torch.float32, [100, 37, 64], 2, None),
+}
+
+
+@pytest.mark.parametrize("form", list(STRONG_DECAY_FORMS))
+@pytest.mark.parametrize("gate", ["g_minus_50", "g_minus_1000", "mixed_channels", "spikes"])
+def test_strong_decay_gates(form, gate):
+    """Decays far beyond the block split's range (e^{g} underflows to 0 within a token or
+    a few) against the oracle on every state-pass form: g = -50 and g = -1000 everywhere
+    (the state reduces to beta k v^T, the pin of the token-by-token recurrence), channels
+    alternating -0.1 and -40, and the configs' gates with isolated -200 spikes."""
+    D, io, lengths, H, heads = STRONG_DECAY_FORMS[form]
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    inp = wl.token_inputs(cu[-1], H, D, D, io, seed=D + H + len(gate), device=DEV)
+    g = inp["g"]
+    if gate == "g_minus_50":
+        g.fill_(-50.0)
+    elif gate == "g_minus_1000":
+        g.fill_(-1000.0)
+    elif gate == "mixed_channels":
+        g.copy_(torch.where(torch.arange(D, device=DEV) % 2 == 0, -0.1, -40.0).expand_as(g))
+    else:
+        gen = wl.generator(77, DEV)
+        spikes = torch.rand(g.shape, generator=gen, device=DEV) < 0.002
+        g.copy_(torch.where(spikes, torch.full_like(g, -200.0), g))
+    init = torch.randn(len(lengths), H, D, D, generator=wl.generator(33, DEV), device=DEV) * 0.5
+    out, fin = run_prefill(inp, cu, H, D, init=init, scale=D ** -0.5)
+    check_against_oracle(inp, cu, H, D, init, out, fin, D ** -0.5, heads=heads)
