@@ -130,6 +130,26 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_
                                   int32_t dv);
 
 /* ------------------------------------------------------------------------
+ * kda_prefill_workspace_size_compact
+ *
+ * The smallest workspace kda_prefill_varlen (and _timed, _cached) accepts
+ * for the batch with inputs of `io_dtype`.  For bf16 at dk == dv == 128 it is
+ * a few kilobytes (a header and the chunk table): a call given less than
+ * kda_prefill_workspace_size(...) bytes runs the fused kernel, which keeps
+ * every per-chunk intermediate on chip (one persistent CTA per SM runs the
+ * chunk preparation and the state pass of its (sequence, head) items
+ * together) instead of the two-kernel form, whose per-chunk records (74,240 B
+ * per chunk and head) pass through the workspace.  The results agree within
+ * the same tolerances; the two-kernel form is the faster one on this GPU
+ * (the fused kernel keeps one chunk's preparation in flight per SM), so it is
+ * taken whenever the workspace holds the records.  Other dtypes and head
+ * sizes: the same value as kda_prefill_workspace_size.  0 for an unsupported
+ * combination.
+ * ---------------------------------------------------------------------- */
+size_t kda_prefill_workspace_size_compact(int64_t total_tokens, int64_t num_seqs, int32_t h,
+                                          int32_t dk, int32_t dv, int32_t io_dtype);
+
+/* ------------------------------------------------------------------------
  * kda_prefill_varlen
  *
  * For every sequence b (tokens cu_seqlens[b] .. cu_seqlens[b+1]-1) and head:
@@ -176,7 +196,10 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_
  *               any input (unlike the report's listing, which reuses v's
  *               buffer, the output is a separate buffer here).
  *   workspace   device scratch of at least kda_prefill_workspace_size(...)
- *               bytes, 256-byte aligned; its contents on entry do not matter.
+ *               bytes (the two-kernel form), or, for bf16 at head size 128,
+ *               of at least kda_prefill_workspace_size_compact(...) bytes
+ *               (the fused kernel, when ws_bytes is below the former);
+ *               256-byte aligned; its contents on entry do not matter.
  *   Calls on one workspace must not overlap in time.
  * Errors, checked on the host before anything is launched: KDA_ERR_DTYPE;
  * KDA_ERR_SHAPE (num_seqs < 1, total_tokens < 0, h, dk or dv < 1);
@@ -289,10 +312,14 @@ int64_t kda_prefill_checkpoint_count(const int32_t *cu_seqlens_host, int64_t num
  * workspace: the kernels use a fixed array of KDA_NOALLOC_SCRATCH_BYTES bytes
  * of device memory owned by the library (held by every GPU that loads the
  * library until the process exits).  The call allocates nothing.
- *   - A batch whose kda_prefill_workspace_size(...) exceeds
+ *   - A batch whose kda_prefill_workspace_size_compact(...) exceeds
  *     KDA_NOALLOC_SCRATCH_BYTES is rejected with KDA_ERR_WORKSPACE and
- *     nothing is launched (128 MiB holds, at h = 32, dk = dv = 128, about
- *     53 chunks of 64 tokens: e.g. one 3,300-token sequence).
+ *     nothing is launched.  With bf16 at head size 128 that is never the
+ *     case in practice (the compact workspace is the chunk table: a batch
+ *     larger than the array holds records for, about 53 chunks of 64 tokens
+ *     at h = 32, runs the fused kernel); with fp32, or head size 32 or 64,
+ *     the records must fit (at h = 32, dk = dv = 128, fp32: about 53 chunks,
+ *     e.g. one 3,300-token sequence).
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *     KDA_ERR_CUDA if the lookup fails.

@@ -24,7 +24,8 @@ from ._abi import (EXPORTED, KDA_BF16, KDA_F32, KDA_I32, KDA_I64, LIB_PATH, KdaC
                    _check, lib)
 
 __all__ = [
-    "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_varlen",
+    "kda_state_gather", "kda_state_scatter", "kda_prefill_workspace_size", "kda_prefill_workspace_size_compact",
+    "kda_prefill_varlen",
     "kda_prefill_varlen_cached", "kda_prefill_checkpoint_count", "kda_prefill_varlen_noalloc",
     "kda_prefill_noalloc_status", "kda_decode_step",
     "kda_ckpt_store_int8", "kda_ckpt_load_int8", "kda_conv1d_varlen", "kda_conv1d_update", "kda_target_verify",
@@ -111,6 +112,15 @@ def kda_state_scatter(cache: torch.Tensor, idx: torch.Tensor, packed: torch.Tens
 def kda_prefill_workspace_size(total_tokens: int, num_seqs: int, h: int, dk: int, dv: int) -> int:
     return int(lib().kda_prefill_workspace_size(total_tokens, num_seqs, h, dk, dv))
 
+
+
+def kda_prefill_workspace_size_compact(total_tokens: int, num_seqs: int, h: int, dk: int, dv: int,
+                                       dtype=torch.bfloat16) -> int:
+    """Smallest workspace the prefill accepts for inputs of `dtype`: for bf16 at head size
+    128 the chunk table only (the call then runs the fused kernel, with no per-chunk records
+    in memory); otherwise kda_prefill_workspace_size."""
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(lib().kda_prefill_workspace_size_compact(total_tokens, num_seqs, h, dk, dv, code))
 
 def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, out, workspace, *, scale: float | None = None,
                        qk_l2norm: bool = True, init_state=None, final_state=None, stream=None,

@@ -26,6 +26,7 @@ EXPORTED = (
     "kda_state_gather",
     "kda_state_scatter",
     "kda_prefill_workspace_size",
+    "kda_prefill_workspace_size_compact",
     "kda_prefill_varlen",
     "kda_prefill_varlen_timed",
     "kda_prefill_varlen_noalloc",
@@ -91,6 +92,8 @@ def lib():
         L.kda_state_scatter.restype = ctypes.c_int
         L.kda_prefill_workspace_size.argtypes = [i64, i64, i32, i32, i32]
         L.kda_prefill_workspace_size.restype = sz
+        L.kda_prefill_workspace_size_compact.argtypes = [i64, i64, i32, i32, i32, i32]
+        L.kda_prefill_workspace_size_compact.restype = sz
         L.kda_prefill_varlen.argtypes = [vp, vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, i32, f32, i32,
                                          vp, i32, vp, vp, vp, sz, vp]
         L.kda_prefill_varlen.restype = ctypes.c_int

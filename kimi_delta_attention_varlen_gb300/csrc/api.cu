@@ -30,6 +30,9 @@ bool valid_itype(int32_t t) { return t == KDA_I32 || t == KDA_I64; }
 
 bool built_head_size(int32_t dk, int32_t dv) { return dk == dv && (dk == 32 || dk == 64 || dk == 128); }
 
+// The prefill has a compact form (the fused kernel, no per-chunk records) for bf16 at head size 128.
+bool compact_form(int32_t io_dtype, int32_t dk) { return io_dtype == KDA_BF16 && dk == 128; }
+
 // Layout predicate of the state-copy page ("Automatic dispatch"): fp32/bf16,
 // n_rows > 0, positive inner sizes, rows that do not overlap.
 int check_cache(const kda_cache *c, kda::CacheDesc *out)
@@ -107,6 +110,15 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int64_t num_seqs, int32_
     return L.total;
 }
 
+size_t kda_prefill_workspace_size_compact(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t dk, int32_t dv,
+                                          int32_t io_dtype)
+{
+    if (!built_head_size(dk, dv) || !valid_dtype(io_dtype)) return 0;
+    kda::PrefillLayout L{};
+    if (!kda::prefill_layout(total_tokens, num_seqs, h, dk, &L)) return 0;
+    return compact_form(io_dtype, dk) ? L.compact : L.total;
+}
+
 namespace {
 // Shared by every prefill entry point; `se` says where states come from and go
 // (its cache fields are validated by the caller).
@@ -137,9 +149,9 @@ int prefill_impl(const void *q, const void *k, const void *v, int32_t io_dtype, 
     // ((sequence, head) pairs x at most 8 value slices), checked before anything is launched
     if (L.n_chunk_max * h >= (INT64_C(1) << 31) || num_seqs * h * 8 >= (INT64_C(1) << 31)) return KDA_ERR_RANGE;
     if (!aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
-    if (ws_bytes < L.total) return KDA_ERR_WORKSPACE;
+    if (ws_bytes < (compact_form(io_dtype, dk) ? L.compact : L.total)) return KDA_ERR_WORKSPACE;
     kda::PrefillArgs a{q, k, v, io_dtype, g, beta, cu_seqlens, num_seqs, total_tokens, h, dk, scale,
-                       qk_l2norm ? 1 : 0, se, out, workspace, events};
+                       qk_l2norm ? 1 : 0, se, out, workspace, ws_bytes, events};
     return cuda_status(kda::launch_prefill(a, L, static_cast<cudaStream_t>(stream)));
 }
 

@@ -1044,6 +1044,32 @@ chunk_prep_exact_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
     }
 }
 
+template <int D, typename IO>
+cudaError_t launch_typed(const PrepParams &p, int64_t n_chunk_max, int32_t h, cudaStream_t st)
+{
+    if (p.total_tokens < 1) return cudaSuccess;  // no chunk has rows: every CTA would exit at once
+    if (n_chunk_max * h > 0x7fffffffLL) return cudaErrorInvalidConfiguration;  // one-dimensional grid
+    auto kern = chunk_prep_kernel<D, IO>;
+    constexpr int smem = PrepSmem<D>::BYTES;
+    PrepMaps maps{};
+    if constexpr (sizeof(IO) == 2 && D >= 64) {
+        if (!encode_rows(&maps.q, p.q, p.total_tokens, h, D) || !encode_rows(&maps.k, p.k, p.total_tokens, h, D) ||
+            !encode_rows(&maps.v, p.v, p.total_tokens, h, D))
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(n_chunk_max * h), kThreads, smem, st>>>(p, maps);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto fix = chunk_prep_exact_kernel<D, IO>;
+    if ((e = cudaFuncSetAttribute(fix, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+    const int64_t items = n_chunk_max * h, grid = items < 2 * sm_count() ? items : 2 * sm_count();
+    fix<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, maps);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 // cuTensorMapEncodeTiled from the driver, resolved once through the runtime.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
@@ -1073,31 +1099,18 @@ bool encode_rows(CUtensorMap *m, const void *base, int64_t T, int32_t H, int D)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, typename IO>
-cudaError_t launch_typed(const PrepParams &p, int64_t n_chunk_max, int32_t h, cudaStream_t st)
+bool encode_rows_f32(CUtensorMap *m, const float *base, int64_t T, int32_t H, int D)
 {
-    if (p.total_tokens < 1) return cudaSuccess;  // no chunk has rows: every CTA would exit at once
-    if (n_chunk_max * h > 0x7fffffffLL) return cudaErrorInvalidConfiguration;  // one-dimensional grid
-    auto kern = chunk_prep_kernel<D, IO>;
-    constexpr int smem = PrepSmem<D>::BYTES;
-    PrepMaps maps{};
-    if constexpr (sizeof(IO) == 2 && D >= 64) {
-        if (!encode_rows(&maps.q, p.q, p.total_tokens, h, D) || !encode_rows(&maps.k, p.k, p.total_tokens, h, D) ||
-            !encode_rows(&maps.v, p.v, p.total_tokens, h, D))
-            return cudaErrorInvalidValue;
-    }
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(n_chunk_max * h), kThreads, smem, st>>>(p, maps);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    auto fix = chunk_prep_exact_kernel<D, IO>;
-    if ((e = cudaFuncSetAttribute(fix, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
-    const int64_t items = n_chunk_max * h, grid = items < 2 * sm_count() ? items : 2 * sm_count();
-    fix<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, maps);
-    return cudaGetLastError();
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (fn == nullptr || T < 1) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(H) * D * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(C)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 cudaError_t launch_chunk_prep(int d, int32_t io_dtype, const PrepParams &p, int64_t n_chunk_max, int32_t h,
                               cudaStream_t st)

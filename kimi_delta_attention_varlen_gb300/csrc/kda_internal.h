@@ -107,6 +107,7 @@ cudaError_t launch_ckpt_load_int8(const CacheDesc &c, const int8_t *qdata, const
 struct PrefillLayout {
     int64_t n_chunk_max;
     size_t off_chunk_off, off_seq_order, off_chunk_info, off_ckpt_off, off_fix_list, off_records, rec_bytes, total;
+    size_t compact;  // bytes the fused kernel needs: the header and the chunk table, no records
 };
 
 // Where each sequence's initial state comes from and where its final state and
@@ -145,6 +146,7 @@ struct PrefillArgs {
     StateEnds se;  // ckpt_off is filled in from the workspace
     void *out;
     void *workspace;
+    size_t ws_bytes;      // below the layout's total: the compact form (fused kernel)
     void *const *events;  // NULL, or 4 cudaEvent_t (NULL entries skipped) recorded at the kernel boundaries
 };
 cudaError_t launch_prefill(const PrefillArgs &a, const PrefillLayout &L, cudaStream_t st);

@@ -129,6 +129,7 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_ma
     if (tid == 0) {
         status[0] = 0;
         status[1] = 0;  // the fix-up list of the chunk preparation is empty
+        status[2] = 0;  // the fused kernel's next (sequence, head) item
     }
     const int32_t total = block_prefix(
         cu, B, chunk_off, [](int32_t len) { return len > 0 ? (len + C - 1) / C : 0; }, warp_tot, &carry);
@@ -660,6 +661,7 @@ cudaError_t launch_pair(const PassParams &pp, int64_t items, cudaStream_t st)
     return cudaGetLastError();
 }
 
+
 template <int D, typename IO>
 cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStream_t st)
 {
@@ -682,6 +684,21 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if ((e = mark(1)) != cudaSuccess) return e;
+
+    // Head size 128, bf16, and a workspace without room for the records: the fused kernel
+    // (chunk preparation and state pass in one persistent CTA per SM, no records in memory).
+    if constexpr (D == 128 && sizeof(IO) == 2) {
+        if (a.ws_bytes < L.total) {
+            StateEnds se = a.se;
+            se.ckpt_every = ckpt_every;
+            se.ckpt_off = ckpt_off;
+            e = prefill::launch_prefill_fused(a.q, a.k, a.v, a.g, a.beta, a.cu_seqlens, seq_order, status, status + 2,
+                                              a.num_seqs, a.total_tokens, a.h, a.scale, a.l2norm, se, a.out, st);
+            if (e != cudaSuccess) return e;
+            if ((e = mark(2)) != cudaSuccess) return e;
+            return mark(3);
+        }
+    }
 
     if (L.n_chunk_max > 0) {
         const prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, chunk_info, a.h, a.scale, a.l2norm, records, status,
@@ -740,6 +757,7 @@ bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d
     L.off_chunk_info = up(L.off_seq_order + 4 * static_cast<size_t>(num_seqs), 256);
     L.off_ckpt_off = up(L.off_chunk_info + 8 * static_cast<size_t>(L.n_chunk_max), 256);
     L.off_fix_list = up(L.off_ckpt_off + 4 * static_cast<size_t>(num_seqs + 1), 256);
+    L.compact = L.off_fix_list;
     L.off_records = up(L.off_fix_list + 4 * static_cast<size_t>(L.n_chunk_max) * static_cast<size_t>(h), 1024);
     L.total = L.off_records + static_cast<size_t>(L.n_chunk_max) * static_cast<size_t>(h) * L.rec_bytes;
     *out = L;

@@ -147,6 +147,20 @@ __device__ __forceinline__ void store_state2(void *base, int32_t dtype, int64_t 
 // (sequence, head)) over `items` = num_seqs x h CTAs.
 cudaError_t launch_state_pass_tc(const PassParams &p, int64_t items, cudaStream_t st);
 
+// Tensor map of a bf16 input [T][H][D]: dims (D, H, T), boxes of 64 channels x 1 head
+// x 64 tokens, 128-byte swizzle, zeros outside the tensor (chunk_prep.cu).
+bool encode_rows(CUtensorMap *m, const void *base, int64_t T, int32_t H, int D);
+// ... of an fp32 input [T][H][D] with boxes of D channels x 1 head x 64 tokens, no swizzle.
+bool encode_rows_f32(CUtensorMap *m, const float *base, int64_t T, int32_t H, int D);
+
+// Launches the fused prefill (head size 128, bf16 q, k, v and outputs): one persistent CTA per
+// SM (at most one per item) over the num_seqs x h (sequence, head) items in seq_order.
+// status[0] receives 5 if a bounded wait expires; *item_counter must be zero.
+cudaError_t launch_prefill_fused(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                 const int32_t *cu, const int32_t *seq_order, int32_t *status, int32_t *item_counter,
+                                 int64_t num_seqs, int64_t total_tokens, int32_t h, float scale, int32_t l2norm,
+                                 const StateEnds &se, void *out, cudaStream_t st);
+
 // Launches the chunk-preparation kernel over n_chunk_max x h CTAs (heads fastest).
 cudaError_t launch_chunk_prep(int d, int32_t io_dtype, const PrepParams &p, int64_t n_chunk_max, int32_t h,
                               cudaStream_t st);

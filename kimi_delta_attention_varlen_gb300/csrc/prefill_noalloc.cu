@@ -67,7 +67,8 @@ extern "C" int kda_prefill_varlen_noalloc(const void *q, const void *k, const vo
                                           float scale, int32_t qk_l2norm, const void *init_state,
                                           int32_t init_dtype, float *final_state, void *out, void *stream)
 {
-    const size_t need = kda_prefill_workspace_size(total_tokens, num_seqs, h, dk, dv);
+    // the compact form (bf16, head size 128) needs no per-chunk records
+    const size_t need = kda_prefill_workspace_size_compact(total_tokens, num_seqs, h, dk, dv, io_dtype);
     if (need > kScratchBytes) return KDA_ERR_WORKSPACE;  // batch too large for the fixed scratch
     void *scratch = nullptr;
     const cudaError_t e = scratch_address(&scratch);

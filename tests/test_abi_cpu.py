@@ -130,7 +130,20 @@ def test_prefill_rejections(L):
     assert prefill(L, final=A + 8) == ALIGN
     assert prefill(L, ws=A + 16) == WORKSPACE
     need = L.kda_prefill_workspace_size(100, 2, 4, 128, 128)
-    assert prefill(L, ws_bytes=need - 1) == WORKSPACE
+    assert prefill(L, io=0, ws_bytes=need - 1) == WORKSPACE  # fp32: the records must fit
+    compact = L.kda_prefill_workspace_size_compact(100, 2, 4, 128, 128, 1)
+    assert prefill(L, ws_bytes=compact - 1) == WORKSPACE     # bf16, head size 128: the compact form
+
+
+def test_compact_workspace_size(L):
+    full = L.kda_prefill_workspace_size(73364, 16, 32, 128, 128)
+    compact = L.kda_prefill_workspace_size_compact(73364, 16, 32, 128, 128, 1)
+    # bf16 at head size 128: the header and chunk table only, no per-chunk records
+    assert 0 < compact < 64 << 10 and full > 2_700_000_000
+    assert L.kda_prefill_workspace_size_compact(73364, 16, 32, 128, 128, 0) == full  # fp32: records
+    assert L.kda_prefill_workspace_size_compact(640, 2, 4, 64, 64, 1) == L.kda_prefill_workspace_size(640, 2, 4, 64, 64)
+    assert L.kda_prefill_workspace_size_compact(640, 2, 4, 128, 128, 7) == 0  # unknown dtype
+    assert L.kda_prefill_workspace_size_compact(640, 2, 4, 48, 48, 1) == 0    # head size not built
 
 
 def cached(L, c, **kw):

@@ -7,7 +7,8 @@ results must be bit-identical to kda_prefill_varlen with a caller workspace -
 checked here through the C ABI on two calls in a row, since every call reuses
 the one array - and the first batch is also checked against the oracle.  The
 status word of the fixed array (kda_prefill_noalloc_status) must read 0 after
-each call.  The file is named to be collected last."""
+each call.  Batches whose records do not fit the array run the compact form
+(bf16, head size 128) or are rejected.  The file is named to be collected last."""
 import numpy as np
 import pytest
 import torch
@@ -71,12 +72,29 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 
 def test_noalloc_rejects_a_batch_beyond_its_scratch():
     H, D = 32, 128
-    T = 64 * 64  # 64 chunks of 32 heads: more than the fixed scratch holds
+    T = 64 * 64  # fp32: 64 chunks of 32 heads need more records than the fixed scratch holds
     assert kda.kda_prefill_workspace_size(T, 1, H, D, D) > _abi.KDA_NOALLOC_SCRATCH_BYTES
-    inp, cu, _ = _batch([T], 3)
-    out = torch.zeros(T, H, D, dtype=torch.bfloat16, device=DEV)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=DEV)
+    inp = wl.token_inputs(T, H, D, D, torch.float32, seed=3, device=DEV)
+    out = torch.zeros(T, H, D, dtype=torch.float32, device=DEV)
     with pytest.raises(kda.KdaError) as e:
         kda.kda_prefill_varlen_noalloc(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu, out)
     assert e.value.status == -6  # KDA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert not torch.any(out != 0)  # nothing was launched
+
+
+def test_noalloc_runs_a_large_bf16_batch_in_the_compact_form():
+    # bf16 at head size 128: a batch beyond the records the scratch holds runs the fused
+    # kernel, whose workspace is only the chunk table
+    lengths = [4100, 30, 2000]
+    H, D = 32, 128
+    T = sum(lengths)
+    assert kda.kda_prefill_workspace_size(T, len(lengths), H, D, D) > _abi.KDA_NOALLOC_SCRATCH_BYTES
+    inp, cu, init = _batch(lengths, 4)
+    out, fin = _noalloc(inp, cu, init)
+    assert kda.kda_prefill_noalloc_status() == 0
+    heads = [0, 31]
+    o_ref, f_ref, toks = oracle_prefill_from_device(inp, cu.tolist(), init, 128 ** -0.5, heads=heads)
+    assert_out_close(f64(out[toks][:, heads]), o_ref)
+    assert_state_close(f64(fin[:, heads]), f_ref)
