@@ -386,6 +386,38 @@ def long_prefill_measure(dev, steps: int, warmup: int, tokens: int | None = None
     return {"workload": w.name, "prep_ms": prep, "pass_ms": pas, "ms": tot, "tokens_per_s": T / (tot * 1e-3)}
 
 
+def compact_measure(P, dev, steps: int, warmup: int, long_tokens: int | None = None) -> dict:
+    """The prefill's compact form (bf16, head size 128, a workspace of only the chunk table):
+    the fused kernel on the step's varlen batch and on the long single sequence; median device
+    time and the workspace bytes against the two-kernel form's."""
+    import kimi_delta_attention_varlen_gb300 as kda
+    from kimi_delta_attention_varlen_gb300 import workloads as wl
+    res = {}
+    w = P["w"]
+    T, B, H, D = P["cu_list"][-1], w.B, w.H, w.K
+    inp = P["inp"]
+    ws = torch.empty(kda.kda_prefill_workspace_size_compact(T, B, H, D, D), dtype=torch.uint8, device=dev)
+    ms = _time_calls(lambda: kda.kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], P["cu"],
+                                                    P["out"], ws, init_state=P["packed"], final_state=P["final"]),
+                     steps, warmup)
+    res["varlen"] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3), "workspace_bytes": ws.numel(),
+                     "two_kernel_workspace_bytes": kda.kda_prefill_workspace_size(T, B, H, D, D)}
+    lw = wl.long_seq(0, T=long_tokens) if long_tokens else wl.long_seq(0)
+    TL = lw.lengths[0]
+    li = wl.token_inputs(TL, H, D, D, lw.io_dtype, seed=7, device=dev)
+    lo = torch.empty(TL, H, D, dtype=lw.io_dtype, device=dev)
+    lf = torch.empty(1, H, D, D, dtype=torch.float32, device=dev)
+    lcu = torch.tensor([0, TL], dtype=torch.int32, device=dev)
+    lws = torch.empty(kda.kda_prefill_workspace_size_compact(TL, 1, H, D, D), dtype=torch.uint8, device=dev)
+    ms = _time_calls(lambda: kda.kda_prefill_varlen(li["q"], li["k"], li["v"], li["g"], li["beta"], lcu, lo, lws,
+                                                    final_state=lf), max(2, min(steps, 5)), 1)
+    res["long"] = {"workload": lw.name, "ms": ms, "tokens_per_s": TL / (ms * 1e-3), "workspace_bytes": lws.numel(),
+                   "two_kernel_workspace_bytes": kda.kda_prefill_workspace_size(TL, 1, H, D, D)}
+    del li, lo, lf, lws, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def verify_measure(P, steps: int, warmup: int, L: int = 4, requests: int | None = None) -> dict:
     """Speculative target verification of L draft tokens for the decode workload's
     requests (bf16 cache [2048, 32, 128, 128], R = 512): every token's state to its own
@@ -585,6 +617,7 @@ def native(args, ranks: Ranks) -> dict | None:
                 "ckpt_int8": ckpt_int8_measure(P, 1, 1, pairs=64),
                 "conv1d": conv1d_measure(P, 1, 1),
                 "target_verify": verify_measure(P, 1, 1, requests=128),
+                "compact_prefill": compact_measure(P, dev, 1, 1, long_tokens=16384),
                 "long_prefill": long_prefill_measure(dev, 1, 3, tokens=16384)}
         return {"metric": METRIC, "value": value, "unit": UNIT, "workload": P["w"].name, "tokens": T,
                 "breakdown_ms": br, "legs": legs} if ranks.rank == 0 else None
@@ -655,6 +688,7 @@ def native(args, ranks: Ranks) -> dict | None:
     conv = conv1d_measure(P, leg_steps, max(3, args.warmup))
     ver = verify_measure(P, leg_steps, max(3, args.warmup))
     long_pf = long_prefill_measure(dev, 5, 3)
+    compact = compact_measure(P, dev, leg_steps, max(3, args.warmup))
     nb = prefill_bytes(P)
     flops = prefill_flops(P)
     prefill_ms = br["chunk_table"] + br["chunk_prep"] + br["state_pass"]
@@ -706,6 +740,7 @@ def native(args, ranks: Ranks) -> dict | None:
         "conv1d": {**conv, "frac": conv["gbs"] / pk["hbm_gbs"]},
         "target_verify": {**ver, "frac": ver["gbs"] / pk["hbm_gbs"]},
         "long_prefill": long_pf,
+        "compact_prefill": compact,
         "ckpt_int8": {**ck8, "store_frac": ck8["store"]["gbs"] / pk["hbm_gbs"],
                       "load_frac": ck8["load"]["gbs"] / pk["hbm_gbs"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
