@@ -13,10 +13,12 @@
 //
 // Layout: S^T (fp32, 128 lanes x 128 columns), X^T (64 columns) and two
 // Y^T/O^T buffers (64 columns each) live in tensor memory.  Value row v is TMEM
-// lane v; four warps share each 32-lane quadrant and split its columns.  The MMA
-// operands are bf16 in shared memory in the 128-byte-swizzle layout: S^T and
-// V_new^T written by the threads each chunk, W, Q~, A_qk (K-major) and K~
-// (MN-major) straight from the bulk-copied record.  One thread issues the MMAs;
+// lane v; four warps share each 32-lane quadrant and split its columns.  The
+// A operands of the MMAs, S^T and V_new^T in bf16, are written by the threads
+// into tensor memory too (two values per column), so the tensor cores read only
+// the B operands from shared memory: W, Q~, A_qk (K-major) and K~ (MN-major),
+// straight from the bulk-copied record in the 128-byte-swizzle layout.  One
+// thread issues the MMAs;
 // an mbarrier signals their completion.  Records are double-buffered (the
 // copy of chunk i + 2 starts when chunk i is done).  The outputs of chunk
 // i - 1 move from tensor memory to a staging tile while the first MMA group of
@@ -39,15 +41,17 @@ constexpr uint32_t kTcWaitLimit = 1u << 22;
 constexpr int kTcD = 128;
 using RT = Rec<kTcD>;
 constexpr int kStage = (RT::BYTES + 1023) / 1024 * 1024;  // one record, padded to 1 KiB
-constexpr int kSA = 2 * kStage;          // S^T bf16 [128][128] (2 slabs); V_new^T [128][64] reuses slab 0
-constexpr int kOS = kSA + 32768;         // output staging bf16 [64 tokens][128 values]
+constexpr int kOS = 2 * kStage;          // output staging bf16 [64 tokens][128 values]
 constexpr int kTcSmem = kOS + 16384 + 1024;  // + slack to align the base to 1 KiB
-constexpr uint32_t kColS = 0, kColX = 128, kColY = 192, kTmemCols = 512;  // Y buffers at 192 and 256
+// Tensor memory: S^T fp32 (128 columns), X^T (64), two Y^T / O^T buffers (64 each), and the MMAs'
+// A operands in bf16, two values per 32-bit column: S^T (64 columns) and V_new^T (32).
+constexpr uint32_t kColS = 0, kColX = 128, kColY = 192, kColA = 320, kColV = 384, kTmemCols = 512;
 
-// Byte offset of (row, col) in a [rows][64k] bf16 operand: 64-column slabs of rows x 128 bytes.
-__device__ __forceinline__ uint32_t op_off(int rows, int row, int col)
+// 2n fp32 values (as bits) -> n bf16 pairs
+template <int N> __device__ __forceinline__ void pack_pairs(const uint32_t *r, uint32_t (&p)[N])
 {
-    return static_cast<uint32_t>((col >> 6) * rows * 128) + swz_off<128>(row, col & 63);
+#pragma unroll
+    for (int e = 0; e < N; ++e) p[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
 }
 
 // N (32 or 16) consecutive TMEM columns of this thread's lane
@@ -55,14 +59,6 @@ template <int N> __device__ __forceinline__ void ld_cols(uint32_t t, uint32_t (&
 {
     if constexpr (N == 32) tc::ld32(t, r);
     else tc::ld16(t, r);
-}
-
-__device__ __forceinline__ uint4 pack8(const uint32_t *r)
-{
-    return make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
-                      pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
-                      pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
-                      pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -142,7 +138,6 @@ state_pass_tc_kernel(PassParams p)
 
     constexpr uint32_t kIdN64 = tc::idesc_bf16(128, 64, false);
     constexpr uint32_t kIdN128Mn = tc::idesc_bf16(128, 128, true);
-    const uint32_t sa = smem_u32(smem + kSA);
     uint32_t mma_phase = 0;
     bool gave_up = false;
     auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
@@ -203,9 +198,11 @@ state_pass_tc_kernel(PassParams p)
             uint32_t r[32];
             tc::ld32(tl + kColS + c0, r);
             tc::wait_ld();
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4 *>(smem + kSA + op_off(128, v, c0 + 8 * q)) = pack8(r + 8 * q);
+            {
+                uint32_t a[16];
+                pack_pairs(r, a);
+                tc::st16(tl + kColA + c0 / 2, a);
+            }
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {  // channel pairs through the packed fp32x2 multiply
                 const float4 gv = gam4[(c0 + e) >> 2];
@@ -221,7 +218,6 @@ state_pass_tc_kernel(PassParams p)
             tc::st32(tl + kColS + c0, r);
         }
         tc::wait_st();
-        fence_proxy_async_smem();  // generic-proxy operand writes -> visible to the tensor cores
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -231,10 +227,10 @@ state_pass_tc_kernel(PassParams p)
             const uint32_t w = smem_u32(sb + RT::W), qt = smem_u32(sb + RT::QT);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a = tc::sdesc_sw128(sa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                const uint32_t a = tmem + kColA + 8 * ks;
                 const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
-                tc::mma_bf16(tmem + kColX, a, tc::sdesc_sw128(w + kb, 16, 1024), kIdN64, ks > 0 ? 1u : 0u);
-                tc::mma_bf16(tmem + ycol, a, tc::sdesc_sw128(qt + kb, 16, 1024), kIdN64, ks > 0 ? 1u : 0u);
+                tc::mma_bf16_ts(tmem + kColX, a, tc::sdesc_sw128(w + kb, 16, 1024), kIdN64, ks > 0 ? 1u : 0u);
+                tc::mma_bf16_ts(tmem + ycol, a, tc::sdesc_sw128(qt + kb, 16, 1024), kIdN64, ks > 0 ? 1u : 0u);
             }
             tc::commit(&bars[2]);
         }
@@ -243,26 +239,25 @@ state_pass_tc_kernel(PassParams p)
         mma_phase ^= 1u;
         tc::fence_after_sync();
 
-        // (C) V_new^T row v, this warp's 32 columns = U^T - X^T -> bf16 operand (slab 0 of S^T's)
+        // (C) V_new^T row v, this thread's 16 token columns = U^T - X^T -> bf16 operand in tensor memory
         {
             uint32_t x[kTcYCols];
             ld_cols(tl + kColX + kTcYCols * part, x);
             tc::wait_ld();
             const char *ut = sb + RT::UT;
+            uint32_t w[kTcYCols / 2];
 #pragma unroll
             for (int q = 0; q < kTcYCols / 8; ++q) {
-                const uint32_t off = swz_off<128>(v, kTcYCols * part + 8 * q);
-                const uint4 u = *reinterpret_cast<const uint4 *>(ut + off);
+                const uint4 u = *reinterpret_cast<const uint4 *>(ut + swz_off<128>(v, kTcYCols * part + 8 * q));
                 const uint32_t *xx = x + 8 * q;
-                uint4 w;
-                w.x = pack_bf16x2(bf16_lo(u.x) - __uint_as_float(xx[0]), bf16_hi(u.x) - __uint_as_float(xx[1]));
-                w.y = pack_bf16x2(bf16_lo(u.y) - __uint_as_float(xx[2]), bf16_hi(u.y) - __uint_as_float(xx[3]));
-                w.z = pack_bf16x2(bf16_lo(u.z) - __uint_as_float(xx[4]), bf16_hi(u.z) - __uint_as_float(xx[5]));
-                w.w = pack_bf16x2(bf16_lo(u.w) - __uint_as_float(xx[6]), bf16_hi(u.w) - __uint_as_float(xx[7]));
-                *reinterpret_cast<uint4 *>(smem + kSA + off) = w;
+                w[4 * q] = pack_bf16x2(bf16_lo(u.x) - __uint_as_float(xx[0]), bf16_hi(u.x) - __uint_as_float(xx[1]));
+                w[4 * q + 1] = pack_bf16x2(bf16_lo(u.y) - __uint_as_float(xx[2]), bf16_hi(u.y) - __uint_as_float(xx[3]));
+                w[4 * q + 2] = pack_bf16x2(bf16_lo(u.z) - __uint_as_float(xx[4]), bf16_hi(u.z) - __uint_as_float(xx[5]));
+                w[4 * q + 3] = pack_bf16x2(bf16_lo(u.w) - __uint_as_float(xx[6]), bf16_hi(u.w) - __uint_as_float(xx[7]));
             }
+            tc::st8(tl + kColV + (kTcYCols * part) / 2, w);
+            tc::wait_st();
         }
-        fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -272,9 +267,9 @@ state_pass_tc_kernel(PassParams p)
             const uint32_t aq = smem_u32(sb + RT::AQK), kt = smem_u32(sb + RT::KT);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t a = tc::sdesc_sw128(sa + ks * 32, 16, 1024);
-                tc::mma_bf16(tmem + ycol, a, tc::sdesc_sw128(aq + ks * 32, 16, 1024), kIdN64, 1u);
-                tc::mma_bf16(tmem + kColS, a, tc::sdesc_sw128(kt + ks * 2048, 8192, 1024), kIdN128Mn, 1u);
+                const uint32_t a = tmem + kColV + 8 * ks;
+                tc::mma_bf16_ts(tmem + ycol, a, tc::sdesc_sw128(aq + ks * 32, 16, 1024), kIdN64, 1u);
+                tc::mma_bf16_ts(tmem + kColS, a, tc::sdesc_sw128(kt + ks * 2048, 8192, 1024), kIdN128Mn, 1u);
             }
             tc::commit(&bars[2]);
         }
