@@ -311,7 +311,7 @@ __device__ __forceinline__ void exact_gram(const IO *__restrict__ qg, const IO *
                 const float qh = qv * rn[r], kh = kv * rn[C + r];
                 const float eg = ex2_approx(G);
                 const uint32_t o2 = tile_off<D, C>(r, c);
-                *reinterpret_cast<uint16_t *>(rec + R::QT + o2) = f32_to_bf16_bits(qh * eg * scale);
+                *reinterpret_cast<uint16_t *>(rec + R::qt_at(r, c)) = f32_to_bf16_bits(qh * eg * scale);
                 *reinterpret_cast<uint16_t *>(rec + R::KT + o2) = f32_to_bf16_bits(kh * ex2_approx(Gl - G));
                 kpv[e] = kh * eg;
             }
@@ -674,7 +674,7 @@ __device__ __forceinline__ void prep_chunk(const PrepParams &p, const PrepMaps &
             store_bf16<CPL>(smem + SM::KP, o, kp);  // each lane rewrites exactly the bytes it read
             store_bf16<CPL>(smem + SM::QP, o, qp);
             store_bf16<CPL>(smem + SM::KR, o, kr);
-            store_bf16<CPL>(rec + R::QT, o, qt);
+            store_bf16<CPL>(rec, R::qt_at(i, cb), qt);
             store_bf16<CPL>(rec + R::KT, o, kt);
         }
     }
@@ -996,7 +996,10 @@ __device__ __forceinline__ void prep_chunk(const PrepParams &p, const PrepMaps &
 
     // ---- 6. W and U^T out to the record (Q~, K~, A_qk and gamma are already there) ----
     if (tid == 0) {
-        bulk_s2g(rec + R::W, smem + SM::KP, R::TILE);
+        constexpr int kSlabs = D >= 128 ? D / 64 : 1;  // W's 64-column slabs: rows 0..63 of [W; Q~]
+#pragma unroll
+        for (int s = 0; s < kSlabs; ++s)
+            bulk_s2g(rec + R::w_at(0, 64 * s), smem + SM::KP + s * (R::TILE / kSlabs), R::TILE / kSlabs);
         bulk_s2g(rec + R::UT, smem + SM::QP, D * C * 2);
         bulk_commit();
         bulk_wait_all_read();  // shared memory stays valid until the copies have read it

@@ -28,6 +28,10 @@
 //      state_pass_tc_kernel one CTA per (sequence, head), S in tensor memory
 //                           (state_pass_tc.cu; head size 128, bf16 output,
 //                           enough pairs to fill the GPU), or
+//      state_pass_split_kernel  two CTAs per (sequence, head), 64 value
+//                           columns each, S in tensor memory with the key as
+//                           the lane (state_pass_split.cu; head size 128, bf16
+//                           output, few pairs), or
 //      state_pass_kernel    one CTA per (sequence, head, value slice), S in
 //                           registers (fp32 accumulators), double-buffering
 //                           the records into shared memory with bulk copies;
@@ -281,10 +285,10 @@ state_pass_kernel(PassParams p)
         for (int np = 0; np < 4; ++np) {
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t o = tile_off<D, C>(16 * np + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1));
+                const int r = 16 * np + ri + 8 * (mi >> 1), c = 16 * ks + 8 * (mi & 1);
                 uint32_t bw[4], bq[4];
-                ldmatrix_x4(bw, smem_u32(sb + R::W + o));
-                ldmatrix_x4(bq, smem_u32(sb + R::QT + o));
+                ldmatrix_x4(bw, smem_u32(sb + R::w_at(r, c)));
+                ldmatrix_x4(bq, smem_u32(sb + R::qt_at(r, c)));
                 mma_bf16(x[2 * np], sa[ks], bw[0], bw[1]);
                 mma_bf16(x[2 * np + 1], sa[ks], bw[2], bw[3]);
                 mma_bf16(y[2 * np], sa[ks], bq[0], bq[1]);
@@ -517,13 +521,13 @@ state_pass_pair_kernel(PassParams p)
         // (2) role 0: X^T = S^T W^T; role 1: Y^T = S^T Q~^T   (N = 64 chunk rows)
         float x[8][4] = {};
         {
-            const char *opnd = sb + (role ? R::QT : R::W);
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
+                    const int r = 16 * np + ri + 8 * (mi >> 1), c = 16 * ks + 8 * (mi & 1);
                     uint32_t bw[4];
-                    ldmatrix_x4(bw, smem_u32(opnd + tile_off<D, C>(16 * np + ri + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1))));
+                    ldmatrix_x4(bw, smem_u32(sb + (role ? R::qt_at(r, c) : R::w_at(r, c))));
                     const uint32_t *a = ks < KSH ? slo[ks % KSH] : shi[ks % KSH];
                     mma_bf16(x[2 * np], a, bw[0], bw[1]);
                     mma_bf16(x[2 * np + 1], a, bw[2], bw[3]);
@@ -718,12 +722,12 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
     const int64_t items = a.num_seqs * a.h;
     int warps = D / 16;
     while (warps > 1 && items * (D / (16 * warps)) < 120) warps /= 2;
-    if constexpr (D == 128 && sizeof(IO) == 2) {  // one CTA per (sequence, head): tensor-memory state pass
-        // also when the split register pass (one CTA per SM) would need a second wave
-        if (warps == 8 || items * (D / (16 * warps)) > sm_count()) {
-            if ((e = prefill::launch_state_pass_tc(sp, items, st)) != cudaSuccess) return e;
-            return mark(3);
-        }
+    if constexpr (D == 128 && sizeof(IO) == 2) {  // the tensor-memory state passes
+        // value columns split over CTAs while the split fits one wave, else one CTA per (sequence, head)
+        e = items * prefill::state_pass_split_slices() <= sm_count() ? prefill::launch_state_pass_split(sp, items, st)
+                                                                    : prefill::launch_state_pass_tc(sp, items, st);
+        if (e != cudaSuccess) return e;
+        return mark(3);
     }
     if constexpr (D == 128) {  // at most two 16-column groups per CTA: two warps per group
         if (warps == 8) e = launch_pass<D, IO, 8>(sp, items, st);

@@ -27,17 +27,21 @@ template <int D> __host__ __device__ constexpr int tile_row_bytes() { return D >
 
 // One record per (chunk, head).  bf16 tiles use tile_off (A_qk and U^T: 128-
 // byte rows) so the state pass can bulk-copy a record verbatim into shared
-// memory and use it directly as tensor-core operands.
+// memory and use it directly as tensor-core operands.  W and Q~ are the rows
+// 0..63 and 64..127 of one [128][D] tile, so that a single operand of 128 rows
+// (or N = 128) takes both.
 template <int D> struct Rec {
     static constexpr int TILE = C * D * 2;            // bf16 [64][D]
-    static constexpr int W = 0;                       // W       [64][D]
-    static constexpr int QT = TILE;                   // Q~      [64][D]  (scale q e^G)
+    static constexpr int WQ = 0;                      // [W; Q~] [128][D]  (Q~ = scale q e^G)
     static constexpr int KT = 2 * TILE;               // K~      [64][D]  (k e^{G_last - G})
     static constexpr int AQK = 3 * TILE;              // A_qk    [64][64] (scaled, causal)
     static constexpr int GAMMA = AQK + C * C * 2;     // e^G_last [D] fp32
     static constexpr int UT = GAMMA + D * 4;          // U^T     [D][64]
     static constexpr int BYTES = UT + D * C * 2;
     static_assert(UT % 128 == 0 && BYTES % 128 == 0, "record alignment");
+    // byte offsets of W[r][c] and Q~[r][c]
+    static __device__ __forceinline__ uint32_t w_at(int r, int c) { return WQ + tile_off<D, 2 * C>(r, c); }
+    static __device__ __forceinline__ uint32_t qt_at(int r, int c) { return WQ + tile_off<D, 2 * C>(C + r, c); }
 };
 
 inline int rec_bytes_for(int d)
@@ -146,6 +150,9 @@ __device__ __forceinline__ void store_state2(void *base, int32_t dtype, int64_t 
 // Launches the tensor-memory state pass (D = 128, bf16 output, one CTA per
 // (sequence, head)) over `items` = num_seqs x h CTAs.
 cudaError_t launch_state_pass_tc(const PassParams &p, int64_t items, cudaStream_t st);
+// Value-split form: state_pass_split_slices() CTAs per (sequence, head).
+int state_pass_split_slices();
+cudaError_t launch_state_pass_split(const PassParams &p, int64_t items, cudaStream_t st);
 
 // Tensor map of a bf16 input [T][H][D]: dims (D, H, T), boxes of 64 channels x 1 head
 // x 64 tokens, 128-byte swizzle, zeros outside the tensor (chunk_prep.cu).

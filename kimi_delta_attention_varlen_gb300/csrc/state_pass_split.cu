@@ -1,0 +1,326 @@
+// Inter-chunk state pass on the tensor cores for few (sequence, head) pairs:
+// head size 128, bf16 output, the value columns of each state split over two
+// CTAs (64 columns each), so a batch of one long sequence still spreads over
+// twice as many SMs as it has heads.  Columns of S evolve independently: the
+// recurrence S_t = (I - beta k k^T) Diag(e^g) S + beta k v^T of the "KDA's
+// challenges for AI infra" page (section 1.1) multiplies S from the left only,
+// and its chunkwise form in the "Support Kimi-K3 on NPU" report's extend
+// listing keeps that property:
+//   [X; Y] = [W; Q~] S                      (M = 128: 64 rows of each, N = 64 columns, K = 128 keys)
+//   V_new = U - X                           (threads, one token row each)
+//   S <- diag(gamma) S + K~^T V_new,  O = Y + A_qk V_new    (K = 64 tokens)
+//
+// Layout.  S (fp32, 128 key lanes x 64 columns) lives in tensor memory with the
+// key as the lane, so the decay diag(gamma) is one scalar per thread; two [X; Y]
+// buffers (X in lanes 0..63, Y / O in lanes 64..127) sit beside it.  The B
+// operands of every MMA (S and V_new in bf16) are written by the threads into
+// shared memory as 64-column MN-major tiles in the 128-byte-swizzle layout; the
+// A operands come straight from the bulk-copied record: [W; Q~] and A_qk
+// K-major, K~ MN-major (as K~^T).  The O product takes M = 128 rows of which
+// A_qk is the second half, so that it lands on Y's lanes: its first 64 rows are
+// the 8 KB of the record before A_qk, and they add into X's lanes after X has
+// been read.
+//
+// Threads: eight compute warps (warp w serves TMEM lanes 32 (w % 4) ... and
+// columns 32 (w / 4) ... of the slice) and one copy warp that refills a record
+// stage once every MMA reading it has completed.  One thread issues the MMAs;
+// mbarriers signal [X; Y] (to the V_new step), S (to the next chunk) and O (to
+// the output rows and the copy warp).  The warps of lanes 0..63 form V_new while
+// those of lanes 64..127 move the previous chunk's output rows out of tensor
+// memory.  Every wait is bounded; an expired wait
+// sets the workspace status word and the CTA stops waiting, waits (bounded) for
+// its own copies in flight, and still frees its TMEM.
+#include "prefill_common.cuh"
+#include "tcgen05.cuh"
+
+namespace kda {
+namespace prefill {
+namespace {
+
+constexpr int kSpD = 128;
+constexpr int kSpNV = 64;                          // value columns per CTA
+constexpr int kSpSlices = kSpD / kSpNV;
+constexpr int kSpCompute = 256;                    // eight compute warps
+constexpr int kSpThreads = kSpCompute + 32;        // + the copy warp
+constexpr uint32_t kSpWaitLimit = 1u << 22;
+using RS = Rec<kSpD>;
+constexpr int kSpStage = (RS::BYTES + 1023) / 1024 * 1024;
+constexpr int kSpSop = 2 * kSpStage;               // S bf16 [128 keys][64 columns], MN-major
+constexpr int kSpVop = kSpSop + kSpD * 128;        // V_new bf16 [64 tokens][64 columns], MN-major
+constexpr int kSpSmem = kSpVop + C * 128 + 1024;   // + slack to align the base to 1 KiB
+// Tensor memory: S (64 columns), two [X; Y] buffers (64 columns each)
+constexpr uint32_t kSpColS = 0, kSpColXY = 64, kSpTmemCols = 256;
+// The O product's A operand starts 64 rows (8 KB) before A_qk, inside the record.
+static_assert(RS::AQK >= C * 128, "A_qk as rows 64..127");
+
+__host__ __device__ constexpr uint32_t sp_idesc(bool a_mn, bool b_mn)  // M = 128, N = 64, bf16 -> fp32
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(kSpNV >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void compute_sync()  // the 256 compute threads (named barrier 1)
+{
+    asm volatile("bar.sync 1, %0;\n" ::"n"(kSpCompute) : "memory");
+}
+
+__device__ __forceinline__ float load_state1(const void *base, int32_t dtype, int64_t e)
+{
+    if (dtype == KDA_F32) return static_cast<const float *>(base)[e];
+    return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(base)[e]) << 16);
+}
+
+__device__ __forceinline__ void store_state1(void *base, int32_t dtype, int64_t e, float x)
+{
+    if (dtype == KDA_F32) static_cast<float *>(base)[e] = x;
+    else static_cast<__nv_bfloat16 *>(base)[e] = __float2bfloat16_rn(x);
+}
+
+__global__ void __launch_bounds__(kSpThreads, 1)
+state_pass_split_kernel(PassParams p)
+{
+    extern __shared__ char smem_raw[];
+    char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    // two record stages; [X; Y] done, S done, O done per stage
+    __shared__ __align__(8) uint64_t bars[6];
+    __shared__ uint32_t tmem_base;
+    uint64_t *const bar_x = &bars[2], *const bar_s = &bars[3], *const bar_o = &bars[4];
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int quad = warp & 3, part = (warp >> 2) & 1;
+    const int lane = 32 * quad + (tid & 31);        // key (S), token (X) or 64 + token (Y) of this thread
+    const int64_t H = p.H;
+    const int64_t item = blockIdx.x / kSpSlices;
+    const int v0 = kSpNV * static_cast<int>(blockIdx.x % kSpSlices) + 32 * part;  // this thread's 32 columns
+    const int h = static_cast<int>(item % H);
+    const int64_t b = p.seq_order[item / H];
+    const int32_t c_begin = p.chunk_off[b], n_chunks = p.chunk_off[b + 1] - c_begin;
+    const int64_t tok_begin = p.cu[b], tok_end = p.cu[b + 1];
+
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, kSpTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int j = 0; j < 6; ++j) mbar_init(&bars[j], 1);
+        fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base;
+
+    auto issue = [&](int32_t i) {  // record of chunk i -> stage i & 1
+        const char *rec = p.records + (static_cast<int64_t>(c_begin + i) * H + h) * RS::BYTES;
+        mbar_arrive_expect_tx(&bars[i & 1], RS::BYTES);
+        bulk_g2s(smem + (i & 1) * kSpStage, rec, RS::BYTES, &bars[i & 1]);
+    };
+
+    if (warp == kSpCompute / 32) {  // ---- the copy warp ----
+        if ((tid & 31) == 0) {
+            bool fail = false;
+            int32_t last = -1;
+            for (int32_t i = 0; i < n_chunks && i < 2; ++i) issue(last = i);
+            // stage i & 1 is free once chunk i's last MMAs (O) have completed
+            for (int32_t i = 0; i + 2 < n_chunks && !fail; ++i) {
+                if (!mbar_wait(&bar_o[i & 1], (i >> 1) & 1, kSpWaitLimit)) {
+                    fail = true;
+                    atomicExch(p.status, 2);
+                    break;
+                }
+                issue(last = i + 2);
+            }
+            // every copy this CTA issued has landed before it exits
+            for (int32_t i = last; i >= 0 && i > last - 2; --i)
+                if (!mbar_wait(&bars[i & 1], (i >> 1) & 1, kSpWaitLimit)) atomicExch(p.status, 2);
+        }
+        __syncwarp();
+        __syncthreads();
+        return;  // the compute warps free the TMEM
+    }
+
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);  // this warp's lanes
+    // element offset of state row [h][v][k] for this thread's key k = lane and column v
+    auto srow = [&](int v) { return (static_cast<int64_t>(h) * kSpD + v) * kSpD + lane; };
+
+    // initial state: S[k][v0 ... v0 + 31] for key k = lane
+    {
+        const int64_t base = init_base(p.se, b, H * kSpD * kSpD);
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            r[j] = __float_as_uint(base >= 0 ? load_state1(p.se.init, p.se.init_dtype, base + srow(v0 + j)) : 0.f);
+        tc::st32(tl + kSpColS + 32 * part, r);
+        tc::wait_st();
+    }
+    auto put_state = [&](void *dst, int32_t dtype, int64_t base, const uint32_t r[32]) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) store_state1(dst, dtype, base + srow(v0 + j), __uint_as_float(r[j]));
+    };
+
+    constexpr uint32_t kIdKB = sp_idesc(false, true);   // A K-major (W, Q~, A_qk), B MN-major
+    constexpr uint32_t kIdMB = sp_idesc(true, true);    // A MN-major (K~^T), B MN-major
+    uint32_t phase_x = 0, phase_s = 0;
+    bool gave_up = false;
+    auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
+        if (!gave_up && !mbar_wait(bar, parity, kSpWaitLimit)) {
+            gave_up = true;
+            if ((tid & 31) == 0) atomicExch(p.status, 2);
+        }
+    };
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+    char *const sop = smem + kSpSop, *const vop = smem + kSpVop;
+    const uint32_t sop_a = smem_u32(sop), vop_a = smem_u32(vop);
+
+    // O rows of chunk c (buffer c & 1, lanes 64..127) -> out[t][h][v0 ... v0 + 31]; warps of quadrants 2, 3
+    auto store_outputs = [&](int32_t c) {
+        wait_bar(&bar_o[c & 1], (c >> 1) & 1);
+        tc::fence_after_sync();
+        uint32_t y[32];
+        tc::ld32(tl + kSpColXY + 64 * (c & 1) + 32 * part, y);
+        tc::wait_ld();
+        const int64_t t = tok_begin + static_cast<int64_t>(c) * C + (lane - C);
+        if (t < tok_end) {
+            uint4 *dst = reinterpret_cast<uint4 *>(out + (t * H + h) * kSpD + v0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16x2(__uint_as_float(y[8 * q]), __uint_as_float(y[8 * q + 1])),
+                                    pack_bf16x2(__uint_as_float(y[8 * q + 2]), __uint_as_float(y[8 * q + 3])),
+                                    pack_bf16x2(__uint_as_float(y[8 * q + 4]), __uint_as_float(y[8 * q + 5])),
+                                    pack_bf16x2(__uint_as_float(y[8 * q + 6]), __uint_as_float(y[8 * q + 7])));
+        }
+    };
+
+    for (int32_t i = 0; i < n_chunks; ++i) {
+        const int st = i & 1;
+        wait_bar(&bars[st], (i >> 1) & 1);
+        const char *sb = smem + st * kSpStage;
+        const uint32_t xy = kSpColXY + 64 * static_cast<uint32_t>(st);
+
+        // S is the state after chunk i - 1: a checkpoint when that chunk ends on one.
+        if (p.se.ckpt != nullptr && i > 0) {
+            const int64_t ck = ckpt_slot(p.se, b, i - 1, tok_end - tok_begin);
+            if (ck >= 0) {
+                uint32_t r[32];
+                tc::ld32(tl + kSpColS + 32 * part, r);
+                tc::wait_ld();
+                put_state(p.se.ckpt, p.se.ckpt_dtype, ck * H * kSpD * kSpD, r);
+            }
+        }
+        // (A) S row k (this thread's 32 columns) -> bf16 operand (undecayed); decay the TMEM copy by gamma_k
+        {
+            uint32_t r[32];
+            tc::ld32(tl + kSpColS + 32 * part, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(sop + swz_off<128>(lane, 32 * part + 8 * q)) =
+                    make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
+                               pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                               pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                               pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+            const float gk = reinterpret_cast<const float *>(sb + RS::GAMMA)[lane];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gk);
+            tc::st32(tl + kSpColS + 32 * part, r);
+        }
+        tc::wait_st();
+        fence_proxy_async_smem();  // generic-proxy operand writes -> visible to the tensor cores
+        tc::fence_before_sync();
+        compute_sync();
+        tc::fence_after_sync();
+
+        // (B) [X; Y] = [W; Q~] S, K = 128 keys
+        if (tid == 0) {
+            const uint32_t wq = smem_u32(sb + RS::WQ);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem + xy, tc::sdesc_sw128(wq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                             tc::sdesc_sw128(sop_a + ks * 2048, 8192, 1024), kIdKB, ks > 0 ? 1u : 0u);
+            tc::commit(bar_x);
+        }
+        __syncwarp();
+        if (i > 0 && quad >= 2) store_outputs(i - 1);  // the previous chunk's outputs, while these MMAs run
+        wait_bar(bar_x, phase_x);
+        phase_x ^= 1u;
+        tc::fence_after_sync();
+
+        // (C) V_new row t (token lanes 0..63), this thread's 32 columns = U - X -> bf16 operand
+        if (quad < 2) {
+            uint32_t x[32];
+            tc::ld32(tl + xy + 32 * part, x);
+            tc::wait_ld();
+            const char *ut = sb + RS::UT;
+            float u[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                u[j] = __uint_as_float(static_cast<uint32_t>(
+                           *reinterpret_cast<const uint16_t *>(ut + swz_off<128>(v0 + j, lane))) << 16) -
+                       __uint_as_float(x[j]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(vop + swz_off<128>(lane, 32 * part + 8 * q)) =
+                    make_uint4(pack_bf16x2(u[8 * q], u[8 * q + 1]), pack_bf16x2(u[8 * q + 2], u[8 * q + 3]),
+                               pack_bf16x2(u[8 * q + 4], u[8 * q + 5]), pack_bf16x2(u[8 * q + 6], u[8 * q + 7]));
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        compute_sync();
+        tc::fence_after_sync();
+
+        // (D) S += K~^T V_new (committed alone: the next chunk waits for it), then O = Y + A_qk V_new
+        // (A from 8 KB before A_qk: A_qk is rows 64..127, on Y's lanes); K = 64
+        if (tid == 0) {
+            const uint32_t aq = smem_u32(sb + RS::AQK), kt = smem_u32(sb + RS::KT);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + kSpColS, tc::sdesc_sw128(kt + ks * 2048, 8192, 1024),
+                             tc::sdesc_sw128(vop_a + ks * 2048, 8192, 1024), kIdMB, 1u);
+            tc::commit(bar_s);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + xy, tc::sdesc_sw128(aq - C * 128 + ks * 32, 16, 1024),
+                             tc::sdesc_sw128(vop_a + ks * 2048, 8192, 1024), kIdKB, 1u);
+            tc::commit(&bar_o[st]);
+        }
+        __syncwarp();
+        wait_bar(bar_s, phase_s);
+        phase_s ^= 1u;
+        tc::fence_after_sync();
+    }
+    if (n_chunks > 0 && quad >= 2) store_outputs(n_chunks - 1);
+
+    // final state -> packed fp32, the cache row out_idx[b], and the last checkpoint if it ends there
+    {
+        const int64_t per_seq = H * kSpD * kSpD;
+        const int64_t ob = out_base(p.se, b);
+        const int64_t ck = n_chunks > 0 ? ckpt_slot(p.se, b, n_chunks - 1, tok_end - tok_begin) : -1;
+        if (p.se.final_state != nullptr || ob >= 0 || ck >= 0) {
+            uint32_t r[32];
+            tc::ld32(tl + kSpColS + 32 * part, r);
+            tc::wait_ld();
+            if (p.se.final_state != nullptr) put_state(p.se.final_state, KDA_F32, b * per_seq, r);
+            if (ob >= 0) put_state(p.se.out_cache, p.se.out_dtype, ob, r);
+            if (ck >= 0) put_state(p.se.ckpt, p.se.ckpt_dtype, ck * per_seq, r);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kSpTmemCols);
+}
+
+}  // namespace
+
+int state_pass_split_slices() { return kSpSlices; }
+
+cudaError_t launch_state_pass_split(const PassParams &p, int64_t items, cudaStream_t st)
+{
+    cudaError_t e =
+        cudaFuncSetAttribute(state_pass_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
+    if (e != cudaSuccess) return e;
+    state_pass_split_kernel<<<static_cast<unsigned>(items * kSpSlices), kSpThreads, kSpSmem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace prefill
+}  // namespace kda

@@ -33,8 +33,9 @@ namespace kda {
 namespace prefill {
 namespace {
 
-constexpr int kTcThreads = 512;
-constexpr int kTcParts = kTcThreads / 128;   // warps sharing one 32-lane TMEM quadrant
+constexpr int kTcCompute = 512;                // sixteen compute warps
+constexpr int kTcThreads = kTcCompute + 32;    // + the copy warp
+constexpr int kTcParts = kTcCompute / 128;   // warps sharing one 32-lane TMEM quadrant
 constexpr int kTcSCols = 128 / kTcParts;     // S^T columns per thread
 constexpr int kTcYCols = 64 / kTcParts;      // X^T / Y^T columns per thread
 constexpr uint32_t kTcWaitLimit = 1u << 22;
@@ -43,9 +44,15 @@ using RT = Rec<kTcD>;
 constexpr int kStage = (RT::BYTES + 1023) / 1024 * 1024;  // one record, padded to 1 KiB
 constexpr int kOS = 2 * kStage;          // output staging bf16 [64 tokens][128 values]
 constexpr int kTcSmem = kOS + 16384 + 1024;  // + slack to align the base to 1 KiB
-// Tensor memory: S^T fp32 (128 columns), X^T (64), two Y^T / O^T buffers (64 each), and the MMAs'
-// A operands in bf16, two values per 32-bit column: S^T (64 columns) and V_new^T (32).
-constexpr uint32_t kColS = 0, kColX = 128, kColY = 192, kColA = 320, kColV = 384, kTmemCols = 512;
+// Tensor memory: S^T fp32 (128 columns), two [X^T | Y^T] buffers (128 columns each: X^T, then
+// Y^T / O^T), and the MMAs' A operands in bf16, two values per 32-bit column: S^T (64 columns)
+// and V_new^T (32).
+constexpr uint32_t kColS = 0, kColXY = 128, kColA = 384, kColV = 448, kTmemCols = 512;
+
+__device__ __forceinline__ void compute_sync()  // the compute warps (named barrier 1)
+{
+    asm volatile("bar.sync 1, %0;\n" ::"n"(kTcCompute) : "memory");
+}
 
 // 2n fp32 values (as bits) -> n bf16 pairs
 template <int N> __device__ __forceinline__ void pack_pairs(const uint32_t *r, uint32_t (&p)[N])
@@ -66,11 +73,13 @@ state_pass_tc_kernel(PassParams p)
 {
     extern __shared__ char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t bars[3];  // two record stages, MMA completion
+    // two record stages; X|Y done, S done, O done per stage
+    __shared__ __align__(8) uint64_t bars[6];
     __shared__ uint32_t tmem_base;
+    uint64_t *const bar_xy = &bars[2], *const bar_s = &bars[3], *const bar_o = &bars[4];
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int quad = warp & 3, part = warp >> 2;   // TMEM lane quadrant; which part of the columns
+    const int quad = warp & 3, part = (warp >> 2) & 3;  // TMEM lane quadrant; which part of the columns
     const int v = 32 * quad + (tid & 31);          // value row = TMEM lane
     const int64_t H = p.H;
     const int64_t item = blockIdx.x;
@@ -84,15 +93,39 @@ state_pass_tc_kernel(PassParams p)
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        for (int j = 0; j < 6; ++j) mbar_init(&bars[j], 1);
         fence_mbar_init();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base;
+
+    auto issue = [&](int32_t i) {  // record of chunk i -> stage i & 1
+        const char *rec = p.records + (static_cast<int64_t>(c_begin + i) * H + h) * RT::BYTES;
+        mbar_arrive_expect_tx(&bars[i & 1], RT::BYTES);
+        bulk_g2s(smem + (i & 1) * kStage, rec, RT::BYTES, &bars[i & 1]);
+    };
+    if (warp == kTcCompute / 32) {  // ---- the copy warp ----
+        if ((tid & 31) == 0) {
+            int32_t last = -1;
+            for (int32_t i = 0; i < n_chunks && i < 2; ++i) issue(last = i);
+            // stage i & 1 is free once chunk i's last MMAs (O) have completed
+            for (int32_t i = 0; i + 2 < n_chunks; ++i) {
+                if (!mbar_wait(&bar_o[i & 1], (i >> 1) & 1, kTcWaitLimit)) {
+                    atomicExch(p.status, 2);
+                    break;
+                }
+                issue(last = i + 2);
+            }
+            // every copy this CTA issued has landed before it exits
+            for (int32_t i = last; i >= 0 && i > last - 2; --i)
+                if (!mbar_wait(&bars[i & 1], (i >> 1) & 1, kTcWaitLimit)) atomicExch(p.status, 2);
+        }
+        __syncwarp();
+        __syncthreads();
+        return;  // the compute warps free the TMEM
+    }
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);  // this warp's lanes
 
     const int64_t row_v = (static_cast<int64_t>(h) * kTcD + v) * kTcD;  // element offset of [v][0] within a state
@@ -126,19 +159,10 @@ state_pass_tc_kernel(PassParams p)
         tc::wait_st();
     }
 
-    auto issue = [&](int32_t i, int st) {  // record of chunk i -> stage st (thread 0)
-        const char *rec = p.records + (static_cast<int64_t>(c_begin + i) * H + h) * RT::BYTES;
-        mbar_arrive_expect_tx(&bars[st], RT::BYTES);
-        bulk_g2s(smem + st * kStage, rec, RT::BYTES, &bars[st]);
-    };
-    if (tid == 0) {
-        if (n_chunks > 0) issue(0, 0);
-        if (n_chunks > 1) issue(1, 1);
-    }
-
     constexpr uint32_t kIdN64 = tc::idesc_bf16(128, 64, false);
+    constexpr uint32_t kIdN128 = tc::idesc_bf16(128, 128, false);
     constexpr uint32_t kIdN128Mn = tc::idesc_bf16(128, 128, true);
-    uint32_t mma_phase = 0;
+    uint32_t phase_xy = 0, phase_s = 0;
     bool gave_up = false;
     auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
         if (!gave_up && !mbar_wait(bar, parity, kTcWaitLimit)) {
@@ -148,12 +172,15 @@ state_pass_tc_kernel(PassParams p)
     };
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 
-    // Outputs of chunk c (O^T in Y buffer c & 1): TMEM -> staging [t][v] (stage_outputs), then,
-    // after a CTA barrier, whole output rows from the staging to global memory (store_outputs).
+    // Outputs of chunk c (O^T in the Y half of buffer c & 1): TMEM -> staging [t][v] once the O
+    // MMAs have completed (stage_outputs), then, after a barrier of the compute warps, whole
+    // output rows from the staging to global memory (store_outputs).
     __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(smem + kOS);
     auto stage_outputs = [&](int32_t c) {
+        wait_bar(&bar_o[c & 1], (c >> 1) & 1);
+        tc::fence_after_sync();
         uint32_t y[kTcYCols];
-        ld_cols(tl + kColY + 64 * (c & 1) + kTcYCols * part, y);
+        ld_cols(tl + kColXY + 128 * (c & 1) + 64 + kTcYCols * part, y);
         tc::wait_ld();
 #pragma unroll
         for (int e = 0; e < kTcYCols; ++e)
@@ -164,7 +191,7 @@ state_pass_tc_kernel(PassParams p)
         const int len = static_cast<int>(tok_end - t0 < C ? tok_end - t0 : C);
         const uint4 *src = reinterpret_cast<const uint4 *>(os);
 #pragma unroll
-        for (int e = tid; e < C * (kTcD * 2 / 16); e += kTcThreads) {
+        for (int e = tid; e < C * (kTcD * 2 / 16); e += kTcCompute) {
             const int t = e >> 4, part = e & 15;
             if (t < len) reinterpret_cast<uint4 *>(out + ((t0 + t) * H + h) * kTcD)[part] = src[e];
         }
@@ -175,7 +202,7 @@ state_pass_tc_kernel(PassParams p)
         wait_bar(&bars[st], (i >> 1) & 1);
         const char *sb = smem + st * kStage;
         const float4 *gam4 = reinterpret_cast<const float4 *>(sb + RT::GAMMA);
-        const uint32_t ycol = kColY + 64 * static_cast<uint32_t>(i & 1);
+        const uint32_t xy = kColXY + 128 * static_cast<uint32_t>(st);
 
         // S is now the state after chunk i - 1: a checkpoint when that chunk ends on one.
         if (p.se.ckpt != nullptr && i > 0) {
@@ -219,30 +246,29 @@ state_pass_tc_kernel(PassParams p)
         }
         tc::wait_st();
         tc::fence_before_sync();
-        __syncthreads();
+        compute_sync();
         tc::fence_after_sync();
 
-        // (B) X^T = S^T W^T and Y^T = S^T Q~^T: M = 128, N = 64, K = 128 in 8 steps of 16
+        // (B) [X^T | Y^T] = S^T [W; Q~]^T: M = 128, N = 128 (W rows, then Q~ rows), K = 128 in 8 steps
         if (tid == 0) {
-            const uint32_t w = smem_u32(sb + RT::W), qt = smem_u32(sb + RT::QT);
+            const uint32_t wq = smem_u32(sb + RT::WQ);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t a = tmem + kColA + 8 * ks;
-                const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
-                tc::mma_bf16_ts(tmem + kColX, a, tc::sdesc_sw128(w + kb, 16, 1024), kIdN64, ks > 0 ? 1u : 0u);
-                tc::mma_bf16_ts(tmem + ycol, a, tc::sdesc_sw128(qt + kb, 16, 1024), kIdN64, ks > 0 ? 1u : 0u);
-            }
-            tc::commit(&bars[2]);
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16_ts(tmem + xy, tmem + kColA + 8 * ks,
+                                tc::sdesc_sw128(wq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), kIdN128,
+                                ks > 0 ? 1u : 0u);
+            tc::commit(bar_xy);
         }
+        __syncwarp();
         if (i > 0) stage_outputs(i - 1);  // the previous chunk's outputs into the staging, while these MMAs run
-        wait_bar(&bars[2], mma_phase);
-        mma_phase ^= 1u;
+        wait_bar(bar_xy, phase_xy);
+        phase_xy ^= 1u;
         tc::fence_after_sync();
 
         // (C) V_new^T row v, this thread's 16 token columns = U^T - X^T -> bf16 operand in tensor memory
         {
             uint32_t x[kTcYCols];
-            ld_cols(tl + kColX + kTcYCols * part, x);
+            ld_cols(tl + xy + kTcYCols * part, x);
             tc::wait_ld();
             const char *ut = sb + RT::UT;
             uint32_t w[kTcYCols / 2];
@@ -259,31 +285,35 @@ state_pass_tc_kernel(PassParams p)
             tc::wait_st();
         }
         tc::fence_before_sync();
-        __syncthreads();
+        compute_sync();
         tc::fence_after_sync();
 
-        // (D) Y^T += V_new^T A_qk^T (N = 64) and S^T += V_new^T K~ (N = 128, K~ MN-major), K = 64
+        // (D) S^T += V_new^T K~ (N = 128, K~ MN-major; committed alone: the next chunk waits for it),
+        // then O^T = Y^T + V_new^T A_qk^T (N = 64); K = 64.  The copy warp refills this stage once
+        // the O MMAs have completed (gamma in A and U^T in C were read before the barrier above).
         if (tid == 0) {
             const uint32_t aq = smem_u32(sb + RT::AQK), kt = smem_u32(sb + RT::KT);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t a = tmem + kColV + 8 * ks;
-                tc::mma_bf16_ts(tmem + ycol, a, tc::sdesc_sw128(aq + ks * 32, 16, 1024), kIdN64, 1u);
-                tc::mma_bf16_ts(tmem + kColS, a, tc::sdesc_sw128(kt + ks * 2048, 8192, 1024), kIdN128Mn, 1u);
-            }
-            tc::commit(&bars[2]);
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16_ts(tmem + kColS, tmem + kColV + 8 * ks, tc::sdesc_sw128(kt + ks * 2048, 8192, 1024),
+                                kIdN128Mn, 1u);
+            tc::commit(bar_s);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16_ts(tmem + xy + 64, tmem + kColV + 8 * ks, tc::sdesc_sw128(aq + ks * 32, 16, 1024),
+                                kIdN64, 1u);
+            tc::commit(&bar_o[st]);
         }
+        __syncwarp();
         if (i > 0) store_outputs(i - 1);  // staged before the barrier above; stored while these MMAs run
-        wait_bar(&bars[2], mma_phase);
-        mma_phase ^= 1u;
+        wait_bar(bar_s, phase_s);
+        phase_s ^= 1u;
         tc::fence_after_sync();
-        // Every read of this stage is over (gamma in A and U^T in C precede the barriers above,
-        // the MMAs have completed): refill it with chunk i + 2.
-        if (tid == 0 && i + 2 < n_chunks) issue(i + 2, st);
     }
     if (n_chunks > 0) {
+        compute_sync();  // the staging's last rows (chunk n - 2) have been stored
         stage_outputs(n_chunks - 1);
-        __syncthreads();
+        compute_sync();
         store_outputs(n_chunks - 1);
     }
 
