@@ -194,6 +194,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return false;
 }
 
+// Whether the barrier's phase `parity` has completed, without waiting.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // 3-D tiled tensor copy global -> shared (the box and swizzle encoded in the map),
 // completion signalled on `bar` as transaction bytes.  Coordinates are elements
 // (x fastest); x times the element size must be a multiple of 16 bytes.  `map`

@@ -19,8 +19,9 @@
 // the B operands from shared memory: W, Q~, A_qk (K-major) and K~ (MN-major),
 // straight from the bulk-copied record in the 128-byte-swizzle layout.  One
 // thread issues the MMAs;
-// an mbarrier signals their completion.  Records are double-buffered (the
-// copy of chunk i + 2 starts when chunk i is done).  The outputs of chunk
+// mbarriers signal their completion.  Records are double-buffered: the copy of
+// chunk i + 1 starts in chunk i once chunk i - 1's MMAs are done, and each copy
+// prefetches the record kTcAhead chunks further on into L2.  The outputs of chunk
 // i - 1 move from tensor memory to a staging tile while the first MMA group of
 // chunk i runs and from there to global memory while the second group runs, so
 // neither half waits on a barrier of its own.  Every wait is bounded; an
@@ -33,12 +34,13 @@ namespace kda {
 namespace prefill {
 namespace {
 
-constexpr int kTcCompute = 512;                // sixteen compute warps
-constexpr int kTcThreads = kTcCompute + 32;    // + the copy warp
+constexpr int kTcCompute = 512;                // sixteen warps
+constexpr int kTcThreads = kTcCompute;
 constexpr int kTcParts = kTcCompute / 128;   // warps sharing one 32-lane TMEM quadrant
 constexpr int kTcSCols = 128 / kTcParts;     // S^T columns per thread
 constexpr int kTcYCols = 64 / kTcParts;      // X^T / Y^T columns per thread
 constexpr uint32_t kTcWaitLimit = 1u << 22;
+constexpr int kTcAhead = 2;                     // records prefetched into L2 beyond the two stages
 constexpr int kTcD = 128;
 using RT = Rec<kTcD>;
 constexpr int kStage = (RT::BYTES + 1023) / 1024 * 1024;  // one record, padded to 1 KiB
@@ -101,30 +103,19 @@ state_pass_tc_kernel(PassParams p)
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base;
 
-    auto issue = [&](int32_t i) {  // record of chunk i -> stage i & 1
-        const char *rec = p.records + (static_cast<int64_t>(c_begin + i) * H + h) * RT::BYTES;
-        mbar_arrive_expect_tx(&bars[i & 1], RT::BYTES);
-        bulk_g2s(smem + (i & 1) * kStage, rec, RT::BYTES, &bars[i & 1]);
-    };
-    if (warp == kTcCompute / 32) {  // ---- the copy warp ----
-        if ((tid & 31) == 0) {
-            int32_t last = -1;
-            for (int32_t i = 0; i < n_chunks && i < 2; ++i) issue(last = i);
-            // stage i & 1 is free once chunk i's last MMAs (O) have completed
-            for (int32_t i = 0; i + 2 < n_chunks; ++i) {
-                if (!mbar_wait(&bar_o[i & 1], (i >> 1) & 1, kTcWaitLimit)) {
-                    atomicExch(p.status, 2);
-                    break;
-                }
-                issue(last = i + 2);
-            }
-            // every copy this CTA issued has landed before it exits
-            for (int32_t i = last; i >= 0 && i > last - 2; --i)
-                if (!mbar_wait(&bars[i & 1], (i >> 1) & 1, kTcWaitLimit)) atomicExch(p.status, 2);
+    // record of chunk i -> stage i & 1 (thread 0); records kTcAhead chunks further on -> L2
+    auto issue = [&](int32_t i) {
+        if (i < n_chunks) {
+            const char *rec = p.records + (static_cast<int64_t>(c_begin + i) * H + h) * RT::BYTES;
+            mbar_arrive_expect_tx(&bars[i & 1], RT::BYTES);
+            bulk_g2s(smem + (i & 1) * kStage, rec, RT::BYTES, &bars[i & 1]);
         }
-        __syncwarp();
-        __syncthreads();
-        return;  // the compute warps free the TMEM
+        if (i + kTcAhead < n_chunks)
+            prefetch_l2(p.records + (static_cast<int64_t>(c_begin + i + kTcAhead) * H + h) * RT::BYTES, RT::BYTES);
+    };
+    if (tid == 0) {
+        issue(0);
+        issue(1);
     }
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);  // this warp's lanes
 
@@ -260,7 +251,11 @@ state_pass_tc_kernel(PassParams p)
             tc::commit(bar_xy);
         }
         __syncwarp();
-        if (i > 0) stage_outputs(i - 1);  // the previous chunk's outputs into the staging, while these MMAs run
+        if (i > 0) {
+            stage_outputs(i - 1);  // the previous chunk's outputs into the staging, while these MMAs run
+            // every read of chunk i - 1's stage is over (its O products have completed): chunk i + 1
+            if (tid == 0) issue(i + 1);
+        }
         wait_bar(bar_xy, phase_xy);
         phase_xy ^= 1u;
         tc::fence_after_sync();
@@ -289,8 +284,8 @@ state_pass_tc_kernel(PassParams p)
         tc::fence_after_sync();
 
         // (D) S^T += V_new^T K~ (N = 128, K~ MN-major; committed alone: the next chunk waits for it),
-        // then O^T = Y^T + V_new^T A_qk^T (N = 64); K = 64.  The copy warp refills this stage once
-        // the O MMAs have completed (gamma in A and U^T in C were read before the barrier above).
+        // then O^T = Y^T + V_new^T A_qk^T (N = 64); K = 64.  This stage is refilled in the next chunk
+        // once the O MMAs have completed (gamma in A and U^T in C were read before the barrier above).
         if (tid == 0) {
             const uint32_t aq = smem_u32(sb + RT::AQK), kt = smem_u32(sb + RT::KT);
 #pragma unroll
@@ -310,6 +305,8 @@ state_pass_tc_kernel(PassParams p)
         phase_s ^= 1u;
         tc::fence_after_sync();
     }
+    if (gave_up && tid == 0)  // copies still in flight land before the CTA exits
+        for (int32_t i = n_chunks > 2 ? n_chunks - 2 : 0; i < n_chunks; ++i) mbar_wait(&bars[i & 1], (i >> 1) & 1, kTcWaitLimit);
     if (n_chunks > 0) {
         compute_sync();  // the staging's last rows (chunk n - 2) have been stored
         stage_outputs(n_chunks - 1);

@@ -208,16 +208,19 @@ def test_full_long_sequence_sampled():
     torch.cuda.empty_cache()
 
 
-# 16 (sequence, head) pairs fit one wave of the split register pass; 96 would need a
-# second wave, so the tensor-memory pass runs instead.
-@pytest.mark.parametrize("lengths,H", [([327, 100, 1, 0], 4), ([200, 65, 131], 32)])
-def test_prefill_state_pass_dispatch(lengths, H):
-    """Both sides of the state-pass choice at head size 128, bf16, against the oracle."""
+# bf16 at head size 128: 16 or 64 (sequence, head) pairs take the value-split tensor-memory
+# pass (two CTAs per pair, one wave), 96 pairs one CTA per pair; fp32 inputs take the
+# register passes (warp pairs for 16 pairs, one warp per value group for 64).
+@pytest.mark.parametrize("lengths,H,io", [([327, 100, 1, 0], 4, torch.bfloat16), ([150, 71], 32, torch.bfloat16),
+                                          ([200, 65, 131], 32, torch.bfloat16), ([327, 100, 1, 0], 4, torch.float32),
+                                          ([150, 71], 32, torch.float32)])
+def test_prefill_state_pass_dispatch(lengths, H, io):
+    """Every state-pass form at head size 128 against the oracle."""
     D = 128
     cu = [0]
     for n in lengths:
         cu.append(cu[-1] + n)
-    inp = wl.token_inputs(cu[-1], H, D, D, torch.bfloat16, seed=len(lengths) + H, device=DEV, decay_scale=0.1)
+    inp = wl.token_inputs(cu[-1], H, D, D, io, seed=len(lengths) + H, device=DEV, decay_scale=0.1)
     init = torch.randn(len(lengths), H, D, D, generator=wl.generator(9, DEV), device=DEV) * 0.5
     scale = D ** -0.5
     out, fin = run_prefill(inp, cu, H, D, init=init, scale=scale)
@@ -270,13 +273,16 @@ def test_gates_across_the_documented_range(D, io, gate):
     check_against_oracle(inp, cu, H, D, init, out, fin, D ** -0.5)
 
 
-# State-pass forms by shape (the launcher's dispatch): the tensor-memory pass (head size 128,
-# bf16, 96 (sequence, head) pairs), the one-warp register pass (64 pairs), the warp-pair pass
-# (16 pairs), and the register pass at head sizes 64 and 32.
+# State-pass forms by shape (the launcher's dispatch): the tensor-memory passes (head size 128,
+# bf16: one CTA per pair for 96 (sequence, head) pairs, two value-split CTAs per pair for 64
+# and 16), the one-warp and warp-pair register passes (fp32, 64 and 16 pairs), and the register
+# pass at head sizes 64 and 32.
 STRONG_DECAY_FORMS = {
     "tcgen05": (128, torch.bfloat16, [200, 65, 131], 32, [0, 13, 31]),
-    "one_warp": (128, torch.bfloat16, [150, 71], 32, [0, 21]),
-    "warp_pair": (128, torch.bfloat16, [327, 100, 1, 0], 4, None),
+    "tcgen05_split": (128, torch.bfloat16, [150, 71], 32, [0, 21]),
+    "tcgen05_split_few": (128, torch.bfloat16, [327, 100, 1, 0], 4, None),
+    "one_warp": (128, torch.float32, [150, 71], 32, [0, 21]),
+    "warp_pair": (128, torch.float32, [327, 100, 1, 0], 4, None),
     "d64": (64, torch.bfloat16, [130, 64, 9], 3, None),
     "d32_fp32": (32, torch.float32, [100, 37, 64], 2, None),
 }

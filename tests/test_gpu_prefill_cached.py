@@ -51,8 +51,9 @@ def make_case(lengths, H, D, io, cache_dtype, itype, seed, n_rows=24, gap=64):
 @pytest.mark.parametrize("cache_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("itype", [torch.int32, torch.int64])
 def test_cached_equals_unfused_bit_for_bit(D, H, io, cache_dtype, itype):
-    """D = 128 with 40 heads x 4 sequences runs the tensor-memory state pass, with 2 heads
-    the warp-pair register pass; the others the register pass with value splits."""
+    """D = 128, bf16: 40 heads x 4 sequences run the tensor-memory state pass with one CTA per
+    (sequence, head), 2 heads its value-split form; fp32 with 2 heads the warp-pair register
+    pass; the others the register pass with value splits."""
     lengths = [130, 0, 64, 257]
     cu, inp, pc, idx_in, flags, idx_out = make_case(lengths, H, D, io, cache_dtype, itype, seed=D + H)
     B, T = len(lengths), cu[-1]
@@ -116,18 +117,19 @@ def test_cached_in_place_slot_reuse_against_oracle():
     assert np.array_equal(after[~touched], before[~touched])  # every other byte untouched
 
 
-@pytest.mark.parametrize("D,H", [(128, 40), (128, 2), (64, 3)])  # tensor-memory, warp-pair, one-warp passes
+# tensor-memory (one CTA per pair, value-split), warp-pair and one-warp register passes
+@pytest.mark.parametrize("D,H,io", [(128, 40, torch.bfloat16), (128, 2, torch.bfloat16), (128, 2, torch.float32),
+                                    (64, 3, torch.bfloat16)])
 @pytest.mark.parametrize("ckpt_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("every", [64, 128, 192])
-def test_checkpoints_match_oracle(D, H, ckpt_dtype, every):
+def test_checkpoints_match_oracle(D, H, io, ckpt_dtype, every):
     lengths = [130, 0, 384, 63, 192]
-    cu, inp, pc, idx_in, flags, _ = make_case(lengths, H, D, torch.bfloat16, torch.float32, torch.int32,
-                                              seed=every + D)
+    cu, inp, pc, idx_in, flags, _ = make_case(lengths, H, D, io, torch.float32, torch.int32, seed=every + D)
     B, T, N = len(lengths), cu[-1], pc.view.shape[0]
     n = kda_prefill_checkpoint_count(cu, every)
     assert n == sum(L // every for L in lengths)
     cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
-    out = torch.empty(T, H, D, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(T, H, D, dtype=io, device=DEV)
     fin = torch.empty(B, H, D, D, dtype=torch.float32, device=DEV)
     ck = torch.full((max(n, 1), H, D, D), float("nan"), dtype=ckpt_dtype, device=DEV)
     ws = workspace(T, B, H, D)
