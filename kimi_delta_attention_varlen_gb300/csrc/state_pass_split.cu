@@ -26,13 +26,15 @@
 // Threads: eight compute warps (warp w serves TMEM lanes 32 (w % 4) ... and
 // columns 32 (w / 4) ... of the slice), an MMA warp and a copy warp.  The
 // compute warps signal the MMA warp through named barriers (operands written)
-// and never issue or wait on an MMA issue themselves; mbarriers signal [X; Y]
-// (to the V_new step), S (to the next chunk) and O (to the output rows and the
-// copy warp).  Records are triple-buffered, and each CTA copies only its half
-// of U^T, with the next three records prefetched into L2.  The warps of lanes 0..63 form V_new while those of lanes 64..127
-// move the previous chunk's output rows out of tensor memory.  Every wait is bounded; an expired wait
-// sets the workspace status word and the CTA stops waiting, waits (bounded) for
-// its own copies in flight, and still frees its TMEM.
+// and never issue or wait on an MMA issue themselves; mbarriers signal
+// [-V_new; Y] (to the V_new step), S (to the next chunk) and O (to the output
+// rows and the copy warp).  Records are triple-buffered, and each CTA copies
+// only its half of U^T (prefetching later records into L2 as well made the
+// pass 3 % slower).  The warps of lanes 0..63 form V_new while those of lanes
+// 64..127 move the previous chunk's output rows out of tensor memory.  Every
+// wait is bounded; an expired wait sets the workspace status word and the CTA
+// stops waiting, waits (bounded) for its own copies in flight, and still frees
+// its TMEM.
 #include "prefill_common.cuh"
 #include "tcgen05.cuh"
 
@@ -50,7 +52,6 @@ constexpr int kSpThreads = kSpCompute + 64;
 constexpr uint32_t kSpWaitLimit = 1u << 22;
 using RS = Rec<kSpD>;
 constexpr int kSpStages = 3;
-constexpr int kSpAhead = 3;                        // records prefetched into L2 beyond the stages
 constexpr int kSpMain = RS::UT;                    // [W; Q~], K~, A_qk, gamma
 constexpr int kSpUt = kSpNV * C * 2;               // this CTA's rows of U^T
 constexpr int kSpUtOff = (kSpMain + 1023) / 1024 * 1024;  // U^T rows at a swizzle-atom boundary
@@ -161,22 +162,14 @@ state_pass_split_kernel(PassParams p)
                 bulk_g2s(dst, rec, kSpMain, bar);
                 bulk_g2s(dst + kSpUtOff, rec + RS::UT + slice * kSpUt, kSpUt, bar);
             };
-            auto prefetch = [&](int32_t i) {  // a record kSpAhead chunks beyond the stages, into L2
-                if (i >= n_chunks) return;
-                const char *rec = p.records + (static_cast<int64_t>(c_begin + i) * H + h) * RS::BYTES;
-                prefetch_l2(rec, kSpMain);
-                prefetch_l2(rec + RS::UT + slice * kSpUt, kSpUt);
-            };
             int32_t last = -1;
             for (int32_t i = 0; i < n_chunks && i < kSpStages; ++i) issue(last = i);
-            for (int32_t i = kSpStages; i < kSpStages + kSpAhead; ++i) prefetch(i);
             for (int32_t i = 0; i + kSpStages < n_chunks; ++i) {
                 if (!mbar_wait(&bar_o[i % kSpStages], (i / kSpStages) & 1, kSpWaitLimit)) {
                     atomicExch(p.status, 2);
                     break;
                 }
                 issue(last = i + kSpStages);
-                prefetch(i + kSpStages + kSpAhead);
             }
             // every copy this CTA issued has landed before it exits
             for (int32_t i = last; i >= 0 && i > last - kSpStages; --i)
