@@ -467,7 +467,7 @@ __device__ __forceinline__ void prep_chunk(const PrepParams &p, const PrepMaps &
     // sums (an odd warp starts at its block's midpoint m; an even warp ends one row before it
     // and adds g at m).  A chunk where some channel exceeds kSpanLimit goes to the fix-up list,
     // whose kernel forms the whole record again with the exact Gram; this CTA carries on, and
-    // what it writes is overwritten.  The fast kernel's block index is the item, chunk * H + h.
+    // what it writes is overwritten.  The list holds the item, chunk * H + h.
     bool wide = false;
     if constexpr (!kExact) {
         float gmid[CPL];
@@ -486,7 +486,7 @@ __device__ __forceinline__ void prep_chunk(const PrepParams &p, const PrepMaps &
             for (int c = 0; c < CPL; ++c) wide |= fabsf(gr[j][c] - gmid[c]) > kSpanLimit;
     }
     cp_async_wait_all();
-    if (__syncthreads_or(wide) && tid == 0) p.fix_list[atomicAdd(p.fix_count, 1)] = static_cast<int32_t>(blockIdx.x);
+    if (__syncthreads_or(wide) && tid == 0) p.fix_list[atomicAdd(p.fix_count, 1)] = static_cast<int32_t>(chunk * p.H + h);
     if constexpr (kTma) wait_loads(0);  // q and k are in their tiles
     float gm[4][CPL], glast[CPL], off[CPL];
     {
@@ -1025,7 +1025,8 @@ chunk_prep_kernel(PrepParams p, const __grid_constant__ PrepMaps maps)
     __shared__ __align__(8) uint64_t ld_bar;
     bool gave_up = false;
     init_load_barrier<D, IO>(ld_bar);
-    prep_chunk<D, IO, false>(p, maps, blockIdx.x / p.H, static_cast<int>(blockIdx.x % p.H), smem, ld_bar, gave_up);
+    prep_chunk<D, IO, false>(p, maps, p.chunk_base + blockIdx.x / p.H, static_cast<int>(blockIdx.x % p.H), smem, ld_bar,
+                             gave_up);
 }
 
 // The (chunk, head) items the block split left in the fix-up list, with the exact Gram;

@@ -107,6 +107,7 @@ cudaError_t launch_ckpt_load_int8(const CacheDesc &c, const int8_t *qdata, const
 struct PrefillLayout {
     int64_t n_chunk_max;
     size_t off_chunk_off, off_seq_order, off_chunk_info, off_ckpt_off, off_fix_list, off_records, rec_bytes, total;
+    size_t off_seg_state;  // one sequence at head size 128: its state between segments (fp32 [H][V][K]), else 0
     size_t compact;  // bytes the fused kernel needs: the header and the chunk table, no records
 };
 

@@ -47,6 +47,7 @@
 // the products stay in fp32/bf16 range while that decay is above -80.  All
 // inter-chunk factors (e^G, e^{G_last - G}, e^{G_last}) are <= 1 for g <= 0.
 #include <atomic>
+#include <mutex>
 
 #include "prefill_common.cuh"
 
@@ -77,6 +78,37 @@ using prefill::ckpt_slot;
 using prefill::load_state2;
 using prefill::store_state2;
 constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier polls
+constexpr int64_t kSegChunks = 256;         // chunks per segment of the segmented prefill
+
+// The segmented prefill's second stream (the highest priority, non-blocking) and its events, one
+// set per device, created on first use and kept for the process; calls that use them hold the mutex
+// while they enqueue.
+struct SegStreams {
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, seg = nullptr, join = nullptr;
+};
+std::mutex g_seg_mu;
+SegStreams g_seg[64];
+
+cudaError_t seg_streams(SegStreams **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    SegStreams &r = g_seg[dev];
+    if (r.aux == nullptr) {
+        int least = 0, greatest = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+        SegStreams n;
+        if ((e = cudaStreamCreateWithPriority(&n.aux, cudaStreamNonBlocking, greatest)) != cudaSuccess) return e;
+        for (cudaEvent_t *ev : {&n.fork, &n.seg, &n.join})
+            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+        r = n;
+    }
+    *out = &r;
+    return cudaSuccess;
+}
 
 // ---------------------------------------------------------- chunk table ---
 
@@ -704,22 +736,53 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
         }
     }
 
+    prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, chunk_info, a.h, a.scale, a.l2norm, records, status,
+                           a.total_tokens, status + 1, reinterpret_cast<int32_t *>(ws + L.off_fix_list), 0};
+    StateEnds se = a.se;
+    se.ckpt_every = ckpt_every;
+    se.ckpt_off = ckpt_off;
+    PassParams sp{a.cu_seqlens, chunk_off, seq_order, status, records, a.h, se, a.out};
+    const int64_t items = a.num_seqs * a.h;
+
+    // One long sequence with few heads (head size 128, bf16): its chunks in segments of kSegChunks.
+    // The value-split state pass of segment s runs on a second stream of the highest priority while
+    // segment s + 1 is prepared on the SMs it leaves free; the pass alone would leave most SMs idle
+    // for its serial chain.  Events order everything after the caller's stream and back onto it.
+    if constexpr (D == 128 && sizeof(IO) == 2) {
+        if (L.off_seg_state != 0 && items * prefill::state_pass_split_slices() <= sm_count() &&
+            L.n_chunk_max >= 2 * kSegChunks) {
+            std::lock_guard<std::mutex> lock(g_seg_mu);
+            SegStreams *ss = nullptr;
+            if ((e = seg_streams(&ss)) != cudaSuccess) return e;
+            sp.seg_state = reinterpret_cast<float *>(ws + L.off_seg_state);
+            if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
+            if ((e = cudaStreamWaitEvent(ss->aux, ss->fork, 0)) != cudaSuccess) return e;
+            for (int64_t lo = 0; lo < L.n_chunk_max; lo += kSegChunks) {
+                const int64_t hi = lo + kSegChunks < L.n_chunk_max ? lo + kSegChunks : L.n_chunk_max;
+                pp.chunk_base = lo;
+                if ((e = prefill::launch_chunk_prep(D, a.io_dtype, pp, hi - lo, a.h, st)) != cudaSuccess) return e;
+                if ((e = cudaMemsetAsync(status + 1, 0, sizeof(int32_t), st)) != cudaSuccess) return e;  // fix-up list
+                if ((e = cudaEventRecord(ss->seg, st)) != cudaSuccess) return e;
+                if ((e = cudaStreamWaitEvent(ss->aux, ss->seg, 0)) != cudaSuccess) return e;
+                sp.seg_lo = static_cast<int32_t>(lo);
+                sp.seg_hi = hi < L.n_chunk_max ? static_cast<int32_t>(hi) : 0x7fffffff;
+                if ((e = prefill::launch_state_pass_split(sp, items, ss->aux)) != cudaSuccess) return e;
+            }
+            if ((e = mark(2)) != cudaSuccess) return e;  // every segment prepared
+            if ((e = cudaEventRecord(ss->join, ss->aux)) != cudaSuccess) return e;
+            if ((e = cudaStreamWaitEvent(st, ss->join, 0)) != cudaSuccess) return e;
+            return mark(3);
+        }
+    }
+
     if (L.n_chunk_max > 0) {
-        const prefill::PrepParams pp{a.q, a.k, a.v, a.g, a.beta, chunk_info, a.h, a.scale, a.l2norm, records, status,
-                                     a.total_tokens, status + 1,
-                                     reinterpret_cast<int32_t *>(ws + L.off_fix_list)};
         e = prefill::launch_chunk_prep(D, a.io_dtype, pp, L.n_chunk_max, a.h, st);
         if (e != cudaSuccess) return e;
     }
 
     if ((e = mark(2)) != cudaSuccess) return e;
-    StateEnds se = a.se;
-    se.ckpt_every = ckpt_every;
-    se.ckpt_off = ckpt_off;
-    PassParams sp{a.cu_seqlens, chunk_off, seq_order, status, records, a.h, se, a.out};
     // Enough CTAs to cover the SMs: split the value columns when there are few
     // (sequence, head) pairs.  Columns of S evolve independently.
-    const int64_t items = a.num_seqs * a.h;
     int warps = D / 16;
     while (warps > 1 && items * (D / (16 * warps)) < 120) warps /= 2;
     if constexpr (D == 128 && sizeof(IO) == 2) {  // the tensor-memory state passes
@@ -764,6 +827,10 @@ bool prefill_layout(int64_t total_tokens, int64_t num_seqs, int32_t h, int32_t d
     L.compact = L.off_fix_list;
     L.off_records = up(L.off_fix_list + 4 * static_cast<size_t>(L.n_chunk_max) * static_cast<size_t>(h), 1024);
     L.total = L.off_records + static_cast<size_t>(L.n_chunk_max) * static_cast<size_t>(h) * L.rec_bytes;
+    if (num_seqs == 1 && d == 128) {  // the segmented prefill of one sequence keeps its state here between segments
+        L.off_seg_state = up(L.total, 256);
+        L.total = L.off_seg_state + static_cast<size_t>(h) * d * d * 4;
+    }
     *out = L;
     return true;
 }

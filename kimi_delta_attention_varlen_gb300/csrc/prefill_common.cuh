@@ -66,6 +66,7 @@ struct PrepParams {
     int64_t total_tokens;  // rows of q, k, v (host side: the tensor maps' extent)
     int32_t *fix_count;    // (chunk, head) items whose decay the block split cannot take ...
     int32_t *fix_list;     // ... (chunk * H + head), formed by the exact kernel
+    int64_t chunk_base;    // first chunk of this launch (CTA i takes chunk chunk_base + i / H)
 };
 
 // Tensor maps of the bf16 q, k, v inputs [T][H][D] (3-D: channel, head, token;
@@ -84,6 +85,11 @@ struct PassParams {
     int32_t H;
     StateEnds se;
     void *out;
+    // A segment of every sequence's chunks, [seg_lo, seg_hi) (the value-split tensor-memory pass
+    // only): a segment after the first starts from seg_state, one before the last ends in it
+    // (fp32 [B][H][V][K]); the defaults take whole sequences.
+    int32_t seg_lo = 0, seg_hi = 0x7fffffff;
+    float *seg_state = nullptr;
 };
 
 __device__ __forceinline__ int64_t row_index(const void *idx, int32_t it, int64_t b)

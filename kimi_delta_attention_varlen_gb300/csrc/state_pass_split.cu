@@ -122,8 +122,15 @@ state_pass_split_kernel(PassParams p)
     const int v0 = kSpNV * slice + 32 * part;       // this thread's 32 columns
     const int h = static_cast<int>(item % H);
     const int64_t b = p.seq_order[item / H];
-    const int32_t c_begin = p.chunk_off[b], n_chunks = p.chunk_off[b + 1] - c_begin;
-    const int64_t tok_begin = p.cu[b], tok_end = p.cu[b + 1];
+    // this launch's chunks of the sequence: the segment [seg_lo, seg_hi) of its n_all chunks
+    const int32_t n_all = p.chunk_off[b + 1] - p.chunk_off[b];
+    const int32_t c_lo = p.seg_lo > 0 ? p.seg_lo : 0, c_hi = p.seg_hi < n_all ? p.seg_hi : n_all;
+    const int32_t n_chunks = c_hi > c_lo ? c_hi - c_lo : 0;
+    if (n_chunks == 0 && (n_all > 0 || c_lo > 0)) return;  // nothing of this sequence here (uniform over the CTA)
+    const bool first = c_lo == 0, last = c_hi >= n_all;     // the segment starts / ends the sequence
+    const int32_t c_begin = p.chunk_off[b] + c_lo;          // record index of the segment's first chunk
+    const int64_t tok_seq = p.cu[b], tok_end = p.cu[b + 1];
+    const int64_t tok_begin = tok_seq + static_cast<int64_t>(c_lo) * C;  // first token of the segment
 
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, kSpTmemCols);
@@ -247,13 +254,15 @@ state_pass_split_kernel(PassParams p)
     // element offset of state row [h][v][k] for this thread's key k = lane and column v
     auto srow = [&](int v) { return (static_cast<int64_t>(h) * kSpD + v) * kSpD + lane; };
 
-    // initial state: S[k][v0 ... v0 + 31] for key k = lane
+    // initial state: S[k][v0 ... v0 + 31] for key k = lane (after the first segment: the previous one's end)
     {
-        const int64_t base = init_base(p.se, b, H * kSpD * kSpD);
+        const void *src = first ? p.se.init : p.seg_state;
+        const int32_t dtype = first ? p.se.init_dtype : KDA_F32;
+        const int64_t base = first ? init_base(p.se, b, H * kSpD * kSpD) : b * H * kSpD * kSpD;
         uint32_t r[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            r[j] = __float_as_uint(base >= 0 ? load_state1(p.se.init, p.se.init_dtype, base + srow(v0 + j)) : 0.f);
+            r[j] = __float_as_uint(base >= 0 ? load_state1(src, dtype, base + srow(v0 + j)) : 0.f);
         tc::st32(tl + kSpColS + 32 * part, r);
         tc::wait_st();
     }
@@ -295,7 +304,7 @@ state_pass_split_kernel(PassParams p)
 
         // S is the state after chunk i - 1: a checkpoint when that chunk ends on one.
         if (p.se.ckpt != nullptr && i > 0) {
-            const int64_t ck = ckpt_slot(p.se, b, i - 1, tok_end - tok_begin);
+            const int64_t ck = ckpt_slot(p.se, b, c_lo + i - 1, tok_end - tok_seq);
             if (ck >= 0) {
                 uint32_t r[32];
                 tc::ld32(tl + kSpColS + 32 * part, r);
@@ -347,16 +356,18 @@ state_pass_split_kernel(PassParams p)
     }
     if (n_chunks > 0 && quad >= 2) store_outputs(n_chunks - 1);
 
-    // final state -> packed fp32, the cache row out_idx[b], and the last checkpoint if it ends there
+    // final state -> packed fp32 and the cache row out_idx[b] (or, before the sequence's last
+    // segment, the segment state), and the checkpoint of the segment's last chunk if it ends on one
     {
         const int64_t per_seq = H * kSpD * kSpD;
-        const int64_t ob = out_base(p.se, b);
-        const int64_t ck = n_chunks > 0 ? ckpt_slot(p.se, b, n_chunks - 1, tok_end - tok_begin) : -1;
-        if (p.se.final_state != nullptr || ob >= 0 || ck >= 0) {
+        const int64_t ob = last ? out_base(p.se, b) : -1;
+        const int64_t ck = n_chunks > 0 ? ckpt_slot(p.se, b, c_hi - 1, tok_end - tok_seq) : -1;
+        float *fin = last ? p.se.final_state : p.seg_state;
+        if (fin != nullptr || ob >= 0 || ck >= 0) {
             uint32_t r[32];
             tc::ld32(tl + kSpColS + 32 * part, r);
             tc::wait_ld();
-            if (p.se.final_state != nullptr) put_state(p.se.final_state, KDA_F32, b * per_seq, r);
+            if (fin != nullptr) put_state(fin, KDA_F32, b * per_seq, r);
             if (ob >= 0) put_state(p.se.out_cache, p.se.out_dtype, ob, r);
             if (ck >= 0) put_state(p.se.ckpt, p.se.ckpt_dtype, ck * per_seq, r);
         }

@@ -1,0 +1,96 @@
+"""GPU parity of the segmented prefill: one sequence at head size 128, bf16, with few
+heads and at least two segments of 256 chunks runs its chunk preparation and its
+value-split state pass segment by segment, the pass of one segment overlapping the
+preparation of the next on a second stream, with the state handed between segments
+through the workspace.
+
+Checked against the token-by-token fp64 oracle at the method's tolerances (outputs
+max|d| <= 2e-2 max|ref|, states ||dS||_F <= 1e-2 ||S_ref||_F), and bit for bit against
+the same sequence run unsegmented (a batch of it and an empty sequence, which takes the
+same kernels in one launch each): outputs, final states, checkpoints on and off the
+segment boundaries, and the cache row written by the cache-indexed entry point."""
+import pytest
+import torch
+
+import oracle
+from kimi_delta_attention_varlen_gb300 import (kda_prefill_checkpoint_count, kda_prefill_varlen,
+                                               kda_prefill_varlen_cached, kda_prefill_workspace_size,
+                                               kda_prefill_workspace_status)
+from kimi_delta_attention_varlen_gb300 import workloads as wl
+from tests.helpers import assert_out_close, assert_state_close, f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+D = 128
+SEG = 256 * 64  # tokens per segment
+
+
+def workspace(cu, H):
+    return torch.empty(kda_prefill_workspace_size(cu[-1], len(cu) - 1, H, D, D), dtype=torch.uint8, device=DEV)
+
+
+def prefill(inp, cu, H, init, every=0, n_slots=0):
+    T, B = cu[-1], len(cu) - 1
+    out = torch.full((T, H, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    fin = torch.full((B, H, D, D), float("nan"), device=DEV)
+    ws = workspace(cu, H)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    if every:
+        rows = wl.paged_cache(B + 2, H, D, D, torch.float32, H * D * D + 64, seed=5, device=DEV)
+        rows.view[:B].copy_(init[:B])
+        idx_in = torch.arange(B, dtype=torch.int32)
+        idx_out = torch.arange(B, dtype=torch.int32) + 2
+        ck = torch.full((max(n_slots, 1), H, D, D), float("nan"), device=DEV)
+        kda_prefill_varlen_cached(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, out, ws, rows.view,
+                                  idx_in.to(DEV), idx_out=idx_out.to(DEV), final_state=fin, checkpoints=ck[:n_slots],
+                                  ckpt_every=every)
+        torch.cuda.synchronize()
+        assert kda_prefill_workspace_status(ws) == 0
+        return out, fin, ck[:n_slots], rows.view[2:2 + B].clone()
+    kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, out, ws, init_state=init,
+                       final_state=fin)
+    torch.cuda.synchronize()
+    assert kda_prefill_workspace_status(ws) == 0
+    return out, fin, None, None
+
+
+@pytest.mark.parametrize("T,H", [(2 * SEG, 4), (2 * SEG + 37, 8), (3 * SEG - 64 * 3 + 5, 2)])
+def test_segmented_equals_unsegmented_and_oracle(T, H):
+    """Two segments exactly, two and a 1-chunk tail of 37 tokens, and three segments whose last
+    is short: bit-identical with the unsegmented run, and within tolerance of the oracle."""
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=T % 997 + H, device=DEV, decay_scale=0.3)
+    init = torch.randn(2, H, D, D, generator=wl.generator(T % 89, DEV), device=DEV) * 0.5
+    out_s, fin_s, _, _ = prefill(inp, [0, T], H, init[:1])
+    out_u, fin_u, _, _ = prefill(inp, [0, T, T], H, init)
+    assert torch.equal(out_s.view(torch.uint8), out_u.view(torch.uint8))
+    assert torch.equal(fin_s[0], fin_u[0])
+    heads = [0, H - 1]
+    o_ref, f_ref = oracle.prefill(f64(inp["q"][:, heads]), f64(inp["k"][:, heads]), f64(inp["v"][:, heads]),
+                                  f64(inp["g"][:, heads]), f64(inp["beta"][:, heads]), [0, T],
+                                  init=f64(init[:1, heads]), scale=D ** -0.5)
+    assert_out_close(f64(out_s[:, heads]), o_ref)
+    assert_state_close(f64(fin_s[:, heads]), f_ref)
+
+
+@pytest.mark.parametrize("every", [4096, SEG])
+def test_segmented_checkpoints_and_cache_rows(every):
+    """Checkpoints every 4,096 tokens (inside segments and at their ends) or every segment, the
+    initial state from a cache row and the final one to another: bit-identical with the
+    unsegmented run, the checkpoints within tolerance of the oracle's chunk-boundary states."""
+    T, H = 2 * SEG + 1000, 4
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=every % 1000, device=DEV, decay_scale=0.3)
+    init = torch.randn(2, H, D, D, generator=wl.generator(every % 97, DEV), device=DEV) * 0.5
+    n = kda_prefill_checkpoint_count([0, T], every)
+    out_s, fin_s, ck_s, row_s = prefill(inp, [0, T], H, init[:1], every, n)
+    out_u, fin_u, ck_u, row_u = prefill(inp, [0, T, T], H, init, every, kda_prefill_checkpoint_count([0, T, T], every))
+    assert torch.equal(out_s.view(torch.uint8), out_u.view(torch.uint8))
+    assert torch.equal(fin_s[0], fin_u[0])
+    assert torch.equal(ck_s, ck_u[:n])
+    assert torch.equal(row_s[0], row_u[0]) and torch.equal(row_s[0], fin_s[0])
+    heads = [1, 3]
+    _, _, ck_ref = oracle.prefill_ckpt(f64(inp["q"][:, heads]), f64(inp["k"][:, heads]), f64(inp["v"][:, heads]),
+                                       f64(inp["g"][:, heads]), f64(inp["beta"][:, heads]), [0, T], every,
+                                       init=f64(init[:1, heads]), scale=D ** -0.5)
+    assert ck_ref.shape[0] == n
+    for s in range(n):
+        assert_state_close(f64(ck_s[s, heads]), ck_ref[s], what=f"checkpoint {s}")
