@@ -355,8 +355,10 @@ def conv1d_measure(P, steps: int, warmup: int, W: int = 4) -> dict:
 def long_prefill_measure(dev, steps: int, warmup: int, tokens: int | None = None) -> dict:
     """The long single-sequence prefill (131,072 tokens unless `tokens` says otherwise; 32 heads,
     head size 128, bf16, zero initial state, final state out).  Its state pass is one serial chain of
-    T / 64 chunks per head over only 32 (sequence, head) pairs, the few-chain shape; chunk
-    preparation and state pass are timed separately with events inside the call."""
+    T / 64 chunks per head over only 32 (sequence, head) pairs, the few-chain shape.  From 512
+    chunks on, the prefill runs segmented (the state pass of each 256-chunk segment overlapping the
+    next segment's preparation): prep_ms is then the time until the last segment is prepared and
+    pass_ms the rest; unsegmented they are the two kernels' times."""
     import kimi_delta_attention_varlen_gb300 as kda
     from kimi_delta_attention_varlen_gb300 import workloads as wl
     w = wl.long_seq(0, T=tokens) if tokens else wl.long_seq(0)
@@ -383,7 +385,9 @@ def long_prefill_measure(dev, steps: int, warmup: int, tokens: int | None = None
     tot = med(e[0].elapsed_time(e[3]) for e in evs)
     del inp, out, fin, ws
     torch.cuda.empty_cache()
-    return {"workload": w.name, "prep_ms": prep, "pass_ms": pas, "ms": tot, "tokens_per_s": T / (tot * 1e-3)}
+    form = "segmented (256-chunk segments, passes overlapping preparation)" if T >= 512 * 64 else "two kernels"
+    return {"workload": w.name, "form": form, "prep_ms": prep, "pass_ms": pas, "ms": tot,
+            "tokens_per_s": T / (tot * 1e-3)}
 
 
 def compact_measure(P, dev, steps: int, warmup: int, long_tokens: int | None = None) -> dict:

@@ -11,11 +11,15 @@
  *
  * Conventions shared by every entry point
  *   - Every data pointer is a DEVICE pointer unless stated otherwise; the
- *     caller owns every buffer.  The library keeps no pointer, stream or
- *     buffer after a call returns, allocates no memory and never
+ *     caller owns every buffer.  The library keeps no pointer or buffer of
+ *     the caller's after a call returns, allocates no device memory and never
  *     synchronises the host with the device.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
- *     stream).  Work is enqueued on it and nothing else.
+ *     stream).  Work is enqueued on it and nothing else, with one exception:
+ *     the segmented prefill of one long sequence (kda_prefill_varlen) also
+ *     enqueues on a stream of the library's own, ordered after `stream` and
+ *     joined back into it by events, so work enqueued on `stream` after the
+ *     call still sees every result.
  *   - All argument checks run on the host, on metadata only, before anything
  *     is launched.  A failed check returns a negative kda_status and launches
  *     nothing.  KDA_ERR_CUDA means the launch itself failed (for example no
@@ -201,6 +205,15 @@ size_t kda_prefill_workspace_size_compact(int64_t total_tokens, int64_t num_seqs
  *               (the fused kernel, when ws_bytes is below the former);
  *               256-byte aligned; its contents on entry do not matter.
  *   Calls on one workspace must not overlap in time.
+ * Segmented prefill.  One sequence (num_seqs == 1) at head size 128, bf16,
+ * with at least 512 chunks and at most half as many heads as the GPU has SMs,
+ * given the full workspace, runs in segments of 256 chunks: the state pass of
+ * a segment runs on a second stream (the device's highest priority, created by
+ * the library on the first such call on each device and kept until the process
+ * exits; make that first call outside stream capture) while the next segment's
+ * chunks are prepared on `stream`.  The results are bit-identical with the
+ * unsegmented form.  Calls from several host threads are serialised while
+ * they enqueue.
  * Errors, checked on the host before anything is launched: KDA_ERR_DTYPE;
  * KDA_ERR_SHAPE (num_seqs < 1, total_tokens < 0, h, dk or dv < 1);
  * KDA_ERR_UNSUPPORTED (head sizes); KDA_ERR_RANGE (total_tokens >= 2^31,
@@ -224,7 +237,9 @@ int kda_prefill_varlen(const void *q, const void *k, const void *v, int32_t io_d
  * caller-created CUDA events (cudaEvent_t passed as void*, host array
  * `events`) on `stream`: events[0] before the chunk-table kernel, events[1]
  * before the chunk-preparation kernel, events[2] before the state-pass
- * kernel, events[3] after it.  For measuring each kernel's device time.
+ * kernel, events[3] after it.  For measuring each kernel's device time.  In
+ * the segmented prefill the state passes overlap the preparation: events[2]
+ * follows the last segment's preparation and events[3] the last state pass.
  * events == NULL returns KDA_ERR_NULL; a NULL entry leaves its boundary
  * unrecorded (each record costs a few microseconds of stream time).
  * ---------------------------------------------------------------------- */
