@@ -8,7 +8,8 @@ Checked against the token-by-token fp64 oracle at the method's tolerances (outpu
 max|d| <= 2e-2 max|ref|, states ||dS||_F <= 1e-2 ||S_ref||_F), and bit for bit against
 the same sequence run unsegmented (a batch of it and an empty sequence, which takes the
 same kernels in one launch each): outputs, final states, checkpoints on and off the
-segment boundaries, and the cache row written by the cache-indexed entry point."""
+segment boundaries, and the cache row written by the cache-indexed entry point; and
+captured into a CUDA graph, whose replay matches the eager call."""
 import pytest
 import torch
 
@@ -94,3 +95,37 @@ def test_segmented_checkpoints_and_cache_rows(every):
     assert ck_ref.shape[0] == n
     for s in range(n):
         assert_state_close(f64(ck_s[s, heads]), ck_ref[s], what=f"checkpoint {s}")
+
+
+def test_segmented_capture_into_a_cuda_graph():
+    """The segmented prefill forks onto the library's stream and joins back by events, which
+    stream capture follows: captured once (after a first call outside capture), a replay on new
+    input values gives the eager results bit for bit."""
+    T, H = 2 * SEG + 37, 2
+    cu = [0, T]
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=3, device=DEV, decay_scale=0.3)
+    init = torch.randn(1, H, D, D, generator=wl.generator(4, DEV), device=DEV) * 0.5
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    ws = workspace(cu, H)
+
+    def call(out, fin):
+        kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, out, ws, init_state=init,
+                           final_state=fin)
+
+    outs = [(torch.empty(T, H, D, dtype=torch.bfloat16, device=DEV), torch.empty(1, H, D, D, device=DEV))
+            for _ in range(2)]
+    call(*outs[0])  # outside capture: the library's stream exists from here on
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call(*outs[1])
+    for t in (inp["q"], inp["v"]):
+        t.copy_(torch.randn(t.shape, device=DEV).to(t.dtype))
+    graph.replay()
+    torch.cuda.synchronize()
+    call(*outs[0])
+    torch.cuda.synchronize()
+    assert kda_prefill_workspace_status(ws) == 0
+    assert torch.equal(outs[1][0].view(torch.uint8), outs[0][0].view(torch.uint8))
+    assert torch.equal(outs[1][1], outs[0][1])
