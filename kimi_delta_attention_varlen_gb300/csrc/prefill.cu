@@ -34,10 +34,14 @@
 //                           output, few pairs), or
 //      state_pass_kernel    one CTA per (sequence, head, value slice), S in
 //                           registers (fp32 accumulators), double-buffering
-//                           the records into shared memory with bulk copies;
-//                           for few pairs at head size 128 its warp-pair form
-//                           (state_pass_pair_kernel) splits each value group's
-//                           key channels over two warps.
+//                           the records into shared memory with bulk copies
+//                           (head sizes 32 and 64, fp32 outputs); for few
+//                           pairs at head size 128 with fp32 outputs its
+//                           warp-pair form (state_pass_pair_kernel) splits
+//                           each value group's key channels over two warps.
+//   One long sequence at head size 128 (bf16) runs 2. and 3. in segments of
+//   256 chunks, the pass of a segment overlapping the next one's preparation
+//   on a second stream.
 // All products run on the tensor cores (bf16 operands, fp32 accumulation).
 //
 // Exponent ranges.  Factors e^{G_i - G_j} are split through a reference row:
@@ -791,8 +795,7 @@ cudaError_t launch_typed(const PrefillArgs &a, const PrefillLayout &L, cudaStrea
                                                                     : prefill::launch_state_pass_tc(sp, items, st);
         if (e != cudaSuccess) return e;
         return mark(3);
-    }
-    if constexpr (D == 128) {  // at most two 16-column groups per CTA: two warps per group
+    } else if constexpr (D == 128) {  // fp32: at most two 16-column groups per CTA: two warps per group
         if (warps == 8) e = launch_pass<D, IO, 8>(sp, items, st);
         else if (warps == 4) e = launch_pass<D, IO, 4>(sp, items, st);
         else if (warps == 2) e = launch_pair<D, IO, 2>(sp, items, st);
