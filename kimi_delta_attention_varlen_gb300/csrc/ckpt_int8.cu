@@ -28,18 +28,32 @@ template <typename IdxT> __device__ __forceinline__ int64_t idx_at(const void *p
     return static_cast<int64_t>(static_cast<const IdxT *>(p)[s]);
 }
 
-// round_half_even(x / sc) clamped to [-127, 127], with x / sc the correctly
+// Codes of four values of one row (columns with scales sc, reciprocals rc),
+// packed little-endian: round_half_even(x / sc) with x / sc the correctly
 // rounded fp32 quotient.  x * (1 / sc) lies within a few ulps (< 1e-4 for
 // |x / sc| <= 128) of the exact quotient, so it rounds to the same integer
 // unless it is within that distance of a half-integer; only there the
-// quotient itself is formed.
-__device__ __forceinline__ int quantize(float x, float sc, float rc)
+// quotient itself is formed.  No clamp is needed: |x| <= amax, so the
+// quotient is at most 127 (1 + 2^-22) in magnitude and rounds into
+// [-127, 127].  A zero scale has rc = 0 and gives code 0.
+__device__ __forceinline__ uint32_t quantize4(const float x[4], const float sc[4], const float rc[4])
 {
-    float y = __fmul_rn(x, rc);
-    const float t = y - rintf(y);                        // exact, in [-0.5, 0.5]
-    if (fabsf(t) > 0.499f) y = __fdiv_rn(x, sc);         // within 1e-3 of a half-integer
-    const int q = __float2int_rn(y);                     // ties to even
-    return q > 127 ? 127 : (q < -127 ? -127 : q);
+    float y[4];
+    bool near = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        y[e] = __fmul_rn(x[e], rc[e]);
+        near |= fabsf(y[e] - rintf(y[e])) > 0.499f;  // y - rint(y) is exact, in [-0.5, 0.5]
+    }
+    if (near) {  // rare: within 1e-3 of a half-integer
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (fabsf(y[e] - rintf(y[e])) > 0.499f) y[e] = __fdiv_rn(x[e], sc[e]);
+    }
+    int q[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q[e] = __float2int_rn(y[e]);  // ties to even
+    return __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
 }
 
 // Store geometry: a [ROWS][COLS] slice of a state block, THREADS threads, each
@@ -145,13 +159,7 @@ ckpt_store_kernel(const ElemT *__restrict__ active, int64_t n_rows, int64_t row_
         const int v = r0 + G::RPP * j;
         float x[4];
         load4(v, x);
-        uint32_t packed = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int q = sc[e] > 0.f ? quantize(x[e], sc[e], rc[e]) : 0;
-            packed |= (static_cast<uint32_t>(q) & 0xffu) << (8 * e);
-        }
-        *reinterpret_cast<uint32_t *>(qb + static_cast<int64_t>(v) * D + col) = packed;
+        *reinterpret_cast<uint32_t *>(qb + static_cast<int64_t>(v) * D + col) = quantize4(x, sc, rc);
     }
 }
 
@@ -166,17 +174,20 @@ ckpt_load_kernel(const int8_t *__restrict__ qdata, const float *__restrict__ sca
     const int64_t c = idx_at<IdxT>(src, pair), r = idx_at<IdxT>(dst, pair);
     if (c < 0 || c >= n_slots || r < 0 || r >= n_rows) return;  // uniform over the CTA
     const int64_t sbase = (c * H + h) * static_cast<int64_t>(D);
-    const uint32_t *qb = reinterpret_cast<const uint32_t *>(qdata + sbase * D);
+    const int8_t *qb = qdata + sbase * D;
     const float *sb = scale + sbase;
     ElemT *out = active + r * row_stride + static_cast<int64_t>(h) * D * D;
     // four codes per thread and step: consecutive threads cover consecutive 16 (fp32) or
-    // 8 (bf16) output bytes, so every store instruction writes one contiguous span
+    // 8 (bf16) output bytes, so every store instruction writes one contiguous span.  A thread's
+    // key columns are the same at every step (kThreads is a multiple of D / 4), so its four
+    // scales are loaded once.
     constexpr int CH = D * D / 4;
+    static_assert(kThreads % (D / 4) == 0, "fixed columns per thread");
+    const uint32_t *qb4 = reinterpret_cast<const uint32_t *>(qb);
+    const float4 s4 = __ldg(reinterpret_cast<const float4 *>(sb + (4 * static_cast<int>(threadIdx.x)) % D));
 #pragma unroll 8
     for (int e = threadIdx.x; e < CH; e += kThreads) {
-        const int k0 = (4 * e) % D;
-        const uint32_t w = __ldg(qb + e);
-        const float4 s4 = __ldg(reinterpret_cast<const float4 *>(sb + k0));
+        const uint32_t w = __ldg(qb4 + e);
         const float y0 = __fmul_rn(static_cast<float>(static_cast<int8_t>(w & 0xffu)), s4.x);
         const float y1 = __fmul_rn(static_cast<float>(static_cast<int8_t>((w >> 8) & 0xffu)), s4.y);
         const float y2 = __fmul_rn(static_cast<float>(static_cast<int8_t>((w >> 16) & 0xffu)), s4.z);
