@@ -129,3 +129,24 @@ def test_segmented_capture_into_a_cuda_graph():
     assert kda_prefill_workspace_status(ws) == 0
     assert torch.equal(outs[1][0].view(torch.uint8), outs[0][0].view(torch.uint8))
     assert torch.equal(outs[1][1], outs[0][1])
+
+
+@pytest.mark.parametrize("gate", ["g_minus_50", "mixed_channels"])
+def test_segmented_strong_decay(gate):
+    """Decays beyond the block split's range (every chunk takes the exact fix-up, whose list is
+    cleared between segments): g = -50 everywhere, and channels alternating -0.1 and -40."""
+    T, H = 2 * SEG + 100, 2
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=len(gate), device=DEV)
+    if gate == "g_minus_50":
+        inp["g"].fill_(-50.0)
+    else:
+        inp["g"].copy_(torch.where(torch.arange(D, device=DEV) % 2 == 0, -0.1, -40.0).expand_as(inp["g"]))
+    init = torch.randn(2, H, D, D, generator=wl.generator(6, DEV), device=DEV) * 0.5
+    out_s, fin_s, _, _ = prefill(inp, [0, T], H, init[:1])
+    out_u, fin_u, _, _ = prefill(inp, [0, T, T], H, init)
+    assert torch.equal(out_s.view(torch.uint8), out_u.view(torch.uint8))
+    assert torch.equal(fin_s[0], fin_u[0])
+    o_ref, f_ref = oracle.prefill(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["g"]), f64(inp["beta"]),
+                                  [0, T], init=f64(init[:1]), scale=D ** -0.5)
+    assert_out_close(f64(out_s), o_ref)
+    assert_state_close(f64(fin_s), f_ref)
