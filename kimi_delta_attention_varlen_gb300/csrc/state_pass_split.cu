@@ -31,7 +31,10 @@
 // rows and the copy warp).  Records are triple-buffered, and each CTA copies
 // only its half of U^T (prefetching later records into L2 as well made the
 // pass 3 % slower).  The warps of lanes 0..63 form V_new while those of lanes
-// 64..127 move the previous chunk's output rows out of tensor memory.  Every
+// 64..127 move the previous chunk's output rows out of tensor memory.  A launch
+// may cover one segment of every sequence's chunks (the segmented prefill of one
+// long sequence): a segment after the first starts from the fp32 state the
+// previous one left in the workspace, one before the last ends in it.  Every
 // wait is bounded; an expired wait sets the workspace status word and the CTA
 // stops waiting, waits (bounded) for its own copies in flight, and still frees
 // its TMEM.
