@@ -8,7 +8,8 @@ checked here through the C ABI on two calls in a row, since every call reuses
 the one array - and the first batch is also checked against the oracle.  The
 status word of the fixed array (kda_prefill_noalloc_status) must read 0 after
 each call.  Batches whose records do not fit the array run the compact form
-(bf16, head size 128) or are rejected.  The file is named to be collected last."""
+(bf16, head size 128) or are rejected; one long sequence whose records fit runs the
+segmented form.  The file is named to be collected last."""
 import numpy as np
 import pytest
 import torch
@@ -98,3 +99,16 @@ def test_noalloc_runs_a_large_bf16_batch_in_the_compact_form():
     o_ref, f_ref, toks = oracle_prefill_from_device(inp, cu.tolist(), init, 128 ** -0.5, heads=heads)
     assert_out_close(f64(out[toks][:, heads]), o_ref)
     assert_state_close(f64(fin[:, heads]), f_ref)
+
+
+def test_noalloc_segmented_long_sequence():
+    # one sequence of 544 chunks at 2 heads: its records fit the scratch, so it runs the
+    # segmented form (the library's second stream) - bit for bit the workspace call's results
+    T, H = 544 * 64 - 17, 2
+    assert kda.kda_prefill_workspace_size(T, 1, H, 128, 128) <= _abi.KDA_NOALLOC_SCRATCH_BYTES
+    inp, cu, init = _batch([T], 5, H=H)
+    want_out, want_fin = _with_workspace(inp, cu, init)
+    got_out, got_fin = _noalloc(inp, cu, init)
+    assert kda.kda_prefill_noalloc_status() == 0
+    assert torch.equal(got_out, want_out)
+    assert torch.equal(got_fin, want_fin)
