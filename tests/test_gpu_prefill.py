@@ -65,11 +65,13 @@ def test_prefill_ragged_varlen(D, io, decay):
     assert torch.equal(fin[4], init[4])  # the empty sequence keeps its state bit for bit
 
 
+@pytest.mark.parametrize("H", [64, 4])
 @pytest.mark.parametrize("init_kind", ["fp32", "bf16", "none"])
-def test_prefill_many_heads(init_kind):
-    """Enough (sequence, head) pairs for one CTA per pair (the tensor-memory state
-    pass at head size 128, bf16): ragged lengths, an empty sequence, every init kind."""
-    lengths, H, D = [1, 63, 64, 65, 0, 130], 64, 128
+def test_prefill_many_heads(init_kind, H):
+    """64 heads: enough (sequence, head) pairs for one CTA per pair (the tensor-memory
+    state pass at head size 128, bf16); 4 heads: its value-split form.  Ragged lengths,
+    an empty sequence, every init kind."""
+    lengths, D = [1, 63, 64, 65, 0, 130], 128
     cu = [0]
     for n in lengths:
         cu.append(cu[-1] + n)
@@ -81,7 +83,7 @@ def test_prefill_many_heads(init_kind):
             init = init.to(torch.bfloat16)
     out, fin = run_prefill(inp, cu, H, D, init=init, scale=D ** -0.5)
     ref_init = None if init is None else init.float()
-    check_against_oracle(inp, cu, H, D, ref_init, out, fin, D ** -0.5, heads=[0, 17, 63])
+    check_against_oracle(inp, cu, H, D, ref_init, out, fin, D ** -0.5, heads=[0, 17, 63] if H == 64 else None)
     if init is not None:
         assert torch.equal(fin[4], init[4].float())  # the empty sequence keeps its state
     else:

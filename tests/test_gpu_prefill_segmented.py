@@ -150,3 +150,25 @@ def test_segmented_strong_decay(gate):
                                   [0, T], init=f64(init[:1]), scale=D ** -0.5)
     assert_out_close(f64(out_s), o_ref)
     assert_state_close(f64(fin_s), f_ref)
+
+
+def test_segmented_timed_events():
+    """kda_prefill_varlen_timed on the segmented form: all four events recorded in order
+    (the state passes overlap the preparation, so events[2] follows the last segment's
+    preparation and events[3] the last pass) and the results those of the untimed call."""
+    T, H = 2 * SEG + 64, 2
+    cu = [0, T]
+    inp = wl.token_inputs(T, H, D, D, torch.bfloat16, seed=8, device=DEV, decay_scale=0.3)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    ws = workspace(cu, H)
+    outs = []
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for events in (None, ev):
+        out = torch.empty(T, H, D, dtype=torch.bfloat16, device=DEV)
+        kda_prefill_varlen(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_t, out, ws, events=events)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.uint8), outs[1].view(torch.uint8))
+    for a, b in zip(ev[:-1], ev[1:]):
+        assert a.elapsed_time(b) >= 0.0
+    assert ev[0].elapsed_time(ev[3]) > 0.0
