@@ -37,7 +37,10 @@
 // (tcgen05, MN-major A).  q, k and v arrive by TMA tensor copies straight into
 // their tiles; the next chunk's rows are prefetched into L2.  Every mbarrier
 // wait is bounded: on expiry the status word gets 5, the group stops and the
-// CTA frees its tensor memory.
+// CTA frees its tensor memory.  The preparation's serial chain is the kernel's
+// critical path, so registers move to it: the pass's warpgroups drop to 96 per
+// thread and the preparation's rise to 160 (setmaxnreg), which removes most of
+// the spilling a uniform 128 left in the preparation.
 #include <cudaTypedefs.h>
 
 #include "prefill_common.cuh"
@@ -50,6 +53,9 @@ namespace {
 constexpr int kD = 128;
 constexpr int kThreads = 512;
 constexpr int kGroup = 256;  // warps 0-7: the state pass; warps 8-15: the chunk preparation
+constexpr int kPassRegs = 96, kPrepRegs = 160;  // registers per thread of each half after the split
+static_assert(kGroup * kPassRegs + kGroup * kPrepRegs == kThreads * 128 && kPassRegs % 8 == 0 && kPrepRegs % 8 == 0,
+              "the split redistributes exactly the registers the CTA is launched with");
 constexpr uint32_t kWait = 1u << 22;
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kSpanMax = 120.f;  // widest in-chunk span of G (log2 units) for the scaled path
@@ -963,8 +969,16 @@ prefill_fused_kernel(const __grid_constant__ FusedParams p, const __grid_constan
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base;
     Waiter w{p.status};
-    if (warp < 8) pass_loop(p, sm, bar, tmem, w);
-    else prep_loop(p, maps, sm, bar, tmem, w);
+    // Registers move from the pass to the preparation: launched at 128 per thread (512 threads,
+    // the whole 65,536-register file), warpgroups 0-1 drop to 96 and warpgroups 2-3 rise to 160,
+    // 8 x 32 x 96 + 8 x 32 x 160 = 65,536, so the increase is always satisfiable.
+    if (warp < 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kPassRegs) : "memory");
+        pass_loop(p, sm, bar, tmem, w);
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kPrepRegs) : "memory");
+        prep_loop(p, maps, sm, bar, tmem, w);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -999,6 +1013,13 @@ cudaError_t launch_prefill_fused(const void *q, const void *k, const void *v, co
     p.se = se;
     p.out = static_cast<__nv_bfloat16 *>(out);
     constexpr int smem = FS::BYTES + 1024;  // + slack to align the base to 1 KiB
+    // The register split (setmaxnreg) needs the kernel launched with exactly 128 registers per
+    // thread: with fewer, the preparation's increase could never be satisfied.
+    static const int regs = [] {
+        cudaFuncAttributes fa{};
+        return cudaFuncGetAttributes(&fa, prefill_fused_kernel) == cudaSuccess ? fa.numRegs : -1;
+    }();
+    if (regs * kThreads != kGroup * (kPassRegs + kPrepRegs)) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = p.n_items < sm_count() ? p.n_items : sm_count();
