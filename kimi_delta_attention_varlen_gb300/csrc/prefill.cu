@@ -158,6 +158,8 @@ __device__ int32_t block_prefix(const int32_t *__restrict__ cu, int64_t B, int32
     return total;
 }
 
+constexpr int64_t kTableStaged = 4096;  // batches up to this many sequences are ranked by length
+
 __global__ void __launch_bounds__(1024)
 chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_max, int32_t *__restrict__ chunk_off,
                    int32_t *__restrict__ seq_order, int2 *__restrict__ chunk_info, int32_t ckpt_every,
@@ -165,6 +167,7 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_ma
 {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
+    __shared__ int32_t s_cu[kTableStaged + 1], s_off[kTableStaged + 1];
     const int tid = threadIdx.x;
     if (tid == 0) {
         status[0] = 0;
@@ -185,6 +188,18 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_ma
     if (ckpt_every > 0)  // checkpoints of sequence b: after every ckpt_every tokens, up to its length
         block_prefix(
             cu, B, ckpt_off, [ckpt_every](int32_t len) { return len > 0 ? len / ckpt_every : 0; }, warp_tot, &carry);
+    // Small batches: cu_seqlens and the chunk offsets staged in shared memory for the
+    // searches below (one parallel read instead of dependent global loads).
+    const bool staged = B <= kTableStaged;
+    if (staged) {
+        for (int64_t b = tid; b <= B; b += 1024) {
+            s_cu[b] = cu[b];
+            s_off[b] = chunk_off[b];
+        }
+        __syncthreads();
+    }
+    auto cu_at = [&](int64_t b) { return staged ? s_cu[b] : cu[b]; };
+    auto off_at = [&](int64_t b) { return staged ? s_off[b] : chunk_off[b]; };
     // Per chunk: its first token and length ({0, 0} past the last chunk), so a
     // chunk's CTA finds its rows with one load.
     for (int64_t c = tid; c < n_chunk_max; c += 1024) {
@@ -193,22 +208,22 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int64_t B, int64_t n_chunk_ma
             int64_t lo = 0, hi = B - 1;  // the b with chunk_off[b] <= c < chunk_off[b + 1]
             while (lo < hi) {
                 const int64_t mid = (lo + hi + 1) / 2;
-                if (chunk_off[mid] <= c) lo = mid;
+                if (off_at(mid) <= c) lo = mid;
                 else hi = mid - 1;
             }
-            const int32_t t0 = cu[lo] + static_cast<int32_t>(c - chunk_off[lo]) * C;
-            const int32_t left = cu[lo + 1] - t0;
+            const int32_t t0 = cu_at(lo) + static_cast<int32_t>(c - off_at(lo)) * C;
+            const int32_t left = cu_at(lo + 1) - t0;
             info = make_int2(t0, left < C ? left : C);
         }
         chunk_info[c] = info;
     }
     // Longest sequences first, so their serial chunk chains start early.
-    if (B <= 4096) {
+    if (staged) {
         for (int64_t b = tid; b < B; b += 1024) {
-            const int32_t lb = cu[b + 1] - cu[b];
+            const int32_t lb = s_cu[b + 1] - s_cu[b];
             int32_t rank = 0;
             for (int64_t o = 0; o < B; ++o) {
-                const int32_t lo = cu[o + 1] - cu[o];
+                const int32_t lo = s_cu[o + 1] - s_cu[o];
                 rank += (lo > lb) || (lo == lb && o < b);
             }
             seq_order[rank] = static_cast<int32_t>(b);
